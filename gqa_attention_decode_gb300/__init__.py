@@ -1,0 +1,32 @@
+"""GB300 (sm_103a) grouped-query attention: split-KV decode and causal prefill.
+
+The computation lives in ``libgqa_attn.so`` (CUDA kernels behind the C ABI of
+``include/gqa_attn.h``).  This package is the thin Python binding: it checks
+and marshals torch tensors into the C calls and raises on any non-zero status.
+There is no CPU fallback: if the library is missing, every call raises.
+"""
+from ._binding import (  # noqa: F401
+    GQAError,
+    GQA_OK,
+    GQA_ERR_INVALID_ARG,
+    GQA_ERR_UNSUPPORTED,
+    GQA_ERR_CUDA,
+    GQA_ERR_WORKSPACE,
+    GQA_ERR_TIMEOUT,
+    lib_path,
+    load_library,
+    gqa_status_string,
+    gqa_attn_abi_version,
+    gqa_attn_decode_plan,
+    gqa_attn_decode_workspace_size,
+    gqa_attn_decode,
+    gqa_attn_decode_split,
+    gqa_attn_decode_merge,
+    gqa_attn_prefill_causal,
+    gqa_attn_decode_from_host_arena_size,
+    gqa_attn_decode_from_host,
+    gqa_attn_prefill_causal_from_host_arena_size,
+    gqa_attn_prefill_causal_from_host,
+    gqa_attn_device_status,
+    gqa_attn_selftest_bounded_wait,
+)

@@ -1,0 +1,324 @@
+"""ctypes binding of libgqa_attn.so: argument checks and marshalling, nothing else.
+
+Function names and argument order follow include/gqa_attn.h.  Tensors are torch
+tensors (device memory and streams come from PyTorch); sizes are read from
+their shapes.  Every non-zero status raises GQAError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = 1
+GQA_ERR_UNSUPPORTED = 2
+GQA_ERR_CUDA = 3
+GQA_ERR_WORKSPACE = 4
+GQA_ERR_TIMEOUT = 5
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libgqa_attn.so"
+_lock = threading.Lock()
+_lib = None
+
+_c_int, _c_size, _c_float, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+_ip = ctypes.POINTER(ctypes.c_int)
+
+_SIGNATURES = {
+    "gqa_status_string": (ctypes.c_char_p, [_c_int]),
+    "gqa_attn_abi_version": (_c_int, []),
+    "gqa_attn_decode_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _ip, _ip]),
+    "gqa_attn_decode_workspace_size": (_c_size, [_c_int] * 7),
+    "gqa_attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                 _c_float, _c_int, _vp, _vp, _vp, _c_size, _vp]),
+    "gqa_attn_decode_split": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                       _c_int, _c_float, _c_int, _vp, _c_size, _vp]),
+    "gqa_attn_decode_merge": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                       _vp, _vp, _vp, _c_size, _vp]),
+    "gqa_attn_prefill_causal": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                         _c_int, _c_int, _c_float, _vp, _vp, _vp]),
+    "gqa_attn_decode_from_host_arena_size": (_c_size, [_c_int] * 7),
+    "gqa_attn_decode_from_host": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                           _c_int, _c_float, _c_int, _vp, _vp, _vp, _c_size,
+                                           _vp]),
+    "gqa_attn_prefill_causal_from_host_arena_size": (_c_size, [_c_int] * 6),
+    "gqa_attn_prefill_causal_from_host": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                                   _c_int, _c_int, _c_int, _c_int, _c_float,
+                                                   _vp, _vp, _vp, _c_size, _vp]),
+    "gqa_attn_device_status": (_c_int, [_vp, _ip]),
+    "gqa_attn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
+}
+
+
+class GQAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gqa_status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return os.environ.get("GQA_ATTN_LIB", os.path.join(_PKG_DIR, _LIB_NAME))
+
+
+def load_library() -> ctypes.CDLL:
+    """Loads libgqa_attn.so once; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with "
+                    "`python -m gqa_attention_decode_gb300.build` (needs nvcc)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def gqa_status_string(status: int) -> str:
+    return load_library().gqa_status_string(int(status)).decode()
+
+
+def gqa_attn_abi_version() -> int:
+    return load_library().gqa_attn_abi_version()
+
+
+def _check(status: int, where: str) -> None:
+    if status != GQA_OK:
+        raise GQAError(status, where)
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return _vp(stream.cuda_stream)
+
+
+def _num_sms(device) -> int:
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int, device=None, cuda=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if cuda and t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not cuda and t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _ptr(t):
+    return _vp(t.data_ptr()) if t is not None else _vp(0)
+
+
+# ---------------------------------------------------------------------------
+# decode
+# ---------------------------------------------------------------------------
+
+def gqa_attn_decode_plan(B: int, H_kv: int, S_max: int, num_sms: int, num_splits: int = 0):
+    """(num_splits, chunk) the library will use; host only."""
+    s, c = ctypes.c_int(), ctypes.c_int()
+    _check(load_library().gqa_attn_decode_plan(B, H_kv, S_max, num_sms, num_splits,
+                                               ctypes.byref(s), ctypes.byref(c)),
+           "gqa_attn_decode_plan")
+    return s.value, c.value
+
+
+def gqa_attn_decode_workspace_size(B, H_q, H_kv, S_max, d, num_sms, num_splits=0) -> int:
+    return int(load_library().gqa_attn_decode_workspace_size(B, H_q, H_kv, S_max, d, num_sms,
+                                                             num_splits))
+
+
+def gqa_attn_decode(q, k_cache, v_cache, seqlens, scale, num_splits=0, o=None, lse=None,
+                    workspace=None, stream=None):
+    """Split-KV GQA decode.  q [B,H_q,d] bf16; k_cache, v_cache [B,H_kv,S_max,d] bf16;
+    seqlens [B] int32 (device).  Returns (o [B,H_q,d] bf16, lse [B,H_q] fp32)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    B, H_q, d = q.shape
+    _, H_kv, S_max, _ = k_cache.shape
+    if tuple(k_cache.shape) != (B, H_kv, S_max, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError(f"k_cache/v_cache must be [B,H_kv,S_max,d] = [{B},H_kv,S_max,{d}]")
+    if seqlens.shape[0] != B:
+        raise ValueError("seqlens must have B entries")
+    if o is None:
+        o = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    _need(o, "o", torch.bfloat16, 3, dev)
+    _need(lse, "lse", torch.float32, 2, dev)
+    if workspace is None:
+        nbytes = gqa_attn_decode_workspace_size(B, H_q, H_kv, S_max, d, _num_sms(dev), num_splits)
+        workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, 1, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), B, H_q,
+                                 H_kv, S_max, d, float(scale), int(num_splits), _ptr(o),
+                                 _ptr(lse), _ptr(workspace), workspace.numel(),
+                                 _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_decode")
+    return o, lse
+
+
+def gqa_attn_decode_split(q, k_cache, v_cache, seqlens, scale, num_splits, workspace,
+                          stream=None):
+    """First phase of gqa_attn_decode: per-split partials into `workspace`."""
+    lib = load_library()
+    dev = q.device
+    B, H_q, d = q.shape
+    _, H_kv, S_max, _ = k_cache.shape
+    for t, n, dt, nd in ((q, "q", torch.bfloat16, 3), (k_cache, "k_cache", torch.bfloat16, 4),
+                         (v_cache, "v_cache", torch.bfloat16, 4), (seqlens, "seqlens", torch.int32, 1),
+                         (workspace, "workspace", torch.uint8, 1)):
+        _need(t, n, dt, nd, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_decode_split(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), B,
+                                       H_q, H_kv, S_max, d, float(scale), int(num_splits),
+                                       _ptr(workspace), workspace.numel(),
+                                       _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_decode_split")
+
+
+def gqa_attn_decode_merge(seqlens, H_kv, S_max, num_splits, o, lse, workspace, stream=None):
+    """Second phase of gqa_attn_decode: merge the partials into o and lse."""
+    lib = load_library()
+    dev = o.device
+    B, H_q, d = o.shape
+    for t, n, dt, nd in ((seqlens, "seqlens", torch.int32, 1), (o, "o", torch.bfloat16, 3),
+                         (lse, "lse", torch.float32, 2), (workspace, "workspace", torch.uint8, 1)):
+        _need(t, n, dt, nd, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_decode_merge(_ptr(seqlens), B, H_q, H_kv, S_max, d, int(num_splits),
+                                       _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                       _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_decode_merge")
+
+
+# ---------------------------------------------------------------------------
+# causal prefill
+# ---------------------------------------------------------------------------
+
+def gqa_attn_prefill_causal(q, k, v, scale, q_offset=0, o=None, lse=None, stream=None):
+    """Causal GQA prefill.  q [B,H_q,T_q,d]; k, v [B,H_kv,S_kv,d] (bf16).
+    Row i of q is at absolute position q_offset + i.  Returns (o, lse)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    _need(k, "k", torch.bfloat16, 4, dev)
+    _need(v, "v", torch.bfloat16, 4, dev)
+    B, H_q, T_q, d = q.shape
+    _, H_kv, S_kv, _ = k.shape
+    if tuple(k.shape) != (B, H_kv, S_kv, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k/v must be [B,H_kv,S_kv,d] matching q")
+    if o is None:
+        o = torch.empty((B, H_q, T_q, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=dev)
+    _need(o, "o", torch.bfloat16, 4, dev)
+    _need(lse, "lse", torch.float32, 3, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_prefill_causal(_ptr(q), _ptr(k), _ptr(v), B, H_q, H_kv, T_q, S_kv, d,
+                                         int(q_offset), float(scale), _ptr(o), _ptr(lse),
+                                         _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_prefill_causal")
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# host-buffer variants
+# ---------------------------------------------------------------------------
+
+def gqa_attn_decode_from_host_arena_size(B, H_q, H_kv, S_max, d, num_sms, num_splits=0) -> int:
+    return int(load_library().gqa_attn_decode_from_host_arena_size(B, H_q, H_kv, S_max, d,
+                                                                   num_sms, num_splits))
+
+
+def gqa_attn_decode_from_host(q, k_cache, v_cache, seqlens, scale, num_splits, o, lse, arena,
+                              stream=None):
+    """Decode on CPU (ideally pinned) tensors, staged through the CUDA uint8 `arena`."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3, cuda=False)
+    _need(k_cache, "k_cache", torch.bfloat16, 4, cuda=False)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, cuda=False)
+    _need(seqlens, "seqlens", torch.int32, 1, cuda=False)
+    _need(o, "o", torch.bfloat16, 3, cuda=False)
+    _need(lse, "lse", torch.float32, 2, cuda=False)
+    _need(arena, "arena", torch.uint8, 1)
+    B, H_q, d = q.shape
+    _, H_kv, S_max, _ = k_cache.shape
+    dev = arena.device
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_decode_from_host(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                                           B, H_q, H_kv, S_max, d, float(scale), int(num_splits),
+                                           _ptr(o), _ptr(lse), _ptr(arena), arena.numel(),
+                                           _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_decode_from_host")
+    return o, lse
+
+
+def gqa_attn_prefill_causal_from_host_arena_size(B, H_q, H_kv, T_q, S_kv, d) -> int:
+    return int(load_library().gqa_attn_prefill_causal_from_host_arena_size(B, H_q, H_kv, T_q,
+                                                                           S_kv, d))
+
+
+def gqa_attn_prefill_causal_from_host(q, k, v, scale, q_offset, o, lse, arena, stream=None):
+    """Causal prefill on CPU (ideally pinned) tensors, staged through the CUDA `arena`."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 4, cuda=False)
+    _need(k, "k", torch.bfloat16, 4, cuda=False)
+    _need(v, "v", torch.bfloat16, 4, cuda=False)
+    _need(o, "o", torch.bfloat16, 4, cuda=False)
+    _need(lse, "lse", torch.float32, 3, cuda=False)
+    _need(arena, "arena", torch.uint8, 1)
+    B, H_q, T_q, d = q.shape
+    _, H_kv, S_kv, _ = k.shape
+    dev = arena.device
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_prefill_causal_from_host(_ptr(q), _ptr(k), _ptr(v), B, H_q, H_kv, T_q,
+                                                   S_kv, d, int(q_offset), float(scale), _ptr(o),
+                                                   _ptr(lse), _ptr(arena), arena.numel(),
+                                                   _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_prefill_causal_from_host")
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# diagnostics
+# ---------------------------------------------------------------------------
+
+def gqa_attn_device_status(stream=None, device=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status word."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    out = ctypes.c_int(-1)
+    with torch.cuda.device(dev):
+        _check(load_library().gqa_attn_device_status(_stream_handle(stream, dev),
+                                                     ctypes.byref(out)),
+               "gqa_attn_device_status")
+    return out.value
+
+
+def gqa_attn_selftest_bounded_wait(timeout_us: int, stream=None, device=None) -> None:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(load_library().gqa_attn_selftest_bounded_wait(int(timeout_us),
+                                                             _stream_handle(stream, dev)),
+               "gqa_attn_selftest_bounded_wait")

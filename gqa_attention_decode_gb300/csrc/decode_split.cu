@@ -1,0 +1,375 @@
+// decode_split.cu -- split-KV GQA decode for sm_103a.
+//
+// What it computes (design record "ADR-0060: AHBM GQA Fused Attention Kernel
+// (Llama3-70B)"): for one sequence b and one KV head, the G = H_q / H_kv query
+// heads that share that KV head are stacked into one matrix product (the
+// record's "M-fold", TL;DR "Kernel 1" and section 5.2), so each K/V tile is read
+// from HBM once for all G heads.  The key range of the head is cut into
+// contiguous chunks (section 2.1, contiguous-block placement); each CTA runs the
+// per-tile online softmax of section 3 over its chunk and writes a partial
+// (O_s / l_s, lse_s).  A second kernel merges the partials with the
+// log-sum-exp merge of section 4.
+//
+// GB300 mapping
+//   * grid (num_splits, H_kv, B); 5 warps: warp 4 issues TMA loads of 64-key
+//     K/V tiles (128B-swizzled, 4D tensor maps so tiles never cross a head)
+//     into a 3-stage shared-memory ring; warps 0..3 consume every tile.
+//   * The fold puts the G (<= 8) heads in the N = 8 dimension of
+//     mma.sync m16n8k16 (bf16 in, fp32 accumulate): S^T[16 keys x 8 heads] =
+//     K[16 x 128] Q^T, so no MMA lane is wasted on padding; P^T is moved into
+//     the B-operand layout with movmatrix and O^T[128 x 8] += V^T P^T reads V
+//     with ldmatrix.trans.
+//   * Warp w owns keys [16w, 16w+16) of every tile and keeps its own running
+//     (m, l, O); the four warp states are merged once per CTA, so no
+//     cross-warp synchronisation sits in the tile loop.
+//   * Decode moves 8 flop per byte of K/V, far below the tensor-core ridge;
+//     the kernel is HBM bound and everything else exists to keep enough bytes
+//     in flight (two CTAs per SM x 3 stages x 32 KiB).
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace gqa {
+namespace decode {
+
+constexpr int kD = 128;
+constexpr int kTileKeys = kDecodeTileKeys;          // 64
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 160
+constexpr int kHalfBytes = kTileKeys * 128;          // 64 keys x 64 d x 2 B = 8 KiB
+constexpr int kStageBytes = 4 * kHalfBytes;          // K lo/hi + V lo/hi = 32 KiB
+constexpr int kBarrierBytes = 2 * kStages * 8;
+constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // + alignment slack
+constexpr int kRedStride = kD + 4;  // padded row of the per-warp O reduction buffer
+
+struct Params {
+  const uint16_t *q;
+  const int32_t *seqlens;
+  float *o_part;
+  float *lse_part;
+  int B, H_q, H_kv, G, S_max, num_splits, chunk;
+  float scale_log2;  // scale * log2(e)
+  WaitCtl wait;
+};
+
+__device__ __forceinline__ uint32_t mask_pair(uint32_t x, bool lo_ok, bool hi_ok) {
+  return (lo_ok ? 0x0000FFFFu : 0u) & x | ((hi_ok ? 0xFFFF0000u : 0u) & x);
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..15 across d) of key row `r` inside one
+// K or V tile as TMA writes it: two 64-column halves, each [64 rows x 128 B]
+// with the 128B swizzle (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t tile_offset(int r, int chunk) {
+  const int half = chunk >> 3, c = chunk & 7;
+  return half * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+  uint64_t *empty_bar = full_bar + kStages;
+
+  const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  const int seqlen = min(max(p.seqlens[b], 0), p.S_max);
+  const int key_begin = split * p.chunk;
+  const int key_end = min(key_begin + p.chunk, seqlen);
+  if (key_begin >= key_end) return;  // empty split: the merge never reads it
+  const int n_tiles = (key_end - key_begin + kTileKeys - 1) / kTileKeys;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int failed;
+  if (threadIdx.x == 0) {
+    failed = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  float m_run[2], l_run[2], o_acc[8][4];
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: one thread issues all TMA loads ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol = l2_policy_evict_first();
+      const int row = b * p.H_kv + kv;
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, p.wait)) break;
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        const uint32_t dst = smem_u32(smem + s * kStageBytes);
+        const int key0 = key_begin + i * kTileKeys;
+        tma_load_4d(dst + 0 * kHalfBytes, &tm_k, fb, 0, 0, key0, row, pol);
+        tma_load_4d(dst + 1 * kHalfBytes, &tm_k, fb, 0, 1, key0, row, pol);
+        tma_load_4d(dst + 2 * kHalfBytes, &tm_v, fb, 0, 0, key0, row, pol);
+        tma_load_4d(dst + 3 * kHalfBytes, &tm_v, fb, 0, 1, key0, row, pol);
+        ++issued;
+      }
+      // Never leave the CTA with a copy in flight: wait for the last loads.
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1, p.wait);
+      if (issued < n_tiles) atomicExch(&failed, 1);
+    }
+  } else {
+    // ---------------- consumers: warps 0..3 ----------------
+    const int g = lane >> 2, t = lane & 3;
+    // Q^T as the B operand: b0 = Q[head g][16kk + 2t .. +1], b1 = the same + 8.
+    uint32_t qf[8][2];
+    {
+      const bool head_ok = g < p.G;
+      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+          p.q + ((size_t)b * p.H_q + (size_t)kv * p.G + (head_ok ? g : 0)) * kD);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qf[kk][0] = head_ok ? __ldg(qrow + kk * 8 + t) : 0u;
+        qf[kk][1] = head_ok ? __ldg(qrow + kk * 8 + 4 + t) : 0u;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) { m_run[j] = -INFINITY; l_run[j] = 0.f; }
+#pragma unroll
+    for (int md = 0; md < 8; ++md)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o_acc[md][j] = 0.f;
+
+    const int key_w0 = 16 * warp;  // this warp's keys inside a tile
+    // ldmatrix lane roles (see the fragment layouts of mma.m16n8k16)
+    const int k_row = key_w0 + (lane & 15), k_chunk_hi = lane >> 4;
+    const int v_row = key_w0 + (lane & 7) + ((lane >> 4) << 3), v_chunk_hi = (lane >> 3) & 1;
+    const float sl2 = p.scale_log2;
+
+    for (int i = 0; i < n_tiles; ++i) {
+      const int s = i % kStages;
+      // every lane waits (acquiring the TMA data); the verdict is made warp-uniform
+      const bool ready = mbar_wait(smem_u32(&full_bar[s]), (i / kStages) & 1, p.wait);
+      if (!__all_sync(0xffffffffu, ready)) {
+        if (lane == 0) atomicExch(&failed, 1);
+        break;
+      }
+      const uint32_t kbase = smem_u32(smem + s * kStageBytes);
+      const uint32_t vbase = kbase + 2 * kHalfBytes;
+      const int tile_key0 = key_begin + i * kTileKeys;
+
+      // S^T[16 keys x 8 heads] = K[16 x 128] * Q^T[128 x 8]
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kbase + tile_offset(k_row, 2 * kk + k_chunk_hi), a0, a1, a2, a3);
+        mma_bf16_16816(sacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+      }
+      // scale into the log2 domain; keys past the end of the split are -inf
+      float sc[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[j] = sacc[j] * sl2;
+      const bool tail = tile_key0 + kTileKeys > key_end;
+      if (tail) {
+        const int k_lo = tile_key0 + key_w0 + g, k_hi = k_lo + 8;
+        if (k_lo >= key_end) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+        if (k_hi >= key_end) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+      }
+      // online softmax; thread holds heads 2t (j=0) and 2t+1 (j=1)
+      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+      const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      const float p0 = fast_exp2(sc[0] - ref0), p1 = fast_exp2(sc[1] - ref1);
+      const float p2 = fast_exp2(sc[2] - ref0), p3 = fast_exp2(sc[3] - ref1);
+      const float c0 = fast_exp2(m_run[0] - ref0), c1 = fast_exp2(m_run[1] - ref1);
+      l_run[0] = l_run[0] * c0 + p0 + p2;
+      l_run[1] = l_run[1] * c1 + p1 + p3;
+      m_run[0] = mn0;
+      m_run[1] = mn1;
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        o_acc[md][0] *= c0; o_acc[md][1] *= c1;
+        o_acc[md][2] *= c0; o_acc[md][3] *= c1;
+      }
+      // P^T in the B-operand layout: rows (keys g, g+8) x cols (heads 2t, 2t+1)
+      // transposed to keys (2t, 2t+1) [+8] x head g.
+      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+      // rows of V past the end are zeroed so stale or NaN cache bytes never
+      // meet a zero probability
+      bool lo0 = true, lo1 = true, hi0 = true, hi1 = true;
+      if (tail) {
+        const int kb = tile_key0 + key_w0 + 2 * t;
+        lo0 = kb < key_end; lo1 = kb + 1 < key_end;
+        hi0 = kb + 8 < key_end; hi1 = kb + 9 < key_end;
+      }
+      // O^T[128 x 8] += V^T[128 x 16 keys] * P^T[16 keys x 8]
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(vbase + tile_offset(v_row, 2 * md + v_chunk_hi), a0, a1, a2, a3);
+        if (tail) {
+          a0 = mask_pair(a0, lo0, lo1); a1 = mask_pair(a1, lo0, lo1);
+          a2 = mask_pair(a2, hi0, hi1); a3 = mask_pair(a3, hi0, hi1);
+        }
+        mma_bf16_16816(o_acc[md], a0, a1, a2, a3, pb0, pb1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+    }
+    // per-thread partial sums over the 8 lanes that share heads 2t, 2t+1
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+      l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+    }
+  }
+  __syncthreads();
+  if (failed) return;
+
+  // ---------------- merge the four warp states, write the split partial ----------------
+  // All loads have landed and been consumed; the stage ring is free.
+  float *red_m = reinterpret_cast<float *>(smem);              // [4][8]
+  float *red_l = red_m + kConsumerWarps * 8;                   // [4][8]
+  float *red_o = red_l + kConsumerWarps * 8;                   // [4][8][kRedStride]
+  if (warp < kConsumerWarps) {
+    const int g = lane >> 2, t = lane & 3;
+    if (g == 0) {
+      red_m[warp * 8 + 2 * t] = m_run[0];
+      red_m[warp * 8 + 2 * t + 1] = m_run[1];
+      red_l[warp * 8 + 2 * t] = l_run[0];
+      red_l[warp * 8 + 2 * t + 1] = l_run[1];
+    }
+    float *ow = red_o + warp * 8 * kRedStride;
+#pragma unroll
+    for (int md = 0; md < 8; ++md) {
+      ow[(2 * t) * kRedStride + 16 * md + g] = o_acc[md][0];
+      ow[(2 * t + 1) * kRedStride + 16 * md + g] = o_acc[md][1];
+      ow[(2 * t) * kRedStride + 16 * md + g + 8] = o_acc[md][2];
+      ow[(2 * t + 1) * kRedStride + 16 * md + g + 8] = o_acc[md][3];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < kD) {
+    const int dd = threadIdx.x;
+    for (int n = 0; n < p.G; ++n) {
+      float mmax = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) mmax = fmaxf(mmax, red_m[w * 8 + n]);
+      float lsum = 0.f, osum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float f = fast_exp2(red_m[w * 8 + n] - mmax);  // warps without keys: 0
+        lsum += red_l[w * 8 + n] * f;
+        osum += red_o[(w * 8 + n) * kRedStride + dd] * f;
+      }
+      const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + n) * p.num_splits + split;
+      p.o_part[row * kD + dd] = osum / lsum;
+      if (dd == 0) p.lse_part[row] = mmax * 0.69314718055994531f + logf(lsum);
+    }
+  }
+}
+
+// One CTA per (query head, sequence); thread = one of the d = 128 columns.
+// lse = max_s lse_s + ln sum_s exp(lse_s - max); O = sum_s exp(lse_s - lse) O_s.
+__global__ void __launch_bounds__(kD)
+    decode_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
+                        const int32_t *__restrict__ seqlens, uint16_t *__restrict__ o,
+                        float *__restrict__ lse, int H_q, int S_max, int num_splits, int chunk) {
+  const int h = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
+  const int seqlen = min(max(seqlens[b], 0), S_max);
+  const int ns = min((seqlen + chunk - 1) / chunk, num_splits);
+  const size_t row = (size_t)b * H_q + h;
+  if (ns == 0) {  // no visible key
+    o[row * kD + dd] = 0;
+    if (dd == 0) lse[row] = -INFINITY;
+    return;
+  }
+  const float *lp = lse_part + row * num_splits;
+  const float *op = o_part + row * num_splits * kD + dd;
+  float mx = -INFINITY;
+  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, lp[s]);
+  constexpr float kLog2e = 1.4426950408889634f;
+  float wsum = 0.f, acc = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float w = fast_exp2((lp[s] - mx) * kLog2e);
+    wsum += w;
+    acc = fmaf(w, op[(size_t)s * kD], acc);
+  }
+  const __nv_bfloat16 r = __float2bfloat16_rn(acc / wsum);
+  o[row * kD + dd] = *reinterpret_cast<const uint16_t *>(&r);
+  if (dd == 0) lse[row] = mx + logf(wsum);
+}
+
+static CUresult make_kv_map(CUtensorMap *map, const uint16_t *base, int B, int H_kv, int S_max,
+                            PFN_cuTensorMapEncodeTiled_v12000 encode) {
+  // dims (innermost first): 64 columns, 2 column halves, S_max keys, B*H_kv heads
+  const cuuint64_t dims[4] = {64, 2, (cuuint64_t)S_max, (cuuint64_t)B * H_kv};
+  const cuuint64_t strides[3] = {128, 256, (cuuint64_t)S_max * 256};  // bytes, dims 1..3
+  const cuuint32_t box[4] = {64, 1, kTileKeys, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(base), dims,
+                strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace decode
+
+cudaError_t decode_prepare_device() {
+  return cudaFuncSetAttribute(decode::decode_split_kernel,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, decode::kSmemBytes);
+}
+
+cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
+                                PFN_cuTensorMapEncodeTiled_v12000 encode) {
+  using namespace decode;
+  if (a.S_max > 0) {
+    CUtensorMap tm_k, tm_v;
+    if (make_kv_map(&tm_k, a.k_cache, a.B, a.H_kv, a.S_max, encode) != CUDA_SUCCESS ||
+        make_kv_map(&tm_v, a.v_cache, a.B, a.H_kv, a.S_max, encode) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    Params p;
+    p.q = a.q;
+    p.seqlens = a.seqlens;
+    p.o_part = a.o_part;
+    p.lse_part = a.lse_part;
+    p.B = a.B;
+    p.H_q = a.H_q;
+    p.H_kv = a.H_kv;
+    p.G = a.H_q / a.H_kv;
+    p.S_max = a.S_max;
+    p.num_splits = a.num_splits;
+    p.chunk = a.chunk;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.wait = a.wait;
+    dim3 grid(a.num_splits, a.H_kv, a.B);
+    decode_split_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_v, p);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream) {
+  using namespace decode;
+  dim3 mgrid(a.H_q, a.B);
+  decode_merge_kernel<<<mgrid, kD, 0, stream>>>(a.o_part, a.lse_part, a.seqlens, a.o, a.lse,
+                                                a.H_q, a.S_max, a.num_splits,
+                                                a.chunk > 0 ? a.chunk : 1);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

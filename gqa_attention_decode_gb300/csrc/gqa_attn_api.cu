@@ -1,0 +1,460 @@
+// gqa_attn_api.cu -- the extern "C" boundary: argument checks, the decode split
+// planner, per-device set-up, host-buffer staging and diagnostics.  Every
+// numerical step runs in the kernels of decode_split.cu and prefill_causal.cu.
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/gqa_attn.h"
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// Status word written by bounded waits that run out (one per device, in the
+// library's static device memory; read and cleared by gqa_attn_device_status).
+__device__ int g_wait_status;
+
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxDevices = 64;
+constexpr int kMaxChunkTiles = 32;  // automatic plan: at most 2048 keys per split
+constexpr int kDecodeCtasPerSm = 2;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int *status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA; }
+
+// Per-device set-up on first use: SM count, the status word's device address,
+// kernel attributes, and the driver's tensor-map encoder (fetched through the
+// runtime so the library never links libcuda directly).
+int device_state(DeviceState **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState &st = g_devices[dev];
+  if (!st.ready) {
+    if (!g_encode) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return GQA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    void *status = nullptr;
+    if (cudaGetSymbolAddress(&status, g_wait_status) != cudaSuccess) return GQA_ERR_CUDA;
+    if (gqa::decode_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
+    if (gqa::prefill_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
+    st.num_sms = sms;
+    st.status = static_cast<int *>(status);
+    st.ready = true;
+  }
+  *out = &st;
+  return GQA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Plan: chunks of whole 64-key tiles.  Automatic: enough splits that one wave
+// of kDecodeCtasPerSm CTAs per SM covers B*H_kv*splits, but no chunk longer
+// than kMaxChunkTiles tiles (long caches then run several waves, which keeps
+// ragged batches balanced).
+int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_splits,
+         int *out_chunk) {
+  if (B < 0 || H_kv <= 0 || S_max < 0 || num_sms <= 0 || num_splits < 0) return GQA_ERR_INVALID_ARG;
+  const int tile = gqa::kDecodeTileKeys;
+  const int tiles = ceil_div(S_max, tile);
+  if (tiles == 0 || B == 0) {
+    *out_splits = 1;
+    *out_chunk = tile;
+    return GQA_OK;
+  }
+  int chunk_tiles;
+  if (num_splits > 0) {
+    chunk_tiles = ceil_div(tiles, num_splits < tiles ? num_splits : tiles);
+  } else {
+    const long long units = (long long)B * H_kv;
+    const long long want = (long long)num_sms * kDecodeCtasPerSm;
+    const int fill = static_cast<int>((want + units - 1) / units);  // splits per unit
+    chunk_tiles = ceil_div(tiles, fill < 1 ? 1 : fill);
+    if (chunk_tiles > kMaxChunkTiles) chunk_tiles = kMaxChunkTiles;
+    if (chunk_tiles < 1) chunk_tiles = 1;
+  }
+  *out_splits = ceil_div(tiles, chunk_tiles);
+  *out_chunk = chunk_tiles * tile;
+  return GQA_OK;
+}
+
+size_t decode_ws_bytes(int B, int H_q, int splits, int d) {
+  return round256((size_t)B * H_q * splits * (size_t)(d + 1) * sizeof(float));
+}
+
+enum DecodePhase { kPhaseSplit = 1, kPhaseMerge = 2, kPhaseBoth = 3 };
+
+bool finite_scale(float scale) {
+  return scale == scale && scale != __builtin_inff() && scale != -__builtin_inff();
+}
+
+// Checks the decode arguments a phase uses; pointers a phase does not use may
+// be null.
+int check_decode_args(int phase, const void *q, const void *k, const void *v,
+                      const void *seqlens, int B, int H_q, int H_kv, int S_max, int d,
+                      float scale, int num_splits, const void *o, const void *lse) {
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || S_max < 0 || d <= 0 || num_splits < 0)
+    return GQA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (!finite_scale(scale)) return GQA_ERR_INVALID_ARG;
+  if (B == 0) return GQA_OK;
+  if (!seqlens || !aligned16(seqlens)) return GQA_ERR_INVALID_ARG;
+  if (phase & kPhaseSplit) {
+    if (!q || !k || !v) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return GQA_ERR_INVALID_ARG;
+  }
+  if (phase & kPhaseMerge) {
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return GQA_ERR_INVALID_ARG;
+  }
+  if (d != 128) return GQA_ERR_UNSUPPORTED;
+  if (H_q / H_kv > gqa::kDecodeMaxG) return GQA_ERR_UNSUPPORTED;
+  if (B > 65535 || H_kv > 65535) return GQA_ERR_UNSUPPORTED;  // grid y/z limits
+  return GQA_OK;
+}
+
+int check_prefill_args(const void *q, const void *k, const void *v, int B, int H_q, int H_kv,
+                       int T_q, int S_kv, int d, int q_offset, float scale, const void *o,
+                       const void *lse) {
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0)
+    return GQA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if ((long long)q_offset + T_q > S_kv) return GQA_ERR_INVALID_ARG;
+  if (!finite_scale(scale)) return GQA_ERR_INVALID_ARG;
+  if (B == 0 || T_q == 0) return GQA_OK;
+  if (!q || !k || !v || !o || !lse) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return GQA_ERR_INVALID_ARG;
+  if (d != 128) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+__global__ void selftest_wait_kernel(gqa::WaitCtl wait) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    gqa::mbar_init(gqa::smem_u32(&bar), 1);
+    gqa::fence_mbar_init();
+  }
+  __syncthreads();
+  // Nobody arrives: the wait must give up on its own and record the timeout.
+  if (threadIdx.x == 0) gqa::mbar_wait(gqa::smem_u32(&bar), 0, wait);
+  __syncthreads();
+}
+
+}  // namespace
+
+namespace gqa {
+cudaError_t selftest_bounded_wait_launch(WaitCtl wait, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(wait);
+  return cudaGetLastError();
+}
+}  // namespace gqa
+
+extern "C" {
+
+GQA_API const char *gqa_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG: invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: unsupported shape";
+    case GQA_ERR_CUDA: return "GQA_ERR_CUDA: CUDA call failed";
+    case GQA_ERR_WORKSPACE: return "GQA_ERR_WORKSPACE: workspace too small";
+    case GQA_ERR_TIMEOUT: return "GQA_ERR_TIMEOUT: bounded device wait ran out";
+    default: return "unknown gqa status";
+  }
+}
+
+GQA_API int gqa_attn_abi_version(void) { return GQA_ATTN_ABI_VERSION; }
+
+GQA_API int gqa_attn_decode_plan(int B, int H_kv, int S_max, int num_sms, int num_splits,
+                                 int *out_num_splits, int *out_chunk) {
+  if (!out_num_splits || !out_chunk) return GQA_ERR_INVALID_ARG;
+  return plan(B, H_kv, S_max, num_sms, num_splits, out_num_splits, out_chunk);
+}
+
+GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_max, int d,
+                                              int num_sms, int num_splits) {
+  int splits = 0, chunk = 0;
+  if (H_q <= 0 || d <= 0 || plan(B, H_kv, S_max, num_sms, num_splits, &splits, &chunk) != GQA_OK)
+    return 0;
+  return decode_ws_bytes(B, H_q, splits, d);
+}
+
+}  // extern "C"
+
+namespace {
+int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
+                 const gqa_bf16_t *v_cache, const int32_t *seqlens, int B, int H_q, int H_kv,
+                 int S_max, int d, float scale, int num_splits, gqa_bf16_t *o, float *lse,
+                 const void *workspace, size_t ws_bytes, gqa_stream_t stream) {
+  int rc = check_decode_args(phase, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
+                             num_splits, o, lse);
+  if (rc != GQA_OK || B == 0) return rc;
+  DeviceState *st = nullptr;
+  if ((rc = device_state(&st)) != GQA_OK) return rc;
+  int splits = 0, chunk = 0;
+  if ((rc = plan(B, H_kv, S_max, st->num_sms, num_splits, &splits, &chunk)) != GQA_OK) return rc;
+  const size_t need = decode_ws_bytes(B, H_q, splits, d);
+  if (!workspace || ws_bytes < need) return GQA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return GQA_ERR_INVALID_ARG;
+
+  gqa::DecodeLaunch a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.seqlens = seqlens;
+  a.B = B;
+  a.H_q = H_q;
+  a.H_kv = H_kv;
+  a.S_max = S_max;
+  a.num_splits = splits;
+  a.chunk = chunk;
+  a.scale = scale;
+  a.o = o;
+  a.lse = lse;
+  a.o_part = static_cast<float *>(const_cast<void *>(workspace));
+  a.lse_part = a.o_part + (size_t)B * H_q * splits * d;
+  a.wait.status = st->status;
+  a.wait.timeout_ns = kWaitTimeoutNs;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (phase & kPhaseSplit) {
+    if (gqa::decode_split_launch(a, s, g_encode) != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  if (phase & kPhaseMerge) {
+    if (gqa::decode_merge_launch(a, s) != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
+                            const gqa_bf16_t *v_cache, const int32_t *seqlens, int B,
+                            int H_q, int H_kv, int S_max, int d, float scale, int num_splits,
+                            gqa_bf16_t *o, float *lse, void *workspace, size_t ws_bytes,
+                            gqa_stream_t stream) {
+  return decode_phase(kPhaseBoth, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
+                      num_splits, o, lse, workspace, ws_bytes, stream);
+}
+
+GQA_API int gqa_attn_decode_split(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
+                                  const gqa_bf16_t *v_cache, const int32_t *seqlens, int B,
+                                  int H_q, int H_kv, int S_max, int d, float scale,
+                                  int num_splits, void *workspace, size_t ws_bytes,
+                                  gqa_stream_t stream) {
+  return decode_phase(kPhaseSplit, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
+                      num_splits, nullptr, nullptr, workspace, ws_bytes, stream);
+}
+
+GQA_API int gqa_attn_decode_merge(const int32_t *seqlens, int B, int H_q, int H_kv, int S_max,
+                                  int d, int num_splits, gqa_bf16_t *o, float *lse,
+                                  const void *workspace, size_t ws_bytes, gqa_stream_t stream) {
+  return decode_phase(kPhaseMerge, nullptr, nullptr, nullptr, seqlens, B, H_q, H_kv, S_max, d,
+                      1.0f, num_splits, o, lse, workspace, ws_bytes, stream);
+}
+
+GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
+                                    const gqa_bf16_t *v, int B, int H_q, int H_kv, int T_q,
+                                    int S_kv, int d, int q_offset, float scale, gqa_bf16_t *o,
+                                    float *lse, gqa_stream_t stream) {
+  int rc = check_prefill_args(q, k, v, B, H_q, H_kv, T_q, S_kv, d, q_offset, scale, o, lse);
+  if (rc != GQA_OK || B == 0 || T_q == 0) return rc;
+  DeviceState *st = nullptr;
+  if ((rc = device_state(&st)) != GQA_OK) return rc;
+  gqa::PrefillLaunch a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.B = B;
+  a.H_q = H_q;
+  a.H_kv = H_kv;
+  a.T_q = T_q;
+  a.S_kv = S_kv;
+  a.q_offset = q_offset;
+  a.scale = scale;
+  a.o = o;
+  a.lse = lse;
+  a.num_sms = st->num_sms;
+  a.wait.status = st->status;
+  a.wait.timeout_ns = kWaitTimeoutNs;
+  cudaError_t e = gqa::prefill_launch(a, static_cast<cudaStream_t>(stream), g_encode);
+  if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+  return to_status(e);
+}
+
+// ---- host-buffer variants ------------------------------------------------------
+
+namespace {
+struct DecodeArena {
+  size_t q, k, v, seqlens, o, lse, ws, total;
+};
+DecodeArena decode_arena_layout(int B, int H_q, int H_kv, int S_max, int d, size_t ws) {
+  DecodeArena a;
+  size_t off = 0;
+  a.q = off; off += round256((size_t)B * H_q * d * 2);
+  a.k = off; off += round256((size_t)B * H_kv * S_max * d * 2);
+  a.v = off; off += round256((size_t)B * H_kv * S_max * d * 2);
+  a.seqlens = off; off += round256((size_t)B * 4);
+  a.o = off; off += round256((size_t)B * H_q * d * 2);
+  a.lse = off; off += round256((size_t)B * H_q * 4);
+  a.ws = off; off += round256(ws);
+  a.total = off;
+  return a;
+}
+}  // namespace
+
+GQA_API size_t gqa_attn_decode_from_host_arena_size(int B, int H_q, int H_kv, int S_max, int d,
+                                                    int num_sms, int num_splits) {
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || S_max < 0 || d <= 0) return 0;
+  const size_t ws = gqa_attn_decode_workspace_size(B, H_q, H_kv, S_max, d, num_sms, num_splits);
+  if (ws == 0 && B > 0) return 0;
+  return decode_arena_layout(B, H_q, H_kv, S_max, d, ws).total;
+}
+
+GQA_API int gqa_attn_decode_from_host(const gqa_bf16_t *q_host, const gqa_bf16_t *k_cache_host,
+                                      const gqa_bf16_t *v_cache_host,
+                                      const int32_t *seqlens_host, int B, int H_q, int H_kv,
+                                      int S_max, int d, float scale, int num_splits,
+                                      gqa_bf16_t *o_host, float *lse_host, void *device_arena,
+                                      size_t arena_bytes, gqa_stream_t stream) {
+  int rc = check_decode_args(kPhaseBoth, q_host, k_cache_host, v_cache_host, seqlens_host, B,
+                             H_q, H_kv, S_max, d, scale, num_splits, o_host, lse_host);
+  if (rc != GQA_OK || B == 0) return rc;
+  DeviceState *st = nullptr;
+  if ((rc = device_state(&st)) != GQA_OK) return rc;
+  const size_t ws = gqa_attn_decode_workspace_size(B, H_q, H_kv, S_max, d, st->num_sms, num_splits);
+  const DecodeArena L = decode_arena_layout(B, H_q, H_kv, S_max, d, ws);
+  if (!device_arena || arena_bytes < L.total) return GQA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(device_arena) & 255u) != 0) return GQA_ERR_INVALID_ARG;
+  char *base = static_cast<char *>(device_arena);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t kv_bytes = (size_t)B * H_kv * S_max * d * 2;
+  if (cudaMemcpyAsync(base + L.q, q_host, (size_t)B * H_q * d * 2, cudaMemcpyHostToDevice, s) ||
+      cudaMemcpyAsync(base + L.k, k_cache_host, kv_bytes, cudaMemcpyHostToDevice, s) ||
+      cudaMemcpyAsync(base + L.v, v_cache_host, kv_bytes, cudaMemcpyHostToDevice, s) ||
+      cudaMemcpyAsync(base + L.seqlens, seqlens_host, (size_t)B * 4, cudaMemcpyHostToDevice, s))
+    return GQA_ERR_CUDA;
+  rc = gqa_attn_decode(reinterpret_cast<gqa_bf16_t *>(base + L.q),
+                       reinterpret_cast<gqa_bf16_t *>(base + L.k),
+                       reinterpret_cast<gqa_bf16_t *>(base + L.v),
+                       reinterpret_cast<int32_t *>(base + L.seqlens), B, H_q, H_kv, S_max, d,
+                       scale, num_splits, reinterpret_cast<gqa_bf16_t *>(base + L.o),
+                       reinterpret_cast<float *>(base + L.lse), base + L.ws, ws, stream);
+  if (rc != GQA_OK) return rc;
+  if (cudaMemcpyAsync(o_host, base + L.o, (size_t)B * H_q * d * 2, cudaMemcpyDeviceToHost, s) ||
+      cudaMemcpyAsync(lse_host, base + L.lse, (size_t)B * H_q * 4, cudaMemcpyDeviceToHost, s))
+    return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+namespace {
+struct PrefillArena {
+  size_t q, k, v, o, lse, total;
+};
+PrefillArena prefill_arena_layout(int B, int H_q, int H_kv, int T_q, int S_kv, int d) {
+  PrefillArena a;
+  size_t off = 0;
+  a.q = off; off += round256((size_t)B * H_q * T_q * d * 2);
+  a.k = off; off += round256((size_t)B * H_kv * S_kv * d * 2);
+  a.v = off; off += round256((size_t)B * H_kv * S_kv * d * 2);
+  a.o = off; off += round256((size_t)B * H_q * T_q * d * 2);
+  a.lse = off; off += round256((size_t)B * H_q * T_q * 4);
+  a.total = off;
+  return a;
+}
+}  // namespace
+
+GQA_API size_t gqa_attn_prefill_causal_from_host_arena_size(int B, int H_q, int H_kv, int T_q,
+                                                            int S_kv, int d) {
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0) return 0;
+  return prefill_arena_layout(B, H_q, H_kv, T_q, S_kv, d).total;
+}
+
+GQA_API int gqa_attn_prefill_causal_from_host(const gqa_bf16_t *q_host, const gqa_bf16_t *k_host,
+                                              const gqa_bf16_t *v_host, int B, int H_q,
+                                              int H_kv, int T_q, int S_kv, int d, int q_offset,
+                                              float scale, gqa_bf16_t *o_host, float *lse_host,
+                                              void *device_arena, size_t arena_bytes,
+                                              gqa_stream_t stream) {
+  int rc = check_prefill_args(q_host, k_host, v_host, B, H_q, H_kv, T_q, S_kv, d, q_offset,
+                              scale, o_host, lse_host);
+  if (rc != GQA_OK || B == 0 || T_q == 0) return rc;
+  const PrefillArena L = prefill_arena_layout(B, H_q, H_kv, T_q, S_kv, d);
+  if (!device_arena || arena_bytes < L.total) return GQA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(device_arena) & 255u) != 0) return GQA_ERR_INVALID_ARG;
+  char *base = static_cast<char *>(device_arena);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t q_bytes = (size_t)B * H_q * T_q * d * 2;
+  const size_t kv_bytes = (size_t)B * H_kv * S_kv * d * 2;
+  if (cudaMemcpyAsync(base + L.q, q_host, q_bytes, cudaMemcpyHostToDevice, s) ||
+      cudaMemcpyAsync(base + L.k, k_host, kv_bytes, cudaMemcpyHostToDevice, s) ||
+      cudaMemcpyAsync(base + L.v, v_host, kv_bytes, cudaMemcpyHostToDevice, s))
+    return GQA_ERR_CUDA;
+  rc = gqa_attn_prefill_causal(reinterpret_cast<gqa_bf16_t *>(base + L.q),
+                               reinterpret_cast<gqa_bf16_t *>(base + L.k),
+                               reinterpret_cast<gqa_bf16_t *>(base + L.v), B, H_q, H_kv, T_q,
+                               S_kv, d, q_offset, scale,
+                               reinterpret_cast<gqa_bf16_t *>(base + L.o),
+                               reinterpret_cast<float *>(base + L.lse), stream);
+  if (rc != GQA_OK) return rc;
+  if (cudaMemcpyAsync(o_host, base + L.o, q_bytes, cudaMemcpyDeviceToHost, s) ||
+      cudaMemcpyAsync(lse_host, base + L.lse, (size_t)B * H_q * T_q * 4, cudaMemcpyDeviceToHost,
+                      s))
+    return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+// ---- diagnostics ------------------------------------------------------------------
+
+GQA_API int gqa_attn_device_status(gqa_stream_t stream, int *out_status) {
+  if (!out_status) return GQA_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int rc = device_state(&st);
+  if (rc != GQA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GQA_ERR_CUDA;
+  int value = 0;
+  if (cudaMemcpy(&value, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(st->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  *out_status = value;
+  return GQA_OK;
+}
+
+GQA_API int gqa_attn_selftest_bounded_wait(int timeout_us, gqa_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return GQA_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int rc = device_state(&st);
+  if (rc != GQA_OK) return rc;
+  gqa::WaitCtl w;
+  w.status = st->status;
+  w.timeout_ns = (uint64_t)timeout_us * 1000ull;
+  return to_status(gqa::selftest_bounded_wait_launch(w, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// kernels.h -- host-side launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+
+namespace gqa {
+
+// ---- decode ----------------------------------------------------------------
+struct DecodeLaunch {
+  const uint16_t *q;        // [B, H_q, d]
+  const uint16_t *k_cache;  // [B, H_kv, S_max, d]
+  const uint16_t *v_cache;  // [B, H_kv, S_max, d]
+  const int32_t *seqlens;   // [B]
+  int B, H_q, H_kv, S_max, num_splits, chunk;
+  float scale;
+  uint16_t *o;      // [B, H_q, d]
+  float *lse;       // [B, H_q]
+  float *o_part;    // [B, H_q, num_splits, d]
+  float *lse_part;  // [B, H_q, num_splits]
+  WaitCtl wait;
+};
+
+constexpr int kDecodeTileKeys = 64;  // keys per pipeline stage
+constexpr int kDecodeMaxG = 8;       // query heads per KV head that fit the MMA N dimension
+
+// One-time per-device kernel attributes (dynamic shared memory opt-in).
+cudaError_t decode_prepare_device();
+// Encodes the tensor maps and launches the split kernel (no-op when S_max == 0).
+cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
+                                PFN_cuTensorMapEncodeTiled_v12000 encode);
+// Launches the log-sum-exp merge of the split partials.
+cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream);
+
+// ---- causal prefill ----------------------------------------------------------
+struct PrefillLaunch {
+  const uint16_t *q;  // [B, H_q, T_q, d]
+  const uint16_t *k;  // [B, H_kv, S_kv, d]
+  const uint16_t *v;  // [B, H_kv, S_kv, d]
+  int B, H_q, H_kv, T_q, S_kv, q_offset;
+  float scale;
+  uint16_t *o;  // [B, H_q, T_q, d]
+  float *lse;   // [B, H_q, T_q]
+  int num_sms;
+  WaitCtl wait;
+};
+
+cudaError_t prefill_prepare_device();
+cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
+                           PFN_cuTensorMapEncodeTiled_v12000 encode);
+
+// ---- diagnostics --------------------------------------------------------------
+cudaError_t selftest_bounded_wait_launch(WaitCtl wait, cudaStream_t stream);
+
+}  // namespace gqa

@@ -1,0 +1,259 @@
+/*
+ * gqa_attn.h -- C ABI of the GB300 (sm_103a) grouped-query attention library.
+ *
+ * Two operations, both defined by the design record "ADR-0060: AHBM GQA Fused
+ * Attention Kernel (Llama3-70B)" (kernbench2):
+ *
+ *   gqa_attn_decode          split-KV decode (FlashDecoding).  The G query heads
+ *                            that share one KV head are folded into one matrix
+ *                            product so every K/V tile is read from HBM once
+ *                            (record: TL;DR "Kernel 1", section 5.2 "DECODE, no
+ *                            SP"); each KV chunk yields a partial that a
+ *                            log-sum-exp merge combines (section 4 "Reduction").
+ *   gqa_attn_prefill_causal  causal prefill with online softmax and fully masked
+ *                            tiles skipped (section 3 "Per-tile op sequence",
+ *                            section 5.4 "PREFILL, no SP"), with q_offset for
+ *                            chunked prefill (section 0.5.3 "q_block_meta").
+ *
+ * Both compute, for query head h, KV head h / G (G = H_q / H_kv) and the keys
+ * visible to the query,
+ *     O   = softmax(scale * q K^T) V          (bf16 out, rounded to nearest even)
+ *     lse = scale * max_j s_j + ln sum_j exp(scale * (s_j - max_j s_j))   (fp32)
+ * i.e. lse is the natural-log log-sum-exp of the scaled scores.  A query that
+ * sees no key (decode with seqlen 0) gets O = 0 and lse = -inf.
+ *
+ * Conventions common to every entry point
+ *   - bf16 tensors are passed as uint16_t bit patterns (gqa_bf16_t).
+ *   - Every tensor is dense, row-major (C order) with the shape given below;
+ *     head dimension d is innermost.
+ *   - Device pointers must point to device memory of the current CUDA device
+ *     and be 16-byte aligned.  The caller owns every buffer; the library keeps
+ *     no pointer after a call returns and allocates no device memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous and stream-ordered; they never synchronise except where a
+ *     function says so.  Inputs must stay valid until the stream reaches the
+ *     work.
+ *   - On any return other than GQA_OK nothing has been launched, except
+ *     GQA_ERR_CUDA, which reports a launch failure (the CUDA error is left for
+ *     cudaGetLastError to read).
+ *   - Waits inside the kernels are bounded (about two seconds).  A wait that
+ *     runs out sets a device-side status word and the kernel returns early;
+ *     gqa_attn_device_status reads it.  No kernel traps.
+ *
+ * Thread safety: all entry points may be called from several host threads; the
+ * per-device set-up done on first use is guarded by a mutex.
+ */
+#ifndef GQA_ATTN_H_
+#define GQA_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GQA_API __attribute__((visibility("default")))
+#else
+#define GQA_API
+#endif
+
+#define GQA_ATTN_ABI_VERSION 1
+
+typedef uint16_t gqa_bf16_t; /* bf16 bit pattern */
+typedef void *gqa_stream_t;  /* a cudaStream_t */
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or shape       */
+  GQA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d != 128, G > 8)  */
+  GQA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed                 */
+  GQA_ERR_WORKSPACE = 4,   /* workspace smaller than the size function reports */
+  GQA_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out               */
+} gqa_status_t;
+
+/* Human-readable name of a status code; never NULL, static storage. */
+GQA_API const char *gqa_status_string(int status);
+
+/* GQA_ATTN_ABI_VERSION of the loaded library. */
+GQA_API int gqa_attn_abi_version(void);
+
+/* ------------------------------------------------------------------------- */
+/* Decode                                                                      */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Split plan for decode (host only, no CUDA call).  The KV sequence of every
+ * (batch, KV head) is cut into contiguous chunks of `chunk` keys; split s owns
+ * keys [s*chunk, min((s+1)*chunk, seqlen)) -- the contiguous-block placement of
+ * the record's section 2.1 ("KV cache allocation"), rank r owning
+ * [r*B, (r+1)*B).  A split whose range is empty does no work and is skipped by
+ * the merge.
+ *
+ *   B, H_kv, S_max  batch, KV heads, capacity of the KV cache in keys (>= 0)
+ *   num_sms         streaming multiprocessors of the target device (> 0)
+ *   num_splits      0: choose from S_max, B*H_kv and num_sms so one wave of CTAs
+ *                   fills the GPU, with chunks no longer than 2048 keys;
+ *                   > 0: use this many splits (clamped to the number of 64-key
+ *                   tiles in S_max).
+ *   out_num_splits  written: splits per sequence (grid width), >= 1 if S_max > 0
+ *   out_chunk       written: keys per split, a multiple of 64
+ * Returns GQA_OK or GQA_ERR_INVALID_ARG (negative sizes, num_sms <= 0, null
+ * outputs).
+ */
+GQA_API int gqa_attn_decode_plan(int B, int H_kv, int S_max, int num_sms, int num_splits,
+                                 int *out_num_splits, int *out_chunk);
+
+/*
+ * Bytes of device workspace gqa_attn_decode needs for these sizes (host only).
+ * Same arguments as gqa_attn_decode_plan plus H_q and d.  The workspace holds
+ * one fp32 partial (O_s [d] normalised by its own sum, and lse_s) per
+ * (batch, query head, split): B*H_q*num_splits*(d+1)*4 bytes, rounded up to
+ * 256.  Returns 0 for invalid arguments.
+ */
+GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_max, int d,
+                                              int num_sms, int num_splits);
+
+/*
+ * Split-KV GQA decode, T_q = 1 (record: TL;DR "Kernel 1", sections 3, 4, 5.2,
+ * 5.3).
+ *
+ *   q         device [B, H_q, d] bf16, post-RoPE queries (section 0.5.3).
+ *   k_cache   device [B, H_kv, S_max, d] bf16, post-RoPE keys; read only.
+ *   v_cache   device [B, H_kv, S_max, d] bf16; read only.
+ *   seqlens   device [B] int32, 0 <= seqlens[b] <= S_max: sequence b sees keys
+ *             0..seqlens[b]-1.  Cache rows at or past seqlens[b] are never
+ *             used and may hold any bits (NaN included).  Values outside
+ *             [0, S_max] are clamped on the device.
+ *   B, H_q, H_kv, S_max, d   sizes; d must be 128; H_q % H_kv == 0 and
+ *             G = H_q / H_kv <= 8 (the G heads fill the 8-wide MMA dimension).
+ *   scale     softmax scale (the record uses 1/sqrt(d)); any finite value.
+ *   num_splits 0 = automatic plan, else the requested split count (see
+ *             gqa_attn_decode_plan; the plan uses this device's SM count).
+ *   o         device [B, H_q, d] bf16 output.
+ *   lse       device [B, H_q] fp32 output (natural log, scaled scores).
+ *   workspace device scratch of at least gqa_attn_decode_workspace_size(...)
+ *             bytes for this device's SM count, 16-byte aligned; its contents
+ *             on entry do not matter; it is overwritten.
+ *   ws_bytes  size of `workspace` in bytes.
+ *   stream    cudaStream_t.
+ * Launches two kernels on `stream`: the split kernel (one CTA per
+ * (split, KV head, batch)) and the log-sum-exp merge.  Deterministic: the
+ * same inputs give bit-identical outputs (fixed reduction order, no atomics).
+ * B == 0 launches nothing and returns GQA_OK.
+ */
+GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
+                            const gqa_bf16_t *v_cache, const int32_t *seqlens, int B,
+                            int H_q, int H_kv, int S_max, int d, float scale, int num_splits,
+                            gqa_bf16_t *o, float *lse, void *workspace, size_t ws_bytes,
+                            gqa_stream_t stream);
+
+/*
+ * The two phases of gqa_attn_decode as separate calls (same arguments, same
+ * plan, same workspace).  gqa_attn_decode_split runs the split kernel and
+ * leaves the per-split partials in `workspace`; gqa_attn_decode_merge reads
+ * them and writes o and lse.  Calling split then merge on one stream is
+ * exactly gqa_attn_decode; between the two the workspace must not be touched.
+ * split needs q, k_cache, v_cache, seqlens; merge needs seqlens, o, lse (the
+ * other pointers may be NULL for the phase that does not use them).
+ */
+GQA_API int gqa_attn_decode_split(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
+                                  const gqa_bf16_t *v_cache, const int32_t *seqlens, int B,
+                                  int H_q, int H_kv, int S_max, int d, float scale,
+                                  int num_splits, void *workspace, size_t ws_bytes,
+                                  gqa_stream_t stream);
+GQA_API int gqa_attn_decode_merge(const int32_t *seqlens, int B, int H_q, int H_kv, int S_max,
+                                  int d, int num_splits, gqa_bf16_t *o, float *lse,
+                                  const void *workspace, size_t ws_bytes, gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Causal prefill                                                              */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Causal GQA prefill with online softmax (record: Kernel 2's math, sections 3
+ * and 5.4; the ring of section 5.5 is not used on one GPU).
+ *
+ *   q        device [B, H_q, T_q, d] bf16; row i is the query at absolute
+ *            position q_offset + i.
+ *   k, v     device [B, H_kv, S_kv, d] bf16; read only.
+ *   q_offset 0 <= q_offset and q_offset + T_q <= S_kv.  Row i sees keys
+ *            0..q_offset+i (the diagonal included); q_offset = 0 with
+ *            T_q = S_kv is the square causal mask, q_offset = S_kv - T_q is the
+ *            last chunk of a chunked prefill.
+ *   scale    softmax scale.
+ *   o        device [B, H_q, T_q, d] bf16 output.
+ *   lse      device [B, H_q, T_q] fp32 output.
+ *   d must be 128; H_q % H_kv == 0.  T_q == 0 or B == 0 launches nothing.
+ * Key tiles wholly after a query tile are never loaded.  Deterministic.
+ */
+GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
+                                    const gqa_bf16_t *v, int B, int H_q, int H_kv, int T_q,
+                                    int S_kv, int d, int q_offset, float scale, gqa_bf16_t *o,
+                                    float *lse, gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Host-buffer variants (whole-call end-to-end path)                           */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Device bytes gqa_attn_decode_from_host needs in `device_arena`: room for q,
+ * k_cache, v_cache, seqlens, o, lse and the decode workspace, each 256-byte
+ * aligned.  Host only; 0 for invalid arguments.
+ */
+GQA_API size_t gqa_attn_decode_from_host_arena_size(int B, int H_q, int H_kv, int S_max, int d,
+                                                    int num_sms, int num_splits);
+
+/*
+ * gqa_attn_decode on HOST buffers: copies q, k_cache, v_cache and seqlens from
+ * host memory into `device_arena` (cudaMemcpyAsync on `stream`), runs the
+ * decode there, and copies o and lse back to host memory.  Host buffers should
+ * be page-locked for the copies to be asynchronous.  The call returns once the
+ * work is queued; the host outputs are valid after the stream synchronises.
+ * Argument rules are those of gqa_attn_decode; `device_arena` must hold
+ * gqa_attn_decode_from_host_arena_size(...) bytes and be 256-byte aligned.
+ */
+GQA_API int gqa_attn_decode_from_host(const gqa_bf16_t *q_host, const gqa_bf16_t *k_cache_host,
+                                      const gqa_bf16_t *v_cache_host,
+                                      const int32_t *seqlens_host, int B, int H_q, int H_kv,
+                                      int S_max, int d, float scale, int num_splits,
+                                      gqa_bf16_t *o_host, float *lse_host, void *device_arena,
+                                      size_t arena_bytes, gqa_stream_t stream);
+
+/* Device bytes gqa_attn_prefill_causal_from_host needs (q, k, v, o, lse). */
+GQA_API size_t gqa_attn_prefill_causal_from_host_arena_size(int B, int H_q, int H_kv, int T_q,
+                                                            int S_kv, int d);
+
+/* gqa_attn_prefill_causal on host buffers, staged through `device_arena`. */
+GQA_API int gqa_attn_prefill_causal_from_host(const gqa_bf16_t *q_host, const gqa_bf16_t *k_host,
+                                              const gqa_bf16_t *v_host, int B, int H_q,
+                                              int H_kv, int T_q, int S_kv, int d, int q_offset,
+                                              float scale, gqa_bf16_t *o_host, float *lse_host,
+                                              void *device_arena, size_t arena_bytes,
+                                              gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Diagnostics                                                                 */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word that bounded waits set when they run out.  *out_status receives GQA_OK
+ * or GQA_ERR_TIMEOUT.  Returns GQA_ERR_CUDA if a CUDA call fails.
+ */
+GQA_API int gqa_attn_device_status(gqa_stream_t stream, int *out_status);
+
+/*
+ * Exercises the bounded wait: launches one CTA that waits on a shared-memory
+ * barrier nobody arrives at, with a limit of `timeout_us` microseconds
+ * (1 .. 1000000).  The kernel gives up, records GQA_ERR_TIMEOUT in the status
+ * word read by gqa_attn_device_status, and returns; nothing traps or hangs.
+ */
+GQA_API int gqa_attn_selftest_bounded_wait(int timeout_us, gqa_stream_t stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* GQA_ATTN_H_ */

@@ -1,0 +1,153 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+* the library builds for sm_103a and loads without a CUDA driver;
+* it exports every function include/gqa_attn.h declares;
+* the decode split planner and workspace sizing (pure host functions);
+* argument rejection happens before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gqa_attention_decode_gb300 as gqa
+from gqa_attention_decode_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gqa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GQA_API\s+[\w\s\*]+?\b(gqa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("gqa_attn_decode", "gqa_attn_prefill_causal", "gqa_attn_decode_plan",
+                 "gqa_attn_decode_workspace_size", "gqa_status_string",
+                 "gqa_attn_device_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(gqa.lib_path())
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, f"symbols declared in gqa_attn.h but not exported: {missing}"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert gqa.gqa_attn_abi_version() == 1
+    for code in range(6):
+        assert gqa.gqa_status_string(code).startswith("GQA_")
+    assert "unknown" in gqa.gqa_status_string(99)
+
+
+@pytest.mark.parametrize("B,H_kv,S_max,sms,req,expect", [
+    # one 32K sequence, 8 KV heads, 152 SMs: 37 splits of 14 tiles fill 2 CTAs/SM
+    (1, 8, 32768, 152, 0, (37, 896)),
+    # tiny decode with 4 requested splits of one 64-key tile each
+    (1, 1, 256, 152, 4, (4, 64)),
+    # ragged batch: chunks capped at 2048 keys
+    (16, 8, 131072, 152, 0, (64, 2048)),
+    # requested splits above the tile count are clamped
+    (1, 1, 100, 152, 50, (2, 64)),
+    # empty cache
+    (2, 8, 0, 152, 0, (1, 64)),
+])
+def test_decode_plan(lib, B, H_kv, S_max, sms, req, expect):
+    assert gqa.gqa_attn_decode_plan(B, H_kv, S_max, sms, req) == expect
+
+
+@pytest.mark.parametrize("B,H_kv,S_max,sms", [(1, 8, 32768, 152), (3, 2, 1000, 20),
+                                               (16, 8, 131072, 152), (1, 1, 1, 152),
+                                               (7, 3, 4097, 152)])
+def test_decode_plan_covers_every_key_once(lib, B, H_kv, S_max, sms):
+    for req in (0, 1, 3, 1000):
+        splits, chunk = gqa.gqa_attn_decode_plan(B, H_kv, S_max, sms, req)
+        assert chunk % 64 == 0 and chunk > 0 and splits >= 1
+        assert splits * chunk >= S_max          # the splits cover the cache
+        assert (splits - 1) * chunk < S_max     # and no split starts past it
+
+
+def test_workspace_size(lib):
+    splits, _ = gqa.gqa_attn_decode_plan(1, 8, 32768, 152, 0)
+    ws = gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 152, 0)
+    assert ws >= 64 * splits * 129 * 4 and ws % 256 == 0
+    assert gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 0, 0) == 0  # bad num_sms
+
+
+def test_plan_rejects_bad_arguments(lib):
+    with pytest.raises(gqa.GQAError) as e:
+        gqa.gqa_attn_decode_plan(-1, 8, 100, 152, 0)
+    assert e.value.status == gqa.GQA_ERR_INVALID_ARG
+    with pytest.raises(gqa.GQAError):
+        gqa.gqa_attn_decode_plan(1, 8, 100, 0, 0)
+
+
+def _raw_decode(lib, **kw):
+    args = dict(q=1 << 20, k=1 << 20, v=1 << 20, seqlens=1 << 20, B=1, H_q=64, H_kv=8,
+                S_max=1024, d=128, scale=0.088, num_splits=0, o=1 << 20, lse=1 << 20,
+                ws=1 << 20, ws_bytes=1 << 30, stream=0)
+    args.update(kw)
+    v = ctypes.c_void_p
+    return lib.gqa_attn_decode(v(args["q"]), v(args["k"]), v(args["v"]), v(args["seqlens"]),
+                               args["B"], args["H_q"], args["H_kv"], args["S_max"], args["d"],
+                               args["scale"], args["num_splits"], v(args["o"]), v(args["lse"]),
+                               v(args["ws"]), args["ws_bytes"], v(args["stream"]))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=0), gqa.GQA_ERR_INVALID_ARG),                      # null pointer
+    (dict(k=(1 << 20) + 2), gqa.GQA_ERR_INVALID_ARG),          # misaligned pointer
+    (dict(H_q=60), gqa.GQA_ERR_INVALID_ARG),                   # H_q % H_kv != 0
+    (dict(d=64), gqa.GQA_ERR_UNSUPPORTED),                     # only d = 128
+    (dict(H_q=72, H_kv=4), gqa.GQA_ERR_UNSUPPORTED),           # G = 18 > 8
+    (dict(num_splits=-1), gqa.GQA_ERR_INVALID_ARG),
+    (dict(S_max=-5), gqa.GQA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), gqa.GQA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), gqa.GQA_ERR_INVALID_ARG),
+    (dict(B=0), gqa.GQA_OK),                                   # empty batch: nothing to do
+])
+def test_decode_rejects_before_any_cuda_call(lib, kw, expect):
+    assert _raw_decode(lib, **kw) == expect
+
+
+def _raw_prefill(lib, **kw):
+    args = dict(q=1 << 20, k=1 << 20, v=1 << 20, B=1, H_q=64, H_kv=8, T_q=128, S_kv=256,
+                d=128, q_offset=0, scale=0.088, o=1 << 20, lse=1 << 20, stream=0)
+    args.update(kw)
+    v = ctypes.c_void_p
+    return lib.gqa_attn_prefill_causal(v(args["q"]), v(args["k"]), v(args["v"]), args["B"],
+                                       args["H_q"], args["H_kv"], args["T_q"], args["S_kv"],
+                                       args["d"], args["q_offset"], args["scale"], v(args["o"]),
+                                       v(args["lse"]), v(args["stream"]))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(v=0), gqa.GQA_ERR_INVALID_ARG),
+    (dict(o=(1 << 20) + 8), gqa.GQA_ERR_INVALID_ARG),
+    (dict(q_offset=200), gqa.GQA_ERR_INVALID_ARG),             # q_offset + T_q > S_kv
+    (dict(q_offset=-1), gqa.GQA_ERR_INVALID_ARG),
+    (dict(H_kv=7), gqa.GQA_ERR_INVALID_ARG),
+    (dict(d=96), gqa.GQA_ERR_UNSUPPORTED),
+    (dict(T_q=0), gqa.GQA_OK),
+    (dict(B=0), gqa.GQA_OK),
+])
+def test_prefill_rejects_before_any_cuda_call(lib, kw, expect):
+    assert _raw_prefill(lib, **kw) == expect
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros((1, 8, 128), dtype=torch.bfloat16)
+    k = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gqa.gqa_attn_decode(q, k, k, torch.zeros(1, dtype=torch.int32), 0.1)
