@@ -22,6 +22,8 @@ from ._binding import (  # noqa: F401
     gqa_attn_decode,
     gqa_attn_decode_split,
     gqa_attn_decode_merge,
+    gqa_attn_decode_noalloc,
+    GQA_NOALLOC_SCRATCH_BYTES,
     gqa_attn_prefill_causal,
     gqa_attn_decode_from_host_arena_size,
     gqa_attn_decode_from_host,

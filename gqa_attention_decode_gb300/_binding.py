@@ -38,6 +38,8 @@ _SIGNATURES = {
                                        _c_int, _c_float, _c_int, _vp, _c_size, _vp]),
     "gqa_attn_decode_merge": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                        _vp, _vp, _vp, _c_size, _vp]),
+    "gqa_attn_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                         _c_int, _c_float, _c_int, _vp, _vp, _vp]),
     "gqa_attn_prefill_causal": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                          _c_int, _c_int, _c_float, _vp, _vp, _vp]),
     "gqa_attn_decode_from_host_arena_size": (_c_size, [_c_int] * 7),
@@ -211,6 +213,33 @@ def gqa_attn_decode_merge(seqlens, H_kv, S_max, num_splits, o, lse, workspace, s
                                        _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
                                        _stream_handle(stream, dev))
     _check(rc, "gqa_attn_decode_merge")
+
+
+GQA_NOALLOC_SCRATCH_BYTES = 48 << 20
+
+
+def gqa_attn_decode_noalloc(q, k_cache, v_cache, seqlens, scale, num_splits=0, o=None, lse=None,
+                            stream=None):
+    """gqa_attn_decode for callers that cannot allocate device memory: the split
+    partials go to the library's fixed static scratch (GQA_NOALLOC_SCRATCH_BYTES)
+    instead of a workspace.  Calls that overlap on the GPU race on that scratch.
+    o and lse must be given (this function allocates nothing)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    _need(o, "o", torch.bfloat16, 3, dev)
+    _need(lse, "lse", torch.float32, 2, dev)
+    B, H_q, d = q.shape
+    _, H_kv, S_max, _ = k_cache.shape
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), B,
+                                         H_q, H_kv, S_max, d, float(scale), int(num_splits),
+                                         _ptr(o), _ptr(lse), _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_decode_noalloc")
+    return o, lse
 
 
 # ---------------------------------------------------------------------------

@@ -167,6 +167,38 @@ GQA_API int gqa_attn_decode_merge(const int32_t *seqlens, int B, int H_q, int H_
                                   int d, int num_splits, gqa_bf16_t *o, float *lse,
                                   const void *workspace, size_t ws_bytes, gqa_stream_t stream);
 
+/*
+ * Decode without a workspace argument, for callers that cannot allocate device
+ * memory where they run attention: code inside a custom allocator or memory
+ * pool that must not re-enter it, runtimes that forbid allocation after
+ * start-up, and hosts that have no allocator to hand.  The design record has
+ * no counterpart to this entry point; it exists only for such callers.
+ *
+ * Arguments, outputs and errors are those of gqa_attn_decode minus `workspace`
+ * and `ws_bytes`.  The per-split partials go to a scratch array of
+ * GQA_NOALLOC_SCRATCH_BYTES (48 MiB) in the library's static device memory,
+ * which every GPU that loads the library holds until the process exits.  The
+ * call allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *   - Size limit: a problem whose workspace (gqa_attn_decode_workspace_size for
+ *     this device) exceeds GQA_NOALLOC_SCRATCH_BYTES is rejected with
+ *     GQA_ERR_WORKSPACE and nothing is launched; pass a smaller num_splits or use
+ *     gqa_attn_decode.  (One 32K-key Llama3-70B layer needs under 2 MiB; a batch
+ *     of 16 sequences in a 128K-key cache needs about 33 MiB.)
+ *   - Shared scratch: every call uses the same array, and it keeps the last
+ *     call's contents.  Calls whose GPU work overlaps (other streams, other host
+ *     threads on the same device) race on it; serialise them.  Nothing needs
+ *     clearing between calls: each call writes every partial it reads.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (48u << 20)
+GQA_API int gqa_attn_decode_noalloc(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
+                                    const gqa_bf16_t *v_cache, const int32_t *seqlens, int B,
+                                    int H_q, int H_kv, int S_max, int d, float scale,
+                                    int num_splits, gqa_bf16_t *o, float *lse,
+                                    gqa_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Causal prefill                                                              */
 /* ------------------------------------------------------------------------- */
