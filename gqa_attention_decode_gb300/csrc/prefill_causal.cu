@@ -1,9 +1,467 @@
-// prefill_causal.cu -- causal GQA prefill (placeholder until the tcgen05 kernel lands).
+// prefill_causal.cu -- causal GQA prefill for sm_103a with tcgen05 tensor cores.
+//
+// What it computes (design record "ADR-0060: AHBM GQA Fused Attention Kernel
+// (Llama3-70B)"): for each query tile, the per-tile online softmax of section 3
+// (S = scale Q K^T, running max and sum, O = O corr + P V, normalise once) over
+// the key tiles the tile can see; section 5.4's tile classes decide the work:
+// key tiles wholly in the past run unmasked, the boundary tiles get the causal
+// mask, and tiles wholly in the future are never loaded.  Query row i sits at
+// absolute position q_offset + i (the record's q_block_meta), which makes the
+// same kernel serve chunked prefill.
+//
+// GB300 mapping
+//   * Persistent CTAs (one per SM, 384 threads).  A work unit is one 128-row
+//     query tile of TWO query heads of the same KV group: both heads see exactly
+//     the same key tiles, so every K/V tile loaded by TMA feeds two S = Q K^T and
+//     two O += P V products (the record's GQA reuse, applied to prefill), and the
+//     two softmax warpgroups ping-pong: while one computes exp() the tensor core
+//     works on the other head (the record's "GEMM idle during softmax" bubble,
+//     section 5.6 opt3, removed by warp specialisation instead of software
+//     pipelining).  Units run longest-first (latest query tile first).
+//   * Warp 0: TMA producer (Q tiles, then K_j, V_j through a 3-stage ring).
+//     Warp 1: allocates the 512 TMEM columns and issues every tcgen05.mma from
+//     one thread (M = N = 128, K = 16, bf16 in, fp32 accumulate).  Warps 4-7 and
+//     8-11: softmax for head 0 and head 1, one thread per query row.
+//   * TMEM: S0, S1 (128 columns each) and O0, O1 (128 columns each).  P goes back
+//     to shared memory as bf16 in the 128B-swizzled K-major layout the MMA reads.
+//   * The running max is only moved (and O in TMEM rescaled) when a row's tile
+//     max exceeds it by more than 8 in log2 units; the final O / l and
+//     lse = m ln2 + ln l use the same reference max, so the result is exact.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "device_common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace gqa {
-cudaError_t prefill_prepare_device() { return cudaSuccess; }
-cudaError_t prefill_launch(const PrefillLaunch &, cudaStream_t, PFN_cuTensorMapEncodeTiled_v12000) {
-  return cudaErrorNotSupported;
+namespace prefill {
+
+constexpr int kD = 128;
+constexpr int kBM = 128;                     // query rows per tile
+constexpr int kBN = 128;                     // keys per tile
+constexpr int kStages = 3;                   // K/V ring depth (each stage holds one K or V tile)
+constexpr int kThreads = 384;
+constexpr int kTileBytes = kBM * kD * 2;     // 32 KiB
+constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column half: [128 rows x 128 B]
+constexpr int kOffQ = 0;                     // Q0, Q1
+constexpr int kOffP = 2 * kTileBytes;        // P0, P1
+constexpr int kOffStage = 4 * kTileBytes;    // K/V ring
+constexpr int kOffBar = kOffStage + kStages * kTileBytes;
+// barriers: kv_full[S], kv_empty[S], q_full[2], q_empty, s_full[2], p_full[2], o_final[2], drain
+constexpr int kNumBars = 2 * kStages + 2 + 1 + 2 + 2 + 2 + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base slot, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + 1024 alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units (a factor of 256)
+
+struct Params {
+  uint16_t *o;
+  float *lse;
+  int B, H_q, H_kv, G, T_q, S_kv, q_offset;
+  int n_qtiles, n_pairs, total_units;
+  float sl2;  // scale * log2(e)
+  WaitCtl wait;
+};
+
+struct Unit {
+  int b, kv, qt, h0, h1, n_kv;
+  bool second_valid;
+};
+
+__device__ __forceinline__ Unit unit_at(const Params &p, int u) {
+  Unit w;
+  const int per_qt = p.B * p.H_kv * p.n_pairs;
+  w.qt = p.n_qtiles - 1 - u / per_qt;  // latest (longest) query tiles first
+  int r = u % per_qt;
+  const int pair = r % p.n_pairs;
+  r /= p.n_pairs;
+  w.kv = r % p.H_kv;
+  w.b = r / p.H_kv;
+  w.h0 = w.kv * p.G + 2 * pair;
+  w.second_valid = 2 * pair + 1 < p.G;
+  w.h1 = w.second_valid ? w.h0 + 1 : w.h0;
+  const int qe = min((w.qt + 1) * kBM, p.T_q);
+  w.n_kv = (p.q_offset + qe - 1) / kBN + 1;
+  return w;
 }
+
+__device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity, const WaitCtl &ctl,
+                                               volatile int *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > ctl.timeout_ns) {
+      atomicExch(ctl.status, kStatusTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Descriptor of 16 consecutive K-columns (k-step kk) of a K-major 128x128 bf16 tile
+// stored as two 128B-swizzled 64-column halves.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+  return tc::smem_desc_sw128(tile + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+}
+// Descriptor of 16 consecutive K-rows (k-step kk) of an MN-major tile (V: keys x d,
+// d contiguous); the two 64-column halves are the two MN blocks (lbo).
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
+  return tc::smem_desc_sw128(tile + kk * 2048, kHalfBytes, 1024);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  const uint32_t bar0 = smem_u32(bars);
+  auto kv_full = [&](int s) { return bar0 + 8u * s; };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto q_full = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
+  const uint32_t q_empty = bar0 + 8u * (2 * kStages + 2);
+  auto s_full = [&](int i) { return bar0 + 8u * (2 * kStages + 3 + i); };
+  auto p_full = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + i); };
+  auto o_final = [&](int i) { return bar0 + 8u * (2 * kStages + 7 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 9);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full(i), 1);
+      mbar_init(s_full(i), 1);
+      mbar_init(p_full(i), 128);
+      mbar_init(o_final(i), 1);
+    }
+    mbar_init(q_empty, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------- TMA producer -------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      int ld = 0, it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++it) {
+        const Unit w = unit_at(p, u);
+        if (!wait_abortable(q_empty, (it & 1) ^ 1, p.wait, abort_flag)) { ok = false; break; }
+        for (int i = 0; i < 2; ++i) {
+          const int h = i == 0 ? w.h0 : w.h1;
+          const uint32_t dst = sbase + kOffQ + i * kTileBytes;
+          mbar_arrive_expect_tx(q_full(i), kTileBytes);
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(dst + half * kHalfBytes, &tm_q, q_full(i), 0, half, w.qt * kBM,
+                        w.b * p.H_q + h, pol_q);
+        }
+        for (int j = 0; ok && j < w.n_kv; ++j) {
+          for (int which = 0; which < 2; ++which, ++ld) {
+            const int s = ld % kStages;
+            if (!wait_abortable(kv_empty(s), ((ld / kStages) & 1) ^ 1, p.wait, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = sbase + kOffStage + s * kTileBytes;
+            mbar_arrive_expect_tx(kv_full(s), kTileBytes);
+            const CUtensorMap *map = which == 0 ? &tm_k : &tm_v;
+            for (int half = 0; half < 2; ++half)
+              tma_load_4d(dst + half * kHalfBytes, map, kv_full(s), 0, half, j * kBN,
+                          w.b * p.H_kv + w.kv, pol_kv);
+          }
+        }
+      }
+      // no copy may still be in flight when the CTA exits
+      for (int i = max(0, ld - kStages); i < ld; ++i)
+        wait_abortable(kv_full(i % kStages), (i / kStages) & 1, p.wait, abort_flag);
+    }
+  } else if (warp == 1) {
+    // ------------------------- MMA issuer -------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, 0);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kBM, kD, 1);
+      const uint32_t t_s[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t t_o[2] = {tmem + 256u, tmem + 384u};
+      const uint32_t q_smem[2] = {sbase + kOffQ, sbase + kOffQ + kTileBytes};
+      const uint32_t p_smem[2] = {sbase + kOffP, sbase + kOffP + kTileBytes};
+      int ld_base = 0, tile_base = 0, it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++it) {
+        const Unit w = unit_at(p, u);
+        const int n = w.n_kv;
+        for (int i = 0; ok && i < 2; ++i)
+          if (!wait_abortable(q_full(i), it & 1, p.wait, abort_flag)) ok = false;
+        tc::fence_after_sync();
+        for (int j = 0; ok && j <= n; ++j) {
+          const int ldK = ld_base + 2 * j, ldV = ld_base + 2 * (j - 1) + 1;
+          const uint32_t k_smem = sbase + kOffStage + (ldK % kStages) * kTileBytes;
+          const uint32_t v_smem = sbase + kOffStage + (ldV % kStages) * kTileBytes;
+          if (j < n) {
+            if (!wait_abortable(kv_full(ldK % kStages), (ldK / kStages) & 1, p.wait, abort_flag)) {
+              ok = false;
+              break;
+            }
+          }
+          if (j > 0) {
+            if (!wait_abortable(kv_full(ldV % kStages), (ldV / kStages) & 1, p.wait, abort_flag)) {
+              ok = false;
+              break;
+            }
+          }
+          for (int i = 0; i < 2; ++i) {
+            if (j > 0) {  // O_i += P_i V_{j-1}
+              if (!wait_abortable(p_full(i), (tile_base + j - 1) & 1, p.wait, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc::fence_after_sync();
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                tc::mma_ss(t_o[i], desc_kmajor(p_smem[i], kk), desc_mnmajor(v_smem, kk), idesc_pv,
+                           (j > 1 || kk > 0) ? 1u : 0u);
+              if (i == 1) tc::commit(kv_empty(ldV % kStages));
+              if (j == n) tc::commit(o_final(i));
+            }
+            if (j < n) {  // S_i = Q_i K_j^T
+#pragma unroll
+              for (int kk = 0; kk < kD / 16; ++kk)
+                tc::mma_ss(t_s[i], desc_kmajor(q_smem[i], kk), desc_kmajor(k_smem, kk), idesc_s,
+                           kk > 0 ? 1u : 0u);
+              tc::commit(s_full(i));
+              if (i == 1) {
+                tc::commit(kv_empty(ldK % kStages));
+                if (j == n - 1) tc::commit(q_empty);
+              }
+            }
+          }
+        }
+        ld_base += 2 * n;
+        tile_base += n;
+      }
+      // every issued MMA must finish before TMEM is released
+      tc::commit(drain_bar);
+      wait_abortable(drain_bar, 0, p.wait, abort_flag);
+    }
+  } else if (warp >= 4) {
+    // ------------------------- softmax warpgroups -------------------------
+    const int i = (warp - 4) >> 2;  // 0: head h0, 1: head h1
+    const int wq = warp & 3;
+    const int row = 32 * wq + lane;
+    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+    const uint32_t t_s = tmem + lane_off + 128u * i;
+    const uint32_t t_o = tmem + lane_off + 256u + 128u * i;
+    const uint32_t p_row = sbase + kOffP + i * kTileBytes + row * 128;
+    const bool pos_scale = p.sl2 > 0.f;
+    int tile = 0, it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++it) {
+      const Unit w = unit_at(p, u);
+      const int q0 = p.q_offset + w.qt * kBM;  // absolute position of row 0 of the tile
+      const int qpos = q0 + row;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < w.n_kv; ++j, ++tile) {
+        const bool ready = wait_abortable(s_full(i), tile & 1, p.wait, abort_flag);
+        if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+        tc::fence_after_sync();
+        const bool masked = (j * kBN + kBN - 1 > q0) || (j * kBN + kBN > p.S_kv);
+        const int key0 = j * kBN;
+        // pass 1: row max of this tile (in log2 units)
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc::ld_32x32b_x32(t_s + 32 * c, r);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x = __uint_as_float(r[e]);
+            if (!pos_scale) x *= p.sl2;
+            if (masked) {
+              const int kpos = key0 + 32 * c + e;
+              if (kpos > qpos || kpos >= p.S_kv) x = -INFINITY;
+            }
+            mx = fmaxf(mx, x);
+          }
+        }
+        const float mt = pos_scale ? mx * p.sl2 : mx;
+        if (j == 0) {
+          m_ref = mt;  // key 0 is visible to every row: finite
+        } else {
+          const bool need = mt > m_ref + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(m_ref, mt);
+            const float corr = fast_exp2(m_ref - m_new);
+            l *= corr;
+            // O_i holds P V up to tile j-1 (complete: S_i(j) was issued after it)
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r[32];
+              tc::ld_32x32b_x32(t_o + 32 * c, r);
+              tc::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+              tc::st_32x32b_x32(t_o + 32 * c, r);
+            }
+            tc::wait_st();
+            m_ref = m_new;
+          }
+        }
+        // pass 2: P = exp2(s * scale log2e - m_ref) as bf16 into shared memory
+        const float negm = -m_ref;
+        float rs = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc::ld_32x32b_x32(t_s + 32 * c, r);
+          tc::wait_ld();
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            float e8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float x = __uint_as_float(r[8 * q8 + e]);
+              float pe = fast_exp2(fmaf(x, p.sl2, negm));
+              if (masked) {
+                const int kpos = key0 + 32 * c + 8 * q8 + e;
+                if (kpos > qpos || kpos >= p.S_kv) pe = 0.f;
+              }
+              e8[e] = pe;
+              rs += pe;
+            }
+            const int chunk = 4 * c + q8;  // 16-byte chunk 0..15 of the row
+            const uint32_t addr =
+                p_row + (chunk >> 3) * kHalfBytes + (((chunk & 7) ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                         "r"(pack_bf16x2(e8[0], e8[1])), "r"(pack_bf16x2(e8[2], e8[3])),
+                         "r"(pack_bf16x2(e8[4], e8[5])), "r"(pack_bf16x2(e8[6], e8[7]))
+                         : "memory");
+          }
+        }
+        l += rs;
+        fence_proxy_async_smem();  // P visible to the tensor core
+        tc::fence_before_sync();   // O rescale stores ordered before the signal
+        mbar_arrive(p_full(i));
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, lse = m_ref ln2 + ln l
+      const bool ready = wait_abortable(o_final(i), it & 1, p.wait, abort_flag);
+      if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+      tc::fence_after_sync();
+      const int h = i == 0 ? w.h0 : w.h1;
+      const int qrow = w.qt * kBM + row;
+      const bool store = (i == 0 || w.second_valid) && qrow < p.T_q;
+      const size_t orow = ((size_t)w.b * p.H_q + h) * p.T_q + qrow;
+      const float inv_l = 1.f / l;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::ld_32x32b_x32(t_o + 32 * c, r);
+        tc::wait_ld();
+        if (store) {
+          uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 pk;
+            pk.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * inv_l,
+                               __uint_as_float(r[8 * v4 + 1]) * inv_l);
+            pk.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * inv_l,
+                               __uint_as_float(r[8 * v4 + 3]) * inv_l);
+            pk.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * inv_l,
+                               __uint_as_float(r[8 * v4 + 5]) * inv_l);
+            pk.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * inv_l,
+                               __uint_as_float(r[8 * v4 + 7]) * inv_l);
+            dst[v4] = pk;
+          }
+        }
+      }
+      if (store) p.lse[orow] = m_ref * 0.69314718055994531f + logf(l);
+      tc::fence_before_sync();  // O reads done before the next unit's first P signal
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+CUresult make_map(CUtensorMap *map, const uint16_t *base, int rows, int heads,
+                  PFN_cuTensorMapEncodeTiled_v12000 encode) {
+  // dims (innermost first): 64 columns, 2 column halves, rows, heads
+  const cuuint64_t dims[4] = {64, 2, (cuuint64_t)rows, (cuuint64_t)heads};
+  const cuuint64_t strides[3] = {128, 256, (cuuint64_t)rows * 256};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(base), dims,
+                strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace prefill
+
+cudaError_t prefill_prepare_device() {
+  return cudaFuncSetAttribute(prefill::prefill_causal_kernel,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, prefill::kSmemBytes);
+}
+
+cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
+                           PFN_cuTensorMapEncodeTiled_v12000 encode) {
+  using namespace prefill;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (make_map(&tm_q, a.q, a.T_q, a.B * a.H_q, encode) != CUDA_SUCCESS ||
+      make_map(&tm_k, a.k, a.S_kv, a.B * a.H_kv, encode) != CUDA_SUCCESS ||
+      make_map(&tm_v, a.v, a.S_kv, a.B * a.H_kv, encode) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  Params p;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.B = a.B;
+  p.H_q = a.H_q;
+  p.H_kv = a.H_kv;
+  p.G = a.H_q / a.H_kv;
+  p.T_q = a.T_q;
+  p.S_kv = a.S_kv;
+  p.q_offset = a.q_offset;
+  p.n_qtiles = (a.T_q + kBM - 1) / kBM;
+  p.n_pairs = (p.G + 1) / 2;
+  const long long units = (long long)p.n_qtiles * a.B * a.H_kv * p.n_pairs;
+  if (units > 0x7fffffffLL) return cudaErrorNotSupported;
+  p.total_units = (int)units;
+  p.sl2 = a.scale * 1.4426950408889634f;
+  p.wait = a.wait;
+  const int grid = (int)(units < a.num_sms ? units : a.num_sms);
+  prefill_causal_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+  return cudaGetLastError();
+}
+
 }  // namespace gqa

@@ -1,0 +1,143 @@
+"""GPU parity of the causal GQA prefill against the fp64 oracle, through the C ABI.
+
+Small cases span several 128-row and 128-key tiles with ragged tails and are
+compared in full; the two prefill workloads (8K causal, and the last 2K chunk
+of a 32K prompt with q_offset = 30720) are run at full size and compared on
+sampled rows, which include the first rows (few visible keys), rows around
+tile boundaries and the last rows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_synth
+import oracle
+import gqa_attention_decode_gb300 as gqa
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_attention_decode_gb300 import build
+    build.build()
+    gqa.load_library()
+    torch.cuda.set_device(0)
+    yield
+    assert gqa.gqa_attn_device_status() == gqa.GQA_OK
+
+
+def np64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def run(q, k, v, q_offset, scale):
+    o, lse = gqa.gqa_attn_prefill_causal(q, k, v, scale, q_offset)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,T_q,S_kv,q_offset", [
+    (1, 8, 1, 300, 300, 0),       # square causal, ragged last tile
+    (2, 16, 2, 200, 264, 64),     # chunk after a 64-token prefix
+    (1, 8, 2, 257, 300, 43),      # q_offset not tile aligned, one row past a tile
+    (1, 6, 2, 130, 130, 0),       # G = 3: the last head pair holds a single head
+    (1, 4, 4, 129, 200, 71),      # G = 1 (MHA)
+    (1, 8, 1, 1, 1, 0),           # one query, one key
+    (1, 8, 1, 1, 517, 516),       # one query at the end of a long prefix
+    (1, 16, 2, 384, 384, 0),      # exact multiple of the tile
+])
+def test_small_cases_full_compare(B, H_q, H_kv, T_q, S_kv, q_offset):
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=31, device=DEV)
+    scale = 1 / math.sqrt(128)
+    o, lse = run(q, k, v, q_offset, scale)
+    o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), q_offset, scale)
+    compare(o, lse, o_ref, lse_ref, f"prefill {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
+
+
+def _sampled_rows(w, n_random, seed):
+    rng = np.random.default_rng(seed)
+    rows = {0, 1, 2, 3, 127, 128, 129, 255, 256, w.T_q - 2, w.T_q - 1}
+    rows |= set(int(x) for x in rng.integers(0, w.T_q, n_random))
+    picks = []
+    for i in sorted(r for r in rows if 0 <= r < w.T_q):
+        picks.append((0, int(rng.integers(0, w.H_q)), i))
+    for h in (0, 1, 7, 8, 63):
+        picks.append((0, h, int(rng.integers(0, w.T_q))))
+    return picks
+
+
+@pytest.mark.parametrize("name", ["causal_prefill_8k", "chunked_prefill_32k"])
+def test_prefill_workloads_sampled(name):
+    w = gqa_synth.WORKLOADS[name]
+    q, k, v = gqa_synth.workload_prefill_inputs(w, DEV)
+    o, lse = run(q, k, v, w.q_offset, w.scale)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    picks = _sampled_rows(w, 48, 7)
+    ref_o = np.zeros((len(picks), w.d))
+    ref_lse = np.zeros(len(picks))
+    G = w.G
+    for r, (b, h, i) in enumerate(picks):
+        n = w.q_offset + i + 1
+        ro, rl = oracle.attend_rows(np64(q[b, h, i])[None], np64(k[b, h // G, :n]),
+                                    np64(v[b, h // G, :n]), w.scale, [n])
+        ref_o[r], ref_lse[r] = ro[0], rl[0]
+    got_o = torch.stack([o[b, h, i] for b, h, i in picks])
+    got_lse = torch.stack([lse[b, h, i] for b, h, i in picks])
+    compare(got_o, got_lse, ref_o, ref_lse, name)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.15, 0.3])
+def test_scale_values(scale):
+    q, k, v = gqa_synth.prefill_inputs(1, 8, 1, 200, 260, 128, seed=32, device=DEV)
+    o, lse = run(q, k, v, 60, scale)
+    o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), 60, scale)
+    compare(o, lse, o_ref, lse_ref, f"scale={scale}")
+
+
+def test_deterministic_bitwise():
+    q, k, v = gqa_synth.prefill_inputs(1, 64, 8, 1024, 1024, 128, seed=33, device=DEV)
+    o1, l1 = run(q, k, v, 0, 0.088)
+    o2, l2 = run(q, k, v, 0, 0.088)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_causal_skip_never_reads_future_keys():
+    """Keys after the last query's position are never loaded: NaN there changes nothing."""
+    q, k, v = gqa_synth.prefill_inputs(1, 8, 1, 256, 1024, 128, seed=34, device=DEV)
+    o_ref, l_ref = run(q, k, v, 100, 0.088)     # last query at position 355
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :, 384:] = float("nan")                # tiles starting at 384 are all future
+    v2[:, :, 384:] = float("nan")
+    o, l = run(q, k2, v2, 100, 0.088)
+    assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
+def test_host_buffer_variant_matches_device_call():
+    q, k, v = gqa_synth.prefill_inputs(1, 16, 2, 300, 400, 128, seed=35, device="cpu")
+    o_dev, l_dev = run(q.to(DEV), k.to(DEV), v.to(DEV), 100, 0.088)
+    nbytes = gqa.gqa_attn_prefill_causal_from_host_arena_size(1, 16, 2, 300, 400, 128)
+    arena = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    o_h = torch.empty_like(q).pin_memory()
+    l_h = torch.empty((1, 16, 300), dtype=torch.float32).pin_memory()
+    gqa.gqa_attn_prefill_causal_from_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), 0.088,
+                                          100, o_h, l_h, arena)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_dev.cpu()) and torch.equal(l_h, l_dev.cpu())
+
+
+def test_rejects_bad_q_offset_and_misalignment():
+    q, k, v = gqa_synth.prefill_inputs(1, 8, 1, 64, 64, 128, seed=36, device=DEV)
+    with pytest.raises(gqa.GQAError) as e:
+        gqa.gqa_attn_prefill_causal(q, k, v, 0.1, q_offset=1)   # q_offset + T_q > S_kv
+    assert e.value.status == gqa.GQA_ERR_INVALID_ARG
+    flat = torch.empty(k.numel() + 8, dtype=torch.bfloat16, device=DEV)
+    k_off = flat[4:4 + k.numel()].view(k.shape)                # 8-byte offset
+    with pytest.raises(gqa.GQAError) as e:
+        gqa.gqa_attn_prefill_causal(q, k_off, v, 0.1)
+    assert e.value.status == gqa.GQA_ERR_INVALID_ARG
