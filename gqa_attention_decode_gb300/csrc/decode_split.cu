@@ -281,37 +281,80 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (dd == 0) p.lse_part[row] = mmax * 0.69314718055994531f + logf(lsum);
     }
   }
+  // this CTA's partial is written: the merge grid may be scheduled
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// One CTA per (query head, sequence); thread = one of the d = 128 columns.
-// lse = max_s lse_s + ln sum_s exp(lse_s - max); O = sum_s exp(lse_s - lse) O_s.
-__global__ void __launch_bounds__(kD)
+// One CTA per (query head, sequence), 256 threads: thread (g, lane) owns columns
+// 4*lane .. 4*lane+3 and splits g, g+8, g+16, ...; the eight groups are summed
+// in shared memory.  lse = max_s lse_s + ln sum_s exp(lse_s - max);
+// O = sum_s exp(lse_s - lse) O_s.  Launched as a programmatic dependent of the
+// split kernel: everything before griddepcontrol.wait overlaps its tail.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeGroups = kMergeThreads / 32;
+
+__global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
                         const int32_t *__restrict__ seqlens, uint16_t *__restrict__ o,
                         float *__restrict__ lse, int H_q, int S_max, int num_splits, int chunk) {
-  const int h = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
+  __shared__ float4 red_o[kMergeGroups][32];
+  __shared__ float red_w[kMergeGroups];
+  __shared__ float red_m[kMergeGroups];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int t = threadIdx.x, grp = t >> 5, lane = t & 31;
   const int seqlen = min(max(seqlens[b], 0), S_max);
   const int ns = min((seqlen + chunk - 1) / chunk, num_splits);
   const size_t row = (size_t)b * H_q + h;
   if (ns == 0) {  // no visible key
-    o[row * kD + dd] = 0;
-    if (dd == 0) lse[row] = -INFINITY;
+    if (grp == 0) reinterpret_cast<uint2 *>(o + row * kD)[lane] = make_uint2(0u, 0u);
+    if (t == 0) lse[row] = -INFINITY;
     return;
   }
   const float *lp = lse_part + row * num_splits;
-  const float *op = o_part + row * num_splits * kD + dd;
   float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, lp[s]);
+  for (int s = t; s < ns; s += kMergeThreads) mx = fmaxf(mx, lp[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) red_m[grp] = mx;
+  __syncthreads();
+  mx = red_m[0];
+#pragma unroll
+  for (int g = 1; g < kMergeGroups; ++g) mx = fmaxf(mx, red_m[g]);
+
   constexpr float kLog2e = 1.4426950408889634f;
-  float wsum = 0.f, acc = 0.f;
-  for (int s = 0; s < ns; ++s) {
+  const float4 *op = reinterpret_cast<const float4 *>(o_part + row * num_splits * kD) + lane;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+#pragma unroll 4
+  for (int s = grp; s < ns; s += kMergeGroups) {
     const float w = fast_exp2((lp[s] - mx) * kLog2e);
+    const float4 x = op[(size_t)s * (kD / 4)];
     wsum += w;
-    acc = fmaf(w, op[(size_t)s * kD], acc);
+    acc.x = fmaf(w, x.x, acc.x);
+    acc.y = fmaf(w, x.y, acc.y);
+    acc.z = fmaf(w, x.z, acc.z);
+    acc.w = fmaf(w, x.w, acc.w);
   }
-  const __nv_bfloat16 r = __float2bfloat16_rn(acc / wsum);
-  o[row * kD + dd] = *reinterpret_cast<const uint16_t *>(&r);
-  if (dd == 0) lse[row] = mx + logf(wsum);
+  red_o[grp][lane] = acc;
+  if (lane == 0) red_w[grp] = wsum;
+  __syncthreads();
+  if (grp == 0) {
+    float4 sum = red_o[0][lane];
+    float W = red_w[0];
+#pragma unroll
+    for (int g = 1; g < kMergeGroups; ++g) {
+      const float4 x = red_o[g][lane];
+      sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
+      W += red_w[g];
+    }
+    const float inv = 1.f / W;
+    uint2 packed;
+    packed.x = pack_bf16x2(sum.x * inv, sum.y * inv);
+    packed.y = pack_bf16x2(sum.z * inv, sum.w * inv);
+    reinterpret_cast<uint2 *>(o + row * kD)[lane] = packed;
+    if (lane == 0) lse[row] = mx + logf(W);
+  }
 }
 
 static CUresult make_kv_map(CUtensorMap *map, const uint16_t *base, int B, int H_kv, int S_max,
@@ -365,11 +408,19 @@ cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
 
 cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream) {
   using namespace decode;
-  dim3 mgrid(a.H_q, a.B);
-  decode_merge_kernel<<<mgrid, kD, 0, stream>>>(a.o_part, a.lse_part, a.seqlens, a.o, a.lse,
-                                                a.H_q, a.S_max, a.num_splits,
-                                                a.chunk > 0 ? a.chunk : 1);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.H_q, a.B);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel, (const float *)a.o_part,
+                            (const float *)a.lse_part, a.seqlens, a.o, a.lse, a.H_q, a.S_max,
+                            a.num_splits, a.chunk > 0 ? a.chunk : 1);
 }
 
 }  // namespace gqa
