@@ -10,20 +10,24 @@
 // same kernel serve chunked prefill.
 //
 // GB300 mapping
-//   * Persistent CTAs (one per SM, 384 threads).  A work unit is one 128-row
+//   * Persistent CTAs (one per SM, 320 threads).  A work unit is one 128-row
 //     query tile of TWO query heads of the same KV group: both heads see exactly
 //     the same key tiles, so every K/V tile loaded by TMA feeds two S = Q K^T and
 //     two O += P V products (the record's GQA reuse, applied to prefill), and the
-//     two softmax warpgroups ping-pong: while one computes exp() the tensor core
-//     works on the other head (the record's "GEMM idle during softmax" bubble,
-//     section 5.6 opt3, removed by warp specialisation instead of software
-//     pipelining).  Units run longest-first (latest query tile first).
-//   * Warp 0: TMA producer (Q tiles, then K_j, V_j through a 3-stage ring).
-//     Warp 1: allocates the 512 TMEM columns and issues every tcgen05.mma from
-//     one thread (M = N = 128, K = 16, bf16 in, fp32 accumulate).  Warps 4-7 and
-//     8-11: softmax for head 0 and head 1, one thread per query row.
-//   * TMEM: S0, S1 (128 columns each) and O0, O1 (128 columns each).  P goes back
-//     to shared memory as bf16 in the 128B-swizzled K-major layout the MMA reads.
+//     two softmax warpgroups ping-pong: a token passed between them lets only one
+//     run its exp() phase at a time while the tensor core works on the other
+//     head (the record's "GEMM idle during softmax" bubble, section 5.6 opt3,
+//     removed by warp specialisation instead of software pipelining).  Units run
+//     longest-first (latest query tile first).
+//   * Warps 0-3 and 4-7: softmax for head 0 and head 1, one thread per query
+//     row, the whole 128-column S row held in registers.  Warp 8: TMA producer
+//     (Q tiles, then K_j, V_j through a 5-stage ring).  Warp 9: allocates the 512
+//     TMEM columns and issues every tcgen05.mma from one thread (M = N = 128,
+//     K = 16, bf16 in, fp32 accumulate).
+//   * TMEM: S0, S1 (128 columns each) and O0, O1 (128 columns each).  P is
+//     written back as bf16 over the first 64 columns of its S block and read by
+//     the P V product straight from tensor memory (A operand in TMEM), so P never
+//     touches shared memory.
 //   * The running max is only moved (and O in TMEM rescaled) when a row's tile
 //     max exceeds it by more than 8 in log2 units; the final O / l and
 //     lse = m ln2 + ln l use the same reference max, so the result is exact.
@@ -40,16 +44,17 @@ namespace prefill {
 constexpr int kD = 128;
 constexpr int kBM = 128;                     // query rows per tile
 constexpr int kBN = 128;                     // keys per tile
-constexpr int kStages = 3;                   // K/V ring depth (each stage holds one K or V tile)
-constexpr int kThreads = 384;
+constexpr int kStages = 5;                   // K/V ring depth (each stage holds one K or V tile)
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kThreads = 320;
 constexpr int kTileBytes = kBM * kD * 2;     // 32 KiB
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column half: [128 rows x 128 B]
 constexpr int kOffQ = 0;                     // Q0, Q1
-constexpr int kOffP = 2 * kTileBytes;        // P0, P1
-constexpr int kOffStage = 4 * kTileBytes;    // K/V ring
+constexpr int kOffStage = 2 * kTileBytes;    // K/V ring
 constexpr int kOffBar = kOffStage + kStages * kTileBytes;
-// barriers: kv_full[S], kv_empty[S], q_full[2], q_empty, s_full[2], p_full[2], o_final[2], drain
-constexpr int kNumBars = 2 * kStages + 2 + 1 + 2 + 2 + 2 + 1;
+// barriers: kv_full[S], kv_empty[S], q_full[2], q_empty, s_full[2], p_full[2], o_final[2],
+// exp-turn tokens[2], drain
+constexpr int kNumBars = 2 * kStages + 2 + 1 + 2 + 2 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base slot, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + 1024 alignment slack
 constexpr uint32_t kTmemCols = 512;
@@ -114,6 +119,8 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
   return tc::smem_desc_sw128(tile + kk * 2048, kHalfBytes, 1024);
 }
 
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
@@ -131,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto s_full = [&](int i) { return bar0 + 8u * (2 * kStages + 3 + i); };
   auto p_full = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + i); };
   auto o_final = [&](int i) { return bar0 + 8u * (2 * kStages + 7 + i); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 9);
+  auto tok = [&](int i) { return bar0 + 8u * (2 * kStages + 9 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 11);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -147,13 +155,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_full(i), 1);
       mbar_init(p_full(i), 128);
       mbar_init(o_final(i), 1);
+      mbar_init(tok(i), 128);
     }
     mbar_init(q_empty, 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
   }
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == kWarpTma) {
     // ------------------------- TMA producer -------------------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, ld - kStages); i < ld; ++i)
         wait_abortable(kv_full(i % kStages), (i / kStages) & 1, p.wait, abort_flag);
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ------------------------- MMA issuer -------------------------
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, 0);
@@ -211,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_s[2] = {tmem + 0u, tmem + 128u};
       const uint32_t t_o[2] = {tmem + 256u, tmem + 384u};
       const uint32_t q_smem[2] = {sbase + kOffQ, sbase + kOffQ + kTileBytes};
-      const uint32_t p_smem[2] = {sbase + kOffP, sbase + kOffP + kTileBytes};
       int ld_base = 0, tile_base = 0, it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++it) {
@@ -237,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           for (int i = 0; i < 2; ++i) {
-            if (j > 0) {  // O_i += P_i V_{j-1}
+            if (j > 0) {  // O_i += P_i V_{j-1}, P_i read from tensor memory
               if (!wait_abortable(p_full(i), (tile_base + j - 1) & 1, p.wait, abort_flag)) {
                 ok = false;
                 break;
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::fence_after_sync();
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
-                tc::mma_ss(t_o[i], desc_kmajor(p_smem[i], kk), desc_mnmajor(v_smem, kk), idesc_pv,
+                tc::mma_ts(t_o[i], t_s[i] + kk * 8, desc_mnmajor(v_smem, kk), idesc_pv,
                            (j > 1 || kk > 0) ? 1u : 0u);
               if (i == 1) tc::commit(kv_empty(ldV % kStages));
               if (j == n) tc::commit(o_final(i));
@@ -270,16 +278,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::commit(drain_bar);
       wait_abortable(drain_bar, 0, p.wait, abort_flag);
     }
-  } else if (warp >= 4) {
+  } else if (warp < kWarpTma) {
     // ------------------------- softmax warpgroups -------------------------
-    const int i = (warp - 4) >> 2;  // 0: head h0, 1: head h1
-    const int wq = warp & 3;
+    const int i = warp >> 2;  // 0: head h0, 1: head h1
+    const int wq = warp & 3;  // TMEM lane quarter of this warp
     const int row = 32 * wq + lane;
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const uint32_t t_s = tmem + lane_off + 128u * i;
     const uint32_t t_o = tmem + lane_off + 256u + 128u * i;
-    const uint32_t p_row = sbase + kOffP + i * kTileBytes + row * 128;
     const bool pos_scale = p.sl2 > 0.f;
+    const float mul = pos_scale ? p.sl2 : 1.f;  // multiplier still owed by the held scores
     int tile = 0, it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++it) {
@@ -288,87 +296,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qpos = q0 + row;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < w.n_kv; ++j, ++tile) {
-        const bool ready = wait_abortable(s_full(i), tile & 1, p.wait, abort_flag);
+        bool ready = wait_abortable(s_full(i), tile & 1, p.wait, abort_flag);
         if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
         tc::fence_after_sync();
-        const bool masked = (j * kBN + kBN - 1 > q0) || (j * kBN + kBN > p.S_kv);
-        const int key0 = j * kBN;
-        // pass 1: row max of this tile (in log2 units)
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tc::ld_32x32b_x32(t_s + 32 * c, r);
-          tc::wait_ld();
+        uint32_t sv[kBN];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(r[e]);
-            if (!pos_scale) x *= p.sl2;
-            if (masked) {
-              const int kpos = key0 + 32 * c + e;
-              if (kpos > qpos || kpos >= p.S_kv) x = -INFINITY;
-            }
-            mx = fmaxf(mx, x);
-          }
+        for (int c = 0; c < kBN / 32; ++c) tc::ld32(t_s + 32 * c, sv + 32 * c);
+        tc::wait_ld();
+        if (!pos_scale) {
+#pragma unroll
+          for (int e = 0; e < kBN; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * p.sl2);
         }
+        const bool masked = (j * kBN + kBN - 1 > q0) || (j * kBN + kBN > p.S_kv);
+        if (masked) {
+          const int lim = min(qpos + 1, p.S_kv) - j * kBN;  // keys [0, lim) of the tile visible
+#pragma unroll
+          for (int e = 0; e < kBN; ++e)
+            if (e >= lim) sv[e] = __float_as_uint(-INFINITY);
+        }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < kBN; e += 4)
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) mx4[k4] = fmaxf(mx4[k4], __uint_as_float(sv[e + k4]));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float mt = pos_scale ? mx * p.sl2 : mx;
         if (j == 0) {
           m_ref = mt;  // key 0 is visible to every row: finite
+        } else if (__any_sync(0xffffffffu, mt > m_ref + kRescaleThreshold)) {
+          const float m_new = fmaxf(m_ref, mt);
+          const float corr = fast_exp2(m_ref - m_new);
+          l *= corr;
+          // O_i holds P V up to tile j-1 (complete: S_i(j) was issued after it)
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tc::ld32(t_o + 32 * c, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+            tc::st32(t_o + 32 * c, r);
+          }
+          tc::wait_st();
+          m_ref = m_new;
+        }
+        // exp turn: head 0's tile k follows head 1's tile k-1, head 1's tile k follows
+        // head 0's tile k, so only one warpgroup feeds the exp unit at a time
+        if (i == 0) {
+          ready = tile == 0 || wait_abortable(tok(0), (tile - 1) & 1, p.wait, abort_flag);
         } else {
-          const bool need = mt > m_ref + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            const float m_new = fmaxf(m_ref, mt);
-            const float corr = fast_exp2(m_ref - m_new);
-            l *= corr;
-            // O_i holds P V up to tile j-1 (complete: S_i(j) was issued after it)
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t r[32];
-              tc::ld_32x32b_x32(t_o + 32 * c, r);
-              tc::wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
-              tc::st_32x32b_x32(t_o + 32 * c, r);
-            }
-            tc::wait_st();
-            m_ref = m_new;
-          }
+          ready = wait_abortable(tok(1), tile & 1, p.wait, abort_flag);
         }
-        // pass 2: P = exp2(s * scale log2e - m_ref) as bf16 into shared memory
+        if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+        // P = exp2(s * scale log2e - m_ref) -> bf16 pairs over columns 0..63 of S_i
         const float negm = -m_ref;
-        float rs = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tc::ld_32x32b_x32(t_s + 32 * c, r);
-          tc::wait_ld();
+        float rs0 = 0.f, rs1 = 0.f;
+        uint32_t pk[kBN / 2];
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            float e8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float x = __uint_as_float(r[8 * q8 + e]);
-              float pe = fast_exp2(fmaf(x, p.sl2, negm));
-              if (masked) {
-                const int kpos = key0 + 32 * c + 8 * q8 + e;
-                if (kpos > qpos || kpos >= p.S_kv) pe = 0.f;
-              }
-              e8[e] = pe;
-              rs += pe;
-            }
-            const int chunk = 4 * c + q8;  // 16-byte chunk 0..15 of the row
-            const uint32_t addr =
-                p_row + (chunk >> 3) * kHalfBytes + (((chunk & 7) ^ (row & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                         "r"(pack_bf16x2(e8[0], e8[1])), "r"(pack_bf16x2(e8[2], e8[3])),
-                         "r"(pack_bf16x2(e8[4], e8[5])), "r"(pack_bf16x2(e8[6], e8[7]))
-                         : "memory");
-          }
+        for (int e = 0; e < kBN / 2; ++e) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * e]), mul, negm));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), mul, negm));
+          rs0 += p0;
+          rs1 += p1;
+          pk[e] = pack_bf16x2(p0, p1);
         }
-        l += rs;
-        fence_proxy_async_smem();  // P visible to the tensor core
-        tc::fence_before_sync();   // O rescale stores ordered before the signal
+        tc::st32(t_s, pk);
+        tc::st32(t_s + 32, pk + 32);
+        tc::wait_st();
+        l += rs0 + rs1;
+        tc::fence_before_sync();
         mbar_arrive(p_full(i));
+        mbar_arrive(tok(1 - i));
       }
       if (!ok) break;
       // epilogue: O / l -> bf16, lse = m_ref ln2 + ln l
@@ -379,37 +377,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qrow = w.qt * kBM + row;
       const bool store = (i == 0 || w.second_valid) && qrow < p.T_q;
       const size_t orow = ((size_t)w.b * p.H_q + h) * p.T_q + qrow;
-      const float inv_l = 1.f / l;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tc::ld_32x32b_x32(t_o + 32 * c, r);
-        tc::wait_ld();
-        if (store) {
-          uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD + 32 * c);
+      uint32_t ov[kD];
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 pk;
-            pk.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * inv_l,
-                               __uint_as_float(r[8 * v4 + 1]) * inv_l);
-            pk.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * inv_l,
-                               __uint_as_float(r[8 * v4 + 3]) * inv_l);
-            pk.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * inv_l,
-                               __uint_as_float(r[8 * v4 + 5]) * inv_l);
-            pk.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * inv_l,
-                               __uint_as_float(r[8 * v4 + 7]) * inv_l);
-            dst[v4] = pk;
-          }
+      for (int c = 0; c < kD / 32; ++c) tc::ld32(t_o + 32 * c, ov + 32 * c);
+      tc::wait_ld();
+      if (store) {
+        const float inv_l = 1.f / l;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD);
+#pragma unroll
+        for (int v8 = 0; v8 < kD / 8; ++v8) {
+          uint4 pk4;
+          pk4.x = pack_bf16x2(__uint_as_float(ov[8 * v8 + 0]) * inv_l,
+                              __uint_as_float(ov[8 * v8 + 1]) * inv_l);
+          pk4.y = pack_bf16x2(__uint_as_float(ov[8 * v8 + 2]) * inv_l,
+                              __uint_as_float(ov[8 * v8 + 3]) * inv_l);
+          pk4.z = pack_bf16x2(__uint_as_float(ov[8 * v8 + 4]) * inv_l,
+                              __uint_as_float(ov[8 * v8 + 5]) * inv_l);
+          pk4.w = pack_bf16x2(__uint_as_float(ov[8 * v8 + 6]) * inv_l,
+                              __uint_as_float(ov[8 * v8 + 7]) * inv_l);
+          dst[v8] = pk4;
         }
+        p.lse[orow] = m_ref * 0.69314718055994531f + logf(l);
       }
-      if (store) p.lse[orow] = m_ref * 0.69314718055994531f + logf(l);
       tc::fence_before_sync();  // O reads done before the next unit's first P signal
     }
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
