@@ -36,13 +36,23 @@ namespace decode {
 
 constexpr int kD = 128;
 constexpr int kTileKeys = kDecodeTileKeys;          // 64
-constexpr int kStages = 3;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 160
 constexpr int kHalfBytes = kTileKeys * 128;          // 64 keys x 64 d x 2 B = 8 KiB
 constexpr int kStageBytes = 4 * kHalfBytes;          // K lo/hi + V lo/hi = 32 KiB
-constexpr int kBarrierBytes = 2 * kStages * 8;
-constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // + alignment slack
+// Ring depth: 3 stages (96 KiB) per CTA, two CTAs per SM for plans that run
+// several waves (a finishing CTA's epilogue overlaps its neighbour's
+// streaming).  Single-wave plans run one CTA per SM with kOneWaveStages (4)
+// stages; deeper rings measured slower on GB300 (more bytes in flight only
+// queue longer in the memory system).
+#ifndef GQA_DECODE_ONE_WAVE_STAGES
+#define GQA_DECODE_ONE_WAVE_STAGES 4
+#endif
+constexpr int kOneWaveStages = GQA_DECODE_ONE_WAVE_STAGES;
+template <int kStages>
+constexpr int smem_bytes() {
+  return kStages * kStageBytes + 2 * kStages * 8 + 1024;  // ring + barriers + alignment slack
+}
 constexpr int kRedStride = kD + 4;  // padded row of the per-warp O reduction buffer
 
 struct Params {
@@ -67,7 +77,8 @@ __device__ __forceinline__ uint32_t tile_offset(int r, int chunk) {
   return half * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+template <int kStages, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -77,14 +88,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t *empty_bar = full_bar + kStages;
 
   const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
-  const int seqlen = min(max(p.seqlens[b], 0), p.S_max);
-  const int key_begin = split * p.chunk;
-  const int key_end = min(key_begin + p.chunk, seqlen);
-  if (key_begin >= key_end) return;  // empty split: the merge never reads it
-  const int n_tiles = (key_end - key_begin + kTileKeys - 1) / kTileKeys;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ int failed;
+  // prologue that reads no input: overlaps the previous kernel when this grid
+  // was launched as its programmatic dependent
   if (threadIdx.x == 0) {
     failed = 0;
     for (int s = 0; s < kStages; ++s) {
@@ -93,6 +100,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     fence_mbar_init();
   }
+  if (warp == kConsumerWarps && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs written before us are visible
+
+  const int seqlen = min(max(p.seqlens[b], 0), p.S_max);
+  const int key_begin = split * p.chunk;
+  const int key_end = min(key_begin + p.chunk, seqlen);
+  if (key_begin >= key_end) return;  // empty split: the merge never reads it
+  const int n_tiles = (key_end - key_begin + kTileKeys - 1) / kTileKeys;
   __syncthreads();
 
   float m_run[2], l_run[2], o_acc[8][4];
@@ -100,8 +118,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == kConsumerWarps) {
     // ---------------- producer: one thread issues all TMA loads ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       const uint64_t pol = l2_policy_evict_first();
       const int row = b * p.H_kv + kv;
       int issued = 0;
@@ -300,6 +316,8 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ float4 red_o[kMergeGroups][32];
   __shared__ float red_w[kMergeGroups];
   __shared__ float red_m[kMergeGroups];
+  // the next kernel (typically the next layer's split) may start its prologue
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int h = blockIdx.x, b = blockIdx.y;
   const int t = threadIdx.x, grp = t >> 5, lane = t & 31;
@@ -373,8 +391,14 @@ static CUresult make_kv_map(CUtensorMap *map, const uint16_t *base, int B, int H
 }  // namespace decode
 
 cudaError_t decode_prepare_device() {
-  return cudaFuncSetAttribute(decode::decode_split_kernel,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, decode::kSmemBytes);
+  using namespace decode;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<3, 2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes<3>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_split_kernel<kOneWaveStages, 1>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes<kOneWaveStages>());
 }
 
 cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
@@ -399,9 +423,22 @@ cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
     p.chunk = a.chunk;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait = a.wait;
-    dim3 grid(a.num_splits, a.H_kv, a.B);
-    decode_split_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_v, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_splits, a.H_kv, a.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const long long ctas = (long long)a.num_splits * a.H_kv * a.B;
+    if (ctas <= a.num_sms) {  // one wave, one CTA per SM
+      cfg.dynamicSmemBytes = smem_bytes<kOneWaveStages>();
+      return cudaLaunchKernelEx(&cfg, decode_split_kernel<kOneWaveStages, 1>, tm_k, tm_v, p);
+    }
+    cfg.dynamicSmemBytes = smem_bytes<3>();
+    return cudaLaunchKernelEx(&cfg, decode_split_kernel<3, 2>, tm_k, tm_v, p);
   }
   return cudaSuccess;
 }

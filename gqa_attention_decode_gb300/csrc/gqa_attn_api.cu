@@ -18,7 +18,8 @@ __device__ int g_wait_status;
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxDevices = 64;
-constexpr int kMaxChunkTiles = 32;  // automatic plan: at most 2048 keys per split
+constexpr int kMaxChunkTiles = 32;          // multi-wave plans: at most 2048 keys per split
+constexpr int kMaxChunkTilesOneWave = 32;   // single-wave plans: at most 2048 keys per split
 constexpr int kDecodeCtasPerSm = 2;
 
 struct DeviceState {
@@ -71,10 +72,12 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-// Plan: chunks of whole 64-key tiles.  Automatic: enough splits that one wave
-// of kDecodeCtasPerSm CTAs per SM covers B*H_kv*splits, but no chunk longer
-// than kMaxChunkTiles tiles (long caches then run several waves, which keeps
-// ragged batches balanced).
+// Plan: chunks of whole 64-key tiles.  Automatic:
+//  * if one CTA per SM can cover every (batch, KV head) with chunks of at most
+//    kMaxChunkTilesOneWave tiles, use exactly that single wave (no tail, the
+//    fixed per-CTA cost paid once, a deep ring per CTA);
+//  * otherwise chunks of at most kMaxChunkTiles tiles so that two waves' worth
+//    of CTAs per SM keep ragged batches balanced.
 int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_splits,
          int *out_chunk) {
   if (B < 0 || H_kv <= 0 || S_max < 0 || num_sms <= 0 || num_splits < 0) return GQA_ERR_INVALID_ARG;
@@ -86,10 +89,13 @@ int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_split
     return GQA_OK;
   }
   int chunk_tiles;
+  const long long units = (long long)B * H_kv;
   if (num_splits > 0) {
     chunk_tiles = ceil_div(tiles, num_splits < tiles ? num_splits : tiles);
+  } else if (units <= num_sms &&
+             ceil_div(tiles, num_sms / units) <= kMaxChunkTilesOneWave) {
+    chunk_tiles = ceil_div(tiles, num_sms / units);
   } else {
-    const long long units = (long long)B * H_kv;
     const long long want = (long long)num_sms * kDecodeCtasPerSm;
     const int fill = static_cast<int>((want + units - 1) / units);  // splits per unit
     chunk_tiles = ceil_div(tiles, fill < 1 ? 1 : fill);
@@ -236,6 +242,7 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   a.lse = lse;
   a.o_part = static_cast<float *>(const_cast<void *>(workspace));
   a.lse_part = a.o_part + (size_t)B * H_q * splits * d;
+  a.num_sms = st->num_sms;
   a.wait.status = st->status;
   a.wait.timeout_ns = kWaitTimeoutNs;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -22,6 +22,7 @@ struct DecodeLaunch {
   float *lse;       // [B, H_q]
   float *o_part;    // [B, H_q, num_splits, d]
   float *lse_part;  // [B, H_q, num_splits]
+  int num_sms;
   WaitCtl wait;
 };
 
