@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--parts", default="decode,prefill",
                     help="comma list of decode,prefill (both by default)")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="decode calls per step, each on its own K/V copy")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -307,7 +309,8 @@ def run_ours(args, rank, world, device):
     seqlens = seqlens_cpu.to(device)
     # LAYERS copies of the cache (one per decoded layer), so consecutive calls
     # never find their K/V in L2
-    kv_copies = [(k, v)] + [(k.clone(), v.clone()) for _ in range(LAYERS - 1)]
+    layers = max(1, args.layers)
+    kv_copies = [(k, v)] + [(k.clone(), v.clone()) for _ in range(layers - 1)]
     splits, chunk = gqa.gqa_attn_decode_plan(wd.B, wd.H_kv, wd.S_max, sms, wd.num_splits)
     ws = torch.empty(gqa.gqa_attn_decode_workspace_size(wd.B, wd.H_q, wd.H_kv, wd.S_max, wd.d,
                                                         sms, wd.num_splits),
@@ -326,7 +329,7 @@ def run_ours(args, rank, world, device):
 
     launches_per_step = 0
     if "decode" in parts:
-        launches_per_step += 3 * LAYERS     # LAYERS x (split + merge) + LAYERS x split
+        launches_per_step += 3 * layers     # layers x (split + merge) + layers x split
     if "prefill" in parts:
         launches_per_step += 1
 
@@ -406,8 +409,8 @@ def run_ours(args, rank, world, device):
     region_ms = region0.elapsed_time(region1)
     decode_ms = split_ms = prefill_ms = 0.0
     if "decode" in parts:
-        decode_ms = sum(e[0].elapsed_time(e[1]) for e in events) / LAYERS
-        split_ms = sum(e[2].elapsed_time(e[3]) for e in events) / LAYERS
+        decode_ms = sum(e[0].elapsed_time(e[1]) for e in events) / layers
+        split_ms = sum(e[2].elapsed_time(e[3]) for e in events) / layers
     if "prefill" in parts:
         prefill_ms = sum(e[4].elapsed_time(e[5]) for e in events)
     # max over ranks of every time
@@ -426,9 +429,9 @@ def run_ours(args, rank, world, device):
                    "d": wd.d, "S_kv": wd.S_max, "num_splits": splits, "chunk_keys": chunk,
                    "prefill_workload": PREFILL_WORKLOAD if "prefill" in parts else None,
                    "step": "+".join(p for p in ("decode", "prefill") if p in parts),
-                   "layers_per_step": LAYERS,
-                   "l2": (f"each of the {LAYERS} decode calls of a step reads its own 128 MiB "
-                          f"K/V copy ({LAYERS * 128} MiB rotating set > 126 MB L2)"),
+                   "layers_per_step": layers,
+                   "l2": (f"each of the {layers} decode calls of a step reads its own 128 MiB "
+                          f"K/V copy ({layers * 128} MiB rotating set)"),
                    "parallelism": f"{world} independent replicas (weak scaling)",
                    "launch": "each ABI call replayed as a captured CUDA graph"},
         "gpu_launches": launches_per_step * K,
