@@ -327,9 +327,13 @@ def run_ours(args, rank, world, device):
         plse = torch.empty((wp.B, wp.H_q, wp.T_q), dtype=torch.float32, device=device)
     flops_prefill = prefill_flops(wp)
 
+    # kernels one gqa_attn_decode call launches: 1 (cluster-merged single kernel)
+    # or 2 (split + merge); with 2, a split-only graph times the dominant kernel
+    call_kernels = gqa.gqa_attn_decode_kernel_count(wd.B, wd.H_q, wd.H_kv, wd.S_max, wd.d,
+                                                    wd.num_splits, device)
     launches_per_step = 0
     if "decode" in parts:
-        launches_per_step += 3 * layers     # layers x (split + merge) + layers x split
+        launches_per_step += layers * call_kernels + (layers if call_kernels == 2 else 0)
     if "prefill" in parts:
         launches_per_step += 1
 
@@ -349,7 +353,9 @@ def run_ours(args, rank, world, device):
 
     calls = {}
     if "decode" in parts:
-        calls.update(decode=call_decode_layers, split=call_split_layers)
+        calls["decode"] = call_decode_layers
+        if call_kernels == 2:
+            calls["split"] = call_split_layers
     if "prefill" in parts:
         calls["prefill"] = call_prefill
     for _ in range(max(args.warmup, 3)):          # eager warm-up (also per-device set-up)
@@ -374,9 +380,10 @@ def run_ours(args, rank, world, device):
             ev[0].record(stream)
             graphs["decode"].replay()
             ev[1].record(stream)
-            ev[2].record(stream)
-            graphs["split"].replay()
-            ev[3].record(stream)
+            if "split" in graphs:
+                ev[2].record(stream)
+                graphs["split"].replay()
+                ev[3].record(stream)
         if "prefill" in parts:
             ev[4].record(stream)
             graphs["prefill"].replay()
@@ -410,7 +417,8 @@ def run_ours(args, rank, world, device):
     decode_ms = split_ms = prefill_ms = 0.0
     if "decode" in parts:
         decode_ms = sum(e[0].elapsed_time(e[1]) for e in events) / layers
-        split_ms = sum(e[2].elapsed_time(e[3]) for e in events) / layers
+        split_ms = (sum(e[2].elapsed_time(e[3]) for e in events) / layers
+                    if "split" in graphs else decode_ms)
     if "prefill" in parts:
         prefill_ms = sum(e[4].elapsed_time(e[5]) for e in events)
     # max over ranks of every time
@@ -441,12 +449,15 @@ def run_ours(args, rank, world, device):
         value = world * bytes_decode / (call_ms * 1e-3) / 1e9
         achieved = bytes_decode / (split_ms / K * 1e-3) / 1e9
         result["value"] = value
-        result["decode"] = {"call_us": call_ms * 1e3, "split_us": split_ms / K * 1e3,
+        kernel = ("decode_split_kernel (single launch, cluster merge)" if call_kernels == 1
+                  else "decode_split_kernel")
+        result["decode"] = {"call_us": call_ms * 1e3, "kernels_per_call": call_kernels,
+                            "split_us": split_ms / K * 1e3,
                             "merge_and_gap_us": (decode_ms - split_ms) / K * 1e3,
                             "bytes_per_call": bytes_decode,
                             "frac_of_hbm_peak": value / world / peaks["hbm_gbs"],
                             "frac_of_8tbs_nominal": value / world / 8000.0}
-        result["roofline"] = {"bound": "hbm", "kernel": "decode_split_kernel",
+        result["roofline"] = {"bound": "hbm", "kernel": kernel,
                               "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": achieved / peaks["hbm_gbs"],
                               "traffic": recorded_traffic("decode_split_kernel"),

@@ -34,6 +34,7 @@ _SIGNATURES = {
     "gqa_attn_decode_workspace_size": (_c_size, [_c_int] * 7),
     "gqa_attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                  _c_float, _c_int, _vp, _vp, _vp, _c_size, _vp]),
+    "gqa_attn_decode_kernel_count": (_c_int, [_c_int] * 6 + [_ip]),
     "gqa_attn_decode_split": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                        _c_int, _c_float, _c_int, _vp, _c_size, _vp]),
     "gqa_attn_decode_merge": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
@@ -179,6 +180,17 @@ def gqa_attn_decode(q, k_cache, v_cache, seqlens, scale, num_splits=0, o=None, l
                                  _stream_handle(stream, dev))
     _check(rc, "gqa_attn_decode")
     return o, lse
+
+
+def gqa_attn_decode_kernel_count(B, H_q, H_kv, S_max, d, num_splits=0, device=None) -> int:
+    """Kernels gqa_attn_decode launches for these sizes on the device (1 or 2)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    out = ctypes.c_int(-1)
+    with torch.cuda.device(dev):
+        _check(load_library().gqa_attn_decode_kernel_count(B, H_q, H_kv, S_max, d, num_splits,
+                                                           ctypes.byref(out)),
+               "gqa_attn_decode_kernel_count")
+    return out.value
 
 
 def gqa_attn_decode_split(q, k_cache, v_cache, seqlens, scale, num_splits, workspace,

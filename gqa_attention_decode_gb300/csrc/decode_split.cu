@@ -54,12 +54,15 @@ constexpr int smem_bytes() {
   return kStages * kStageBytes + 2 * kStages * 8 + 1024;  // ring + barriers + alignment slack
 }
 constexpr int kRedStride = kD + 4;  // padded row of the per-warp O reduction buffer
+constexpr int kMaxFusedSplits = kDecodeMaxFusedSplits;  // largest cluster of the fused variant
 
 struct Params {
   const uint16_t *q;
   const int32_t *seqlens;
   float *o_part;
   float *lse_part;
+  uint16_t *o;  // fused variant: final outputs
+  float *lse;
   int B, H_q, H_kv, G, S_max, num_splits, chunk;
   float scale_log2;  // scale * log2(e)
   WaitCtl wait;
@@ -77,7 +80,12 @@ __device__ __forceinline__ uint32_t tile_offset(int r, int chunk) {
   return half * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4);
 }
 
-template <int kStages, int kMinBlocks>
+// kFused = false: each CTA writes its split partial to the workspace and the
+// merge kernel combines them.  kFused = true: the num_splits CTAs of one
+// (sequence, KV head) form a thread-block cluster; each keeps its partial in
+// shared memory and the cluster merges them through distributed shared memory,
+// so one launch produces o and lse and no workspace is touched.
+template <int kStages, int kMinBlocks, bool kFused>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -109,8 +117,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   const int seqlen = min(max(p.seqlens[b], 0), p.S_max);
   const int key_begin = split * p.chunk;
   const int key_end = min(key_begin + p.chunk, seqlen);
-  if (key_begin >= key_end) return;  // empty split: the merge never reads it
-  const int n_tiles = (key_end - key_begin + kTileKeys - 1) / kTileKeys;
+  if (!kFused && key_begin >= key_end) return;  // empty split: the merge never reads it
+  // (a fused CTA with no keys still takes part in the cluster merge)
+  const int n_tiles = max(0, (key_end - key_begin + kTileKeys - 1) / kTileKeys);
   __syncthreads();
 
   float m_run[2], l_run[2], o_acc[8][4];
@@ -254,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     }
   }
   __syncthreads();
-  if (failed) return;
+  if (!kFused && failed) return;
 
   // ---------------- merge the four warp states, write the split partial ----------------
   // All loads have landed and been consumed; the stage ring is free.
@@ -279,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     }
   }
   __syncthreads();
+  float *cta_o = red_o + kConsumerWarps * 8 * kRedStride;  // fused: [8][kD] normalised O_s
+  float *cta_lse = cta_o + 8 * kD;                          // fused: [8] lse_s
   if (threadIdx.x < kD) {
     const int dd = threadIdx.x;
     for (int n = 0; n < p.G; ++n) {
@@ -292,10 +303,44 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         lsum += red_l[w * 8 + n] * f;
         osum += red_o[(w * 8 + n) * kRedStride + dd] * f;
       }
-      const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + n) * p.num_splits + split;
-      p.o_part[row * kD + dd] = osum / lsum;
-      if (dd == 0) p.lse_part[row] = mmax * 0.69314718055994531f + logf(lsum);
+      if (kFused) {
+        const bool empty = failed || mmax == -INFINITY;
+        cta_o[n * kD + dd] = empty ? 0.f : osum / lsum;
+        if (dd == 0) cta_lse[n] = empty ? -INFINITY : mmax * 0.69314718055994531f + logf(lsum);
+      } else {
+        const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + n) * p.num_splits + split;
+        p.o_part[row * kD + dd] = osum / lsum;
+        if (dd == 0) p.lse_part[row] = mmax * 0.69314718055994531f + logf(lsum);
+      }
     }
+  }
+  if (kFused) {
+    // log-sum-exp merge across the cluster: CTA r finalises heads r, r + splits, ...
+    cluster_sync();
+    const int cs = p.num_splits;
+    const uint32_t rank = cluster_ctarank();
+    if (threadIdx.x < kD) {
+      const int dd = threadIdx.x;
+      constexpr float kLog2e = 1.4426950408889634f;
+      for (int n = (int)rank; n < p.G; n += cs) {
+        const uint32_t lse_at = smem_u32(cta_lse + n), o_at = smem_u32(cta_o + n * kD + dd);
+        float mx = -INFINITY;
+        for (int c = 0; c < cs; ++c) mx = fmaxf(mx, ld_dsmem_f32(dsmem_addr(lse_at, c)));
+        float wsum = 0.f, acc = 0.f;
+        if (mx != -INFINITY) {
+          for (int c = 0; c < cs; ++c) {
+            const float w = fast_exp2((ld_dsmem_f32(dsmem_addr(lse_at, c)) - mx) * kLog2e);
+            wsum += w;
+            acc = fmaf(w, ld_dsmem_f32(dsmem_addr(o_at, c)), acc);
+          }
+        }
+        const size_t row = (size_t)b * p.H_q + (size_t)kv * p.G + n;
+        const __nv_bfloat16 r = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+        p.o[row * kD + dd] = *reinterpret_cast<const uint16_t *>(&r);
+        if (dd == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+      }
+    }
+    cluster_sync();  // no CTA leaves while others still read its shared memory
   }
   // this CTA's partial is written: the merge grid may be scheduled
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -390,57 +435,129 @@ static CUresult make_kv_map(CUtensorMap *map, const uint16_t *base, int B, int H
 
 }  // namespace decode
 
-cudaError_t decode_prepare_device() {
+template <int kStages, int kMinBlocks, bool kFused>
+static cudaError_t set_smem_attr() {
   using namespace decode;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<3, 2>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes<3>());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_split_kernel<kOneWaveStages, 1>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem_bytes<kOneWaveStages>());
+  return cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<kStages>());
+}
+
+cudaError_t decode_prepare_device(int *fused_clusters) {
+  using namespace decode;
+  cudaError_t e;
+  if ((e = set_smem_attr<3, 2, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<kOneWaveStages, 1, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<kOneWaveStages, 1, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<3, 2, true>()) != cudaSuccess) return e;
+  // For each cluster size (splits per sequence and KV head) the number of
+  // clusters of the fused kernel the device runs at once (the 3-stage variant,
+  // which may pair two CTAs on an SM); 0 where it cannot.  Sizes above 8 need the
+  // non-portable cluster size opt-in.
+  const bool big = cudaFuncSetAttribute(decode_split_kernel<3, 2, true>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                        1) == cudaSuccess;
+  for (int cs = 1; cs <= kMaxFusedSplits; ++cs) {
+    fused_clusters[cs] = 0;
+    if (cs > 8 && !big) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<3>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_split_kernel<3, 2, true>, &cfg) == cudaSuccess)
+      fused_clusters[cs] = n;
+  }
+  cudaGetLastError();  // a refused opt-in or query is not an error for the caller
+  return cudaSuccess;
+}
+
+static bool make_maps(const DecodeLaunch &a, PFN_cuTensorMapEncodeTiled_v12000 encode,
+                      CUtensorMap *tm_k, CUtensorMap *tm_v) {
+  using namespace decode;
+  return make_kv_map(tm_k, a.k_cache, a.B, a.H_kv, a.S_max, encode) == CUDA_SUCCESS &&
+         make_kv_map(tm_v, a.v_cache, a.B, a.H_kv, a.S_max, encode) == CUDA_SUCCESS;
+}
+
+static decode::Params make_params(const DecodeLaunch &a) {
+  decode::Params p;
+  p.q = a.q;
+  p.seqlens = a.seqlens;
+  p.o_part = a.o_part;
+  p.lse_part = a.lse_part;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.B = a.B;
+  p.H_q = a.H_q;
+  p.H_kv = a.H_kv;
+  p.G = a.H_q / a.H_kv;
+  p.S_max = a.S_max;
+  p.num_splits = a.num_splits;
+  p.chunk = a.chunk;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.wait = a.wait;
+  return p;
+}
+
+bool decode_fused_eligible(const DecodeLaunch &a) {
+  // one launch only when every (sequence, KV head) cluster runs in a single wave
+  if (a.S_max <= 0 || a.num_splits < 1 || a.num_splits > decode::kMaxFusedSplits) return false;
+  return (long long)a.B * a.H_kv <= a.fused_clusters[a.num_splits];
+}
+
+cudaError_t decode_fused_launch(const DecodeLaunch &a, cudaStream_t stream,
+                                PFN_cuTensorMapEncodeTiled_v12000 encode) {
+  using namespace decode;
+  if (!decode_fused_eligible(a)) return cudaErrorNotSupported;
+  CUtensorMap tm_k, tm_v;
+  if (!make_maps(a, encode, &tm_k, &tm_v)) return cudaErrorInvalidValue;
+  const Params p = make_params(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_splits, a.H_kv, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.num_splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cfg.dynamicSmemBytes = smem_bytes<3>();
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<3, 2, true>, tm_k, tm_v, p);
 }
 
 cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
                                 PFN_cuTensorMapEncodeTiled_v12000 encode) {
   using namespace decode;
-  if (a.S_max > 0) {
-    CUtensorMap tm_k, tm_v;
-    if (make_kv_map(&tm_k, a.k_cache, a.B, a.H_kv, a.S_max, encode) != CUDA_SUCCESS ||
-        make_kv_map(&tm_v, a.v_cache, a.B, a.H_kv, a.S_max, encode) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-    Params p;
-    p.q = a.q;
-    p.seqlens = a.seqlens;
-    p.o_part = a.o_part;
-    p.lse_part = a.lse_part;
-    p.B = a.B;
-    p.H_q = a.H_q;
-    p.H_kv = a.H_kv;
-    p.G = a.H_q / a.H_kv;
-    p.S_max = a.S_max;
-    p.num_splits = a.num_splits;
-    p.chunk = a.chunk;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.wait = a.wait;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_splits, a.H_kv, a.B);
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const long long ctas = (long long)a.num_splits * a.H_kv * a.B;
-    if (ctas <= a.num_sms) {  // one wave, one CTA per SM
-      cfg.dynamicSmemBytes = smem_bytes<kOneWaveStages>();
-      return cudaLaunchKernelEx(&cfg, decode_split_kernel<kOneWaveStages, 1>, tm_k, tm_v, p);
-    }
-    cfg.dynamicSmemBytes = smem_bytes<3>();
-    return cudaLaunchKernelEx(&cfg, decode_split_kernel<3, 2>, tm_k, tm_v, p);
+  if (a.S_max <= 0) return cudaSuccess;
+  CUtensorMap tm_k, tm_v;
+  if (!make_maps(a, encode, &tm_k, &tm_v)) return cudaErrorInvalidValue;
+  const Params p = make_params(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_splits, a.H_kv, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const long long ctas = (long long)a.num_splits * a.H_kv * a.B;
+  if (ctas <= a.num_sms) {  // one wave, one CTA per SM
+    cfg.dynamicSmemBytes = smem_bytes<kOneWaveStages>();
+    return cudaLaunchKernelEx(&cfg, decode_split_kernel<kOneWaveStages, 1, false>, tm_k, tm_v, p);
   }
-  return cudaSuccess;
+  cfg.dynamicSmemBytes = smem_bytes<3>();
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<3, 2, false>, tm_k, tm_v, p);
 }
 
 cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream) {

@@ -25,6 +25,7 @@ constexpr int kDecodeCtasPerSm = 2;
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
+  int fused_clusters[gqa::kDecodeMaxFusedSplits + 1] = {};
   int *status = nullptr;
 };
 
@@ -57,7 +58,7 @@ int device_state(DeviceState **out) {
       return GQA_ERR_CUDA;
     void *status = nullptr;
     if (cudaGetSymbolAddress(&status, g_wait_status) != cudaSuccess) return GQA_ERR_CUDA;
-    if (gqa::decode_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
+    if (gqa::decode_prepare_device(st.fused_clusters) != cudaSuccess) return GQA_ERR_CUDA;
     if (gqa::prefill_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
     st.num_sms = sms;
     st.status = static_cast<int *>(status);
@@ -78,6 +79,9 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 //    fixed per-CTA cost paid once, a deep ring per CTA);
 //  * otherwise chunks of at most kMaxChunkTiles tiles so that two waves' worth
 //    of CTAs per SM keep ragged batches balanced.
+// Splits per (sequence, KV head) of a single-wave plan: one CTA per SM.
+int one_wave_splits(long long units, int num_sms) { return (int)(num_sms / units); }
+
 int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_splits,
          int *out_chunk) {
   if (B < 0 || H_kv <= 0 || S_max < 0 || num_sms <= 0 || num_splits < 0) return GQA_ERR_INVALID_ARG;
@@ -93,8 +97,8 @@ int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_split
   if (num_splits > 0) {
     chunk_tiles = ceil_div(tiles, num_splits < tiles ? num_splits : tiles);
   } else if (units <= num_sms &&
-             ceil_div(tiles, num_sms / units) <= kMaxChunkTilesOneWave) {
-    chunk_tiles = ceil_div(tiles, num_sms / units);
+             ceil_div(tiles, one_wave_splits(units, num_sms)) <= kMaxChunkTilesOneWave) {
+    chunk_tiles = ceil_div(tiles, one_wave_splits(units, num_sms));
   } else {
     const long long want = (long long)num_sms * kDecodeCtasPerSm;
     const int fill = static_cast<int>((want + units - 1) / units);  // splits per unit
@@ -243,9 +247,13 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   a.o_part = static_cast<float *>(const_cast<void *>(workspace));
   a.lse_part = a.o_part + (size_t)B * H_q * splits * d;
   a.num_sms = st->num_sms;
+  a.fused_clusters = st->fused_clusters;
   a.wait.status = st->status;
   a.wait.timeout_ns = kWaitTimeoutNs;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (phase == kPhaseBoth && gqa::decode_fused_eligible(a)) {
+    return gqa::decode_fused_launch(a, s, g_encode) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  }
   if (phase & kPhaseSplit) {
     if (gqa::decode_split_launch(a, s, g_encode) != cudaSuccess) return GQA_ERR_CUDA;
   }
@@ -265,6 +273,31 @@ GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                             gqa_stream_t stream) {
   return decode_phase(kPhaseBoth, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
                       num_splits, o, lse, workspace, ws_bytes, stream);
+}
+
+GQA_API int gqa_attn_decode_kernel_count(int B, int H_q, int H_kv, int S_max, int d,
+                                         int num_splits, int *out_kernels) {
+  if (!out_kernels) return GQA_ERR_INVALID_ARG;
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || S_max < 0 || d <= 0 || num_splits < 0 ||
+      H_q % H_kv != 0)
+    return GQA_ERR_INVALID_ARG;
+  if (B == 0) {
+    *out_kernels = 0;
+    return GQA_OK;
+  }
+  DeviceState *st = nullptr;
+  int rc = device_state(&st);
+  if (rc != GQA_OK) return rc;
+  int splits = 0, chunk = 0;
+  if ((rc = plan(B, H_kv, S_max, st->num_sms, num_splits, &splits, &chunk)) != GQA_OK) return rc;
+  gqa::DecodeLaunch a = {};
+  a.B = B;
+  a.H_kv = H_kv;
+  a.S_max = S_max;
+  a.num_splits = splits;
+  a.fused_clusters = st->fused_clusters;
+  *out_kernels = gqa::decode_fused_eligible(a) ? 1 : (S_max > 0 ? 2 : 1);
+  return GQA_OK;
 }
 
 GQA_API int gqa_attn_decode_split(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,

@@ -23,14 +23,24 @@ struct DecodeLaunch {
   float *o_part;    // [B, H_q, num_splits, d]
   float *lse_part;  // [B, H_q, num_splits]
   int num_sms;
+  const int *fused_clusters;  // [kDecodeMaxFusedSplits + 1]: co-resident clusters per size
   WaitCtl wait;
 };
 
 constexpr int kDecodeTileKeys = 64;  // keys per pipeline stage
 constexpr int kDecodeMaxG = 8;       // query heads per KV head that fit the MMA N dimension
+constexpr int kDecodeMaxFusedSplits = 16;  // largest cluster of the single-kernel decode
 
-// One-time per-device kernel attributes (dynamic shared memory opt-in).
-cudaError_t decode_prepare_device();
+// One-time per-device kernel attributes (dynamic shared memory, cluster size
+// opt-in); fills fused_clusters[1..kDecodeMaxFusedSplits] with the number of
+// clusters of that size the single-kernel variant runs at once.
+cudaError_t decode_prepare_device(int *fused_clusters);
+// Single-kernel decode: the splits of one (sequence, KV head) form a cluster and
+// merge through distributed shared memory.  Eligible when every cluster of the
+// plan runs in one wave; cudaErrorNotSupported otherwise.
+bool decode_fused_eligible(const DecodeLaunch &a);
+cudaError_t decode_fused_launch(const DecodeLaunch &a, cudaStream_t stream,
+                                PFN_cuTensorMapEncodeTiled_v12000 encode);
 // Encodes the tensor maps and launches the split kernel (no-op when S_max == 0).
 cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
                                 PFN_cuTensorMapEncodeTiled_v12000 encode);

@@ -138,10 +138,18 @@ GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_ma
  *             on entry do not matter; it is overwritten.
  *   ws_bytes  size of `workspace` in bytes.
  *   stream    cudaStream_t.
- * Launches two kernels on `stream`: the split kernel (one CTA per
- * (split, KV head, batch)) and the log-sum-exp merge.  Deterministic: the
- * same inputs give bit-identical outputs (fixed reduction order, no atomics).
- * B == 0 launches nothing and returns GQA_OK.
+ * Kernels on `stream` (one CTA per (split, KV head, batch)):
+ *   - plans of at most 16 splits whose B*H_kv clusters (one per sequence and
+ *     KV head, one CTA per split) the device runs all at once: ONE kernel;
+ *     the splits of a (sequence, KV head) form a thread-block cluster and
+ *     merge their partials through distributed shared memory; `workspace` is
+ *     not touched;
+ *   - other plans: the split kernel, which writes one partial per split to
+ *     `workspace`, then the log-sum-exp merge kernel (launched as a
+ *     programmatic dependent, so its launch overlaps the split kernel).
+ * gqa_attn_decode_kernel_count reports which.  Deterministic: the same inputs
+ * give bit-identical outputs (fixed reduction order, no atomics).  B == 0
+ * launches nothing and returns GQA_OK.
  */
 GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                             const gqa_bf16_t *v_cache, const int32_t *seqlens, int B,
@@ -150,11 +158,21 @@ GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                             gqa_stream_t stream);
 
 /*
+ * Number of kernels gqa_attn_decode launches for these arguments on the current
+ * device: 1 (single-kernel cluster path), 2 (split + merge), 0 when B == 0.
+ * Host only except for the first call on a device, which performs the
+ * per-device set-up.  Returns the status of the argument checks.
+ */
+GQA_API int gqa_attn_decode_kernel_count(int B, int H_q, int H_kv, int S_max, int d,
+                                         int num_splits, int *out_kernels);
+
+/*
  * The two phases of gqa_attn_decode as separate calls (same arguments, same
  * plan, same workspace).  gqa_attn_decode_split runs the split kernel and
  * leaves the per-split partials in `workspace`; gqa_attn_decode_merge reads
  * them and writes o and lse.  Calling split then merge on one stream is
- * exactly gqa_attn_decode; between the two the workspace must not be touched.
+ * the result of gqa_attn_decode (bit for bit when gqa_attn_decode also runs
+ * split + merge); between the two the workspace must not be touched.
  * split needs q, k_cache, v_cache, seqlens; merge needs seqlens, o, lse (the
  * other pointers may be NULL for the phase that does not use them).
  */

@@ -51,7 +51,7 @@ def test_abi_version_and_status_strings(lib):
 
 
 @pytest.mark.parametrize("B,H_kv,S_max,sms,req,expect", [
-    # one 32K sequence, 8 KV heads, 152 SMs: one wave of 19 splits x 8 heads = 152 CTAs
+    # one 32K sequence, 8 KV heads, 152 SMs: one wave of 19 splits x 8 heads
     (1, 8, 32768, 152, 0, (19, 1728)),
     # 128K keys: chunks capped at 2048 keys, several waves of 2 CTAs/SM
     (1, 8, 131072, 152, 0, (64, 2048)),

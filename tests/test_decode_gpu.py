@@ -105,6 +105,34 @@ def test_group_sizes_below_eight(H_q, H_kv):
     check_full(q, k, v, sl, 1 / math.sqrt(128), 0, f"G={H_q // H_kv}")
 
 
+@pytest.mark.parametrize("num_splits", [1, 2, 5])
+def test_single_kernel_path_matches_two_phase_path(num_splits):
+    """Plans whose clusters all fit in one wave run as one cluster kernel; the
+    explicit split and merge calls always run the two-kernel path.  Both must
+    agree."""
+    q, k, v, sl = gqa_synth.decode_inputs(3, 64, 8, 2000, 128, seed=18, device=DEV,
+                                          seqlens=[2000, 1, 640])
+    sl = sl.to(DEV)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert gqa.gqa_attn_decode_kernel_count(3, 64, 8, 2000, 128, num_splits) == 1
+    o1, l1 = gqa.gqa_attn_decode(q, k, v, sl, 0.088, num_splits=num_splits)
+    ws = torch.empty(gqa.gqa_attn_decode_workspace_size(3, 64, 8, 2000, 128, sms, num_splits),
+                     dtype=torch.uint8, device=DEV)
+    o2 = torch.empty_like(o1)
+    l2 = torch.empty_like(l1)
+    gqa.gqa_attn_decode_split(q, k, v, sl, 0.088, num_splits, ws)
+    gqa.gqa_attn_decode_merge(sl, 8, 2000, num_splits, o2, l2, ws)
+    torch.cuda.synchronize()
+    compare(o1, l1, np64(o2), np64(l2), f"single kernel vs split+merge ({num_splits})")
+    o_ref, lse_ref = oracle.decode(np64(q), np64(k), np64(v), sl.cpu().numpy(), 0.088)
+    compare(o1, l1, o_ref, lse_ref, "single kernel vs oracle")
+
+
+def test_two_kernel_path_for_many_splits():
+    assert gqa.gqa_attn_decode_kernel_count(1, 64, 8, 32768, 128, 37) == 2
+    assert gqa.gqa_attn_decode_kernel_count(1, 8, 1, 256, 128, 4) == 1     # tiny: one cluster
+
+
 def test_nan_padding_is_never_read():
     q, k, v, sl = gqa_synth.decode_inputs(2, 16, 2, 640, 128, seed=13, device=DEV,
                                           seqlens=[577, 100])
