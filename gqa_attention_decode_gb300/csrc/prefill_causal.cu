@@ -59,6 +59,11 @@ constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base slot, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + 1024 alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units (a factor of 256)
+// 1: the two softmax warpgroups alternate their exp phases (a token passed
+// through shared-memory barriers); 0: they run them whenever their S is ready.
+#ifndef GQA_PREFILL_EXP_TURN
+#define GQA_PREFILL_EXP_TURN 1
+#endif
 
 struct Params {
   uint16_t *o;
@@ -340,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::wait_st();
           m_ref = m_new;
         }
+#if GQA_PREFILL_EXP_TURN
         // exp turn: head 0's tile k follows head 1's tile k-1, head 1's tile k follows
         // head 0's tile k, so only one warpgroup feeds the exp unit at a time
         if (i == 0) {
@@ -348,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ready = wait_abortable(tok(1), tile & 1, p.wait, abort_flag);
         }
         if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+#endif
         // P = exp2(s * scale log2e - m_ref) -> bf16 pairs over columns 0..63 of S_i
         const float negm = -m_ref;
         float rs0 = 0.f, rs1 = 0.f;
@@ -366,7 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += rs0 + rs1;
         tc::fence_before_sync();
         mbar_arrive(p_full(i));
+#if GQA_PREFILL_EXP_TURN
         mbar_arrive(tok(1 - i));
+#endif
       }
       if (!ok) break;
       // epilogue: O / l -> bf16, lse = m_ref ln2 + ln l
