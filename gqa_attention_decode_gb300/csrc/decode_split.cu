@@ -63,6 +63,8 @@ struct Params {
   float *lse_part;
   uint16_t *o;  // fused variant: final outputs
   float *lse;
+  const int32_t *block_table;  // paged variant: [B, max_pages]
+  int page_size, max_pages;
   int B, H_q, H_kv, G, S_max, num_splits, chunk;
   float scale_log2;  // scale * log2(e)
   WaitCtl wait;
@@ -85,7 +87,12 @@ __device__ __forceinline__ uint32_t tile_offset(int r, int chunk) {
 // (sequence, KV head) form a thread-block cluster; each keeps its partial in
 // shared memory and the cluster merges them through distributed shared memory,
 // so one launch produces o and lse and no workspace is touched.
-template <int kStages, int kMinBlocks, bool kFused>
+// kPaged = true: K and V live in pages [num_pages, H_kv, page_size, d] and
+// block_table[b][i] names the page that holds keys [i*page_size, (i+1)*page_size)
+// of sequence b (page_size a multiple of the 64-key tile, so no tile straddles
+// two pages).  An out-of-range page id addresses outside the tensor map, which
+// TMA fills with zeros.
+template <int kStages, int kMinBlocks, bool kFused, bool kPaged>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -125,25 +132,46 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   float m_run[2], l_run[2], o_acc[8][4];
 
   if (warp == kConsumerWarps) {
-    // ---------------- producer: one thread issues all TMA loads ----------------
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      const int row = b * p.H_kv + kv;
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
+    // ---------------- producer: lane 0 issues all TMA loads ----------------
+    // (paged: the whole warp keeps 32 block-table entries in registers, so the
+    // page lookup is a shuffle, never a dependent global load per tile)
+    const uint64_t pol = l2_policy_evict_first();
+    const int row = b * p.H_kv + kv;
+    int issued = 0;
+    int page_base = -1 << 30, page_reg = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int key0 = key_begin + i * kTileKeys;
+      int c2 = key0, c3 = row;  // tensor-map coordinates of the tile's first key
+      if (kPaged) {
+        const int page = key0 / p.page_size;
+        if (page - page_base >= 32 || page < page_base) {
+          page_base = page;
+          const int idx = page_base + lane;
+          page_reg = idx < p.max_pages ? __ldg(p.block_table + (size_t)b * p.max_pages + idx) : 0;
+        }
+        const int page_id = __shfl_sync(0xffffffffu, page_reg, page - page_base);
+        c2 = key0 - page * p.page_size;
+        c3 = page_id * p.H_kv + kv;
+      }
+      bool ok = true;
+      if (lane == 0) {
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, p.wait)) break;
-        const uint32_t fb = smem_u32(&full_bar[s]);
-        mbar_arrive_expect_tx(fb, kStageBytes);
-        const uint32_t dst = smem_u32(smem + s * kStageBytes);
-        const int key0 = key_begin + i * kTileKeys;
-        tma_load_4d(dst + 0 * kHalfBytes, &tm_k, fb, 0, 0, key0, row, pol);
-        tma_load_4d(dst + 1 * kHalfBytes, &tm_k, fb, 0, 1, key0, row, pol);
-        tma_load_4d(dst + 2 * kHalfBytes, &tm_v, fb, 0, 0, key0, row, pol);
-        tma_load_4d(dst + 3 * kHalfBytes, &tm_v, fb, 0, 1, key0, row, pol);
-        ++issued;
+        ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, p.wait);
+        if (ok) {
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint32_t dst = smem_u32(smem + s * kStageBytes);
+          tma_load_4d(dst + 0 * kHalfBytes, &tm_k, fb, 0, 0, c2, c3, pol);
+          tma_load_4d(dst + 1 * kHalfBytes, &tm_k, fb, 0, 1, c2, c3, pol);
+          tma_load_4d(dst + 2 * kHalfBytes, &tm_v, fb, 0, 0, c2, c3, pol);
+          tma_load_4d(dst + 3 * kHalfBytes, &tm_v, fb, 0, 1, c2, c3, pol);
+        }
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      ++issued;
+    }
+    if (lane == 0) {
       // Never leave the CTA with a copy in flight: wait for the last loads.
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1, p.wait);
@@ -420,11 +448,13 @@ __global__ void __launch_bounds__(kMergeThreads)
   }
 }
 
-static CUresult make_kv_map(CUtensorMap *map, const uint16_t *base, int B, int H_kv, int S_max,
+// rows = keys per (sequence, KV head) block (S_max, or page_size for pages);
+// blocks = B*H_kv (dense) or num_pages*H_kv (paged)
+static CUresult make_kv_map(CUtensorMap *map, const uint16_t *base, long long blocks, int rows,
                             PFN_cuTensorMapEncodeTiled_v12000 encode) {
-  // dims (innermost first): 64 columns, 2 column halves, S_max keys, B*H_kv heads
-  const cuuint64_t dims[4] = {64, 2, (cuuint64_t)S_max, (cuuint64_t)B * H_kv};
-  const cuuint64_t strides[3] = {128, 256, (cuuint64_t)S_max * 256};  // bytes, dims 1..3
+  // dims (innermost first): 64 columns, 2 column halves, rows, blocks
+  const cuuint64_t dims[4] = {64, 2, (cuuint64_t)rows, (cuuint64_t)blocks};
+  const cuuint64_t strides[3] = {128, 256, (cuuint64_t)rows * 256};  // bytes, dims 1..3
   const cuuint32_t box[4] = {64, 1, kTileKeys, 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(base), dims,
@@ -438,7 +468,11 @@ static CUresult make_kv_map(CUtensorMap *map, const uint16_t *base, int B, int H
 template <int kStages, int kMinBlocks, bool kFused>
 static cudaError_t set_smem_attr() {
   using namespace decode;
-  return cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes<kStages>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<kStages>());
 }
 
@@ -453,7 +487,10 @@ cudaError_t decode_prepare_device(int *fused_clusters) {
   // clusters of the fused kernel the device runs at once (the 3-stage variant,
   // which may pair two CTAs on an SM); 0 where it cannot.  Sizes above 8 need the
   // non-portable cluster size opt-in.
-  const bool big = cudaFuncSetAttribute(decode_split_kernel<3, 2, true>,
+  const bool big = cudaFuncSetAttribute(decode_split_kernel<3, 2, true, false>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                        1) == cudaSuccess &&
+                   cudaFuncSetAttribute(decode_split_kernel<3, 2, true, true>,
                                         cudaFuncAttributeNonPortableClusterSizeAllowed,
                                         1) == cudaSuccess;
   for (int cs = 1; cs <= kMaxFusedSplits; ++cs) {
@@ -471,7 +508,8 @@ cudaError_t decode_prepare_device(int *fused_clusters) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_split_kernel<3, 2, true>, &cfg) == cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, decode_split_kernel<3, 2, true, false>, &cfg) ==
+        cudaSuccess)
       fused_clusters[cs] = n;
   }
   cudaGetLastError();  // a refused opt-in or query is not an error for the caller
@@ -481,8 +519,24 @@ cudaError_t decode_prepare_device(int *fused_clusters) {
 static bool make_maps(const DecodeLaunch &a, PFN_cuTensorMapEncodeTiled_v12000 encode,
                       CUtensorMap *tm_k, CUtensorMap *tm_v) {
   using namespace decode;
-  return make_kv_map(tm_k, a.k_cache, a.B, a.H_kv, a.S_max, encode) == CUDA_SUCCESS &&
-         make_kv_map(tm_v, a.v_cache, a.B, a.H_kv, a.S_max, encode) == CUDA_SUCCESS;
+  const bool paged = a.block_table != nullptr;
+  const long long blocks = paged ? (long long)a.num_pages * a.H_kv : (long long)a.B * a.H_kv;
+  const int rows = paged ? a.page_size : a.S_max;
+  return make_kv_map(tm_k, a.k_cache, blocks, rows, encode) == CUDA_SUCCESS &&
+         make_kv_map(tm_v, a.v_cache, blocks, rows, encode) == CUDA_SUCCESS;
+}
+
+// Launches decode_split_kernel<kStages, kMinBlocks, kFused, paged> for a's layout.
+template <int kStages, int kMinBlocks, bool kFused>
+static cudaError_t launch_variant(cudaLaunchConfig_t *cfg, const CUtensorMap &tm_k,
+                                  const CUtensorMap &tm_v, const decode::Params &p, bool paged) {
+  using namespace decode;
+  cfg->dynamicSmemBytes = smem_bytes<kStages>();
+  if (paged)
+    return cudaLaunchKernelEx(cfg, decode_split_kernel<kStages, kMinBlocks, kFused, true>, tm_k,
+                              tm_v, p);
+  return cudaLaunchKernelEx(cfg, decode_split_kernel<kStages, kMinBlocks, kFused, false>, tm_k,
+                            tm_v, p);
 }
 
 static decode::Params make_params(const DecodeLaunch &a) {
@@ -501,6 +555,9 @@ static decode::Params make_params(const DecodeLaunch &a) {
   p.num_splits = a.num_splits;
   p.chunk = a.chunk;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.block_table = a.block_table;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
   p.wait = a.wait;
   return p;
 }
@@ -531,8 +588,7 @@ cudaError_t decode_fused_launch(const DecodeLaunch &a, cudaStream_t stream,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cfg.dynamicSmemBytes = smem_bytes<3>();
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<3, 2, true>, tm_k, tm_v, p);
+  return launch_variant<3, 2, true>(&cfg, tm_k, tm_v, p, a.block_table != nullptr);
 }
 
 cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
@@ -552,12 +608,10 @@ cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const long long ctas = (long long)a.num_splits * a.H_kv * a.B;
-  if (ctas <= a.num_sms) {  // one wave, one CTA per SM
-    cfg.dynamicSmemBytes = smem_bytes<kOneWaveStages>();
-    return cudaLaunchKernelEx(&cfg, decode_split_kernel<kOneWaveStages, 1, false>, tm_k, tm_v, p);
-  }
-  cfg.dynamicSmemBytes = smem_bytes<3>();
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<3, 2, false>, tm_k, tm_v, p);
+  const bool paged = a.block_table != nullptr;
+  if (ctas <= a.num_sms)  // one wave, one CTA per SM
+    return launch_variant<kOneWaveStages, 1, false>(&cfg, tm_k, tm_v, p, paged);
+  return launch_variant<3, 2, false>(&cfg, tm_k, tm_v, p, paged);
 }
 
 cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream) {

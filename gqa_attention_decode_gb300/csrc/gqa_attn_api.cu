@@ -215,10 +215,16 @@ GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_ma
 }  // extern "C"
 
 namespace {
+struct PagedLayout {
+  const int32_t *block_table;  // nullptr: dense cache
+  int num_pages, page_size, max_pages;
+};
+
 int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                  const gqa_bf16_t *v_cache, const int32_t *seqlens, int B, int H_q, int H_kv,
                  int S_max, int d, float scale, int num_splits, gqa_bf16_t *o, float *lse,
-                 const void *workspace, size_t ws_bytes, gqa_stream_t stream) {
+                 const void *workspace, size_t ws_bytes, gqa_stream_t stream,
+                 const PagedLayout &paged = PagedLayout{nullptr, 0, 0, 0}) {
   int rc = check_decode_args(phase, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
                              num_splits, o, lse);
   if (rc != GQA_OK || B == 0) return rc;
@@ -230,8 +236,12 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   if (!workspace || ws_bytes < need) return GQA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return GQA_ERR_INVALID_ARG;
 
-  gqa::DecodeLaunch a;
+  gqa::DecodeLaunch a = {};
   a.q = q;
+  a.block_table = paged.block_table;
+  a.num_pages = paged.num_pages;
+  a.page_size = paged.page_size;
+  a.max_pages = paged.max_pages;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.seqlens = seqlens;
@@ -273,6 +283,23 @@ GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                             gqa_stream_t stream) {
   return decode_phase(kPhaseBoth, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
                       num_splits, o, lse, workspace, ws_bytes, stream);
+}
+
+GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages,
+                                  const gqa_bf16_t *v_pages, const int32_t *block_table,
+                                  const int32_t *seqlens, int B, int H_q, int H_kv,
+                                  int num_pages, int page_size, int max_pages_per_seq, int d,
+                                  float scale, int num_splits, gqa_bf16_t *o, float *lse,
+                                  void *workspace, size_t ws_bytes, gqa_stream_t stream) {
+  if (num_pages < 0 || max_pages_per_seq < 0 || page_size <= 0) return GQA_ERR_INVALID_ARG;
+  if (page_size % gqa::kDecodeTileKeys != 0) return GQA_ERR_UNSUPPORTED;
+  const long long s_max = (long long)max_pages_per_seq * page_size;
+  if (s_max > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  if (B > 0 && (!block_table || !aligned16(block_table))) return GQA_ERR_INVALID_ARG;
+  if (B > 0 && s_max > 0 && num_pages == 0) return GQA_ERR_INVALID_ARG;
+  const PagedLayout paged{block_table, num_pages, page_size, max_pages_per_seq};
+  return decode_phase(kPhaseBoth, q, k_pages, v_pages, seqlens, B, H_q, H_kv, (int)s_max, d,
+                      scale, num_splits, o, lse, workspace, ws_bytes, stream, paged);
 }
 
 GQA_API int gqa_attn_decode_kernel_count(int B, int H_q, int H_kv, int S_max, int d,

@@ -13,8 +13,10 @@ namespace gqa {
 // ---- decode ----------------------------------------------------------------
 struct DecodeLaunch {
   const uint16_t *q;        // [B, H_q, d]
-  const uint16_t *k_cache;  // [B, H_kv, S_max, d]
-  const uint16_t *v_cache;  // [B, H_kv, S_max, d]
+  const uint16_t *k_cache;  // dense [B, H_kv, S_max, d], or pages [num_pages, H_kv, page_size, d]
+  const uint16_t *v_cache;  // same layout as k_cache
+  const int32_t *block_table;  // paged: [B, max_pages]; nullptr for the dense layout
+  int num_pages, page_size, max_pages;  // paged layout (S_max = max_pages * page_size)
   const int32_t *seqlens;   // [B]
   int B, H_q, H_kv, S_max, num_splits, chunk;
   float scale;

@@ -158,6 +158,32 @@ GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                             gqa_stream_t stream);
 
 /*
+ * Decode over a paged KV cache (block table): the next step beside the
+ * record's per-rank dense buffers (section 2.1), where each sequence's keys
+ * live in fixed-size pages drawn from a shared pool.
+ *
+ *   k_pages, v_pages   device [num_pages, H_kv, page_size, d] bf16: page p holds
+ *                      page_size consecutive keys of one sequence for every KV
+ *                      head; read only; pages may be shared between sequences.
+ *   block_table        device [B, max_pages_per_seq] int32: keys
+ *                      [i*page_size, (i+1)*page_size) of sequence b are in page
+ *                      block_table[b*max_pages_per_seq + i]; entries past the
+ *                      sequence's last key are never read.  An entry outside
+ *                      [0, num_pages) reads zeros (wrong result, no fault).
+ *   seqlens            device [B] int32, 0 <= seqlens[b] <= max_pages_per_seq *
+ *                      page_size (clamped on the device).
+ *   page_size          a positive multiple of 64 (else GQA_ERR_UNSUPPORTED).
+ * Everything else, including the plan and the workspace size, is that of
+ * gqa_attn_decode with S_max = max_pages_per_seq * page_size.
+ */
+GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages,
+                                  const gqa_bf16_t *v_pages, const int32_t *block_table,
+                                  const int32_t *seqlens, int B, int H_q, int H_kv,
+                                  int num_pages, int page_size, int max_pages_per_seq, int d,
+                                  float scale, int num_splits, gqa_bf16_t *o, float *lse,
+                                  void *workspace, size_t ws_bytes, gqa_stream_t stream);
+
+/*
  * Number of kernels gqa_attn_decode launches for these arguments on the current
  * device: 1 (single-kernel cluster path), 2 (split + merge), 0 when B == 0.
  * Host only except for the first call on a device, which performs the

@@ -153,3 +153,31 @@ def test_binding_refuses_cpu_tensors(lib):
     k = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         gqa.gqa_attn_decode(q, k, k, torch.zeros(1, dtype=torch.int32), 0.1)
+
+
+def _raw_paged(lib, **kw):
+    args = dict(q=1 << 20, k=1 << 20, v=1 << 20, table=1 << 20, seqlens=1 << 20, B=2, H_q=64,
+                H_kv=8, num_pages=10, page_size=256, max_pages=4, d=128, scale=0.088,
+                num_splits=0, o=1 << 20, lse=1 << 20, ws=1 << 20, ws_bytes=1 << 30, stream=0)
+    args.update(kw)
+    v = ctypes.c_void_p
+    return lib.gqa_attn_decode_paged(v(args["q"]), v(args["k"]), v(args["v"]), v(args["table"]),
+                                     v(args["seqlens"]), args["B"], args["H_q"], args["H_kv"],
+                                     args["num_pages"], args["page_size"], args["max_pages"],
+                                     args["d"], args["scale"], args["num_splits"], v(args["o"]),
+                                     v(args["lse"]), v(args["ws"]), args["ws_bytes"],
+                                     v(args["stream"]))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(page_size=100), gqa.GQA_ERR_UNSUPPORTED),           # not a multiple of 64
+    (dict(page_size=0), gqa.GQA_ERR_INVALID_ARG),
+    (dict(table=0), gqa.GQA_ERR_INVALID_ARG),                 # no block table
+    (dict(table=(1 << 20) + 4), gqa.GQA_ERR_INVALID_ARG),     # misaligned table
+    (dict(num_pages=0), gqa.GQA_ERR_INVALID_ARG),
+    (dict(max_pages=-1), gqa.GQA_ERR_INVALID_ARG),
+    (dict(d=64), gqa.GQA_ERR_UNSUPPORTED),
+    (dict(B=0), gqa.GQA_OK),
+])
+def test_paged_rejects_before_any_cuda_call(lib, kw, expect):
+    assert _raw_paged(lib, **kw) == expect

@@ -1,0 +1,111 @@
+"""GPU parity of decode over a paged KV cache (block table), through the C ABI.
+
+Pages are a random permutation of a dense cache's 64..1024-key slices in a pool
+that also holds unused pages filled with NaN; the paged call must equal the
+dense call on the same keys bit for bit (same plan) and match the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_synth
+import oracle
+import gqa_attention_decode_gb300 as gqa
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_attention_decode_gb300 import build
+    build.build()
+    gqa.load_library()
+    torch.cuda.set_device(0)
+    yield
+    assert gqa.gqa_attn_device_status() == gqa.GQA_OK
+
+
+def np64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def to_pages(k, v, page_size, extra_pages, seed):
+    """Dense [B, H_kv, S_max, d] -> shuffled pool [num_pages, H_kv, page_size, d] + table."""
+    B, H_kv, S_max, d = k.shape
+    assert S_max % page_size == 0
+    max_pages = S_max // page_size
+    num_pages = B * max_pages + extra_pages
+    perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(seed))
+    kp = torch.full((num_pages, H_kv, page_size, d), float("nan"), dtype=k.dtype, device=k.device)
+    vp = torch.full_like(kp, float("nan"))
+    table = torch.empty((B, max_pages), dtype=torch.int32)
+    for b in range(B):
+        for i in range(max_pages):
+            pid = int(perm[b * max_pages + i])
+            table[b, i] = pid
+            kp[pid] = k[b, :, i * page_size:(i + 1) * page_size]
+            vp[pid] = v[b, :, i * page_size:(i + 1) * page_size]
+    return kp, vp, table.to(k.device)
+
+
+@pytest.mark.parametrize("page_size,seqlens,num_splits", [
+    (64, [1, 700, 1024], 0),
+    (128, [1024, 65, 129], 0),
+    (256, [1000, 1024, 3], 5),
+    (1024, [1024, 1, 513], 0),
+    (256, [256, 512, 1024], 100),      # two-kernel plan
+])
+def test_paged_equals_dense_and_oracle(page_size, seqlens, num_splits):
+    B, H_q, H_kv, S_max, d = 3, 16, 2, 1024, 128
+    q, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S_max, d, seed=41, device=DEV,
+                                          seqlens=seqlens)
+    sl_dev = sl.to(DEV)
+    kp, vp, table = to_pages(k, v, page_size, extra_pages=3, seed=page_size)
+    o_p, l_p = gqa.gqa_attn_decode_paged(q, kp, vp, table, sl_dev, 0.088, num_splits)
+    o_d, l_d = gqa.gqa_attn_decode(q, k, v, sl_dev, 0.088, num_splits)
+    torch.cuda.synchronize()
+    assert torch.equal(o_p, o_d) and torch.equal(l_p, l_d)
+    o_ref, lse_ref = oracle.decode(np64(q), np64(k), np64(v), sl.numpy(), 0.088)
+    compare(o_p, l_p, o_ref, lse_ref, f"paged {page_size}")
+
+
+def test_paged_llama70b_layer():
+    w = gqa_synth.WORKLOADS["llama70b_decode_32k"]
+    q, k, v, sl = gqa_synth.workload_decode_inputs(w, DEV)
+    kp, vp, table = to_pages(k, v, 256, extra_pages=0, seed=7)
+    o_p, l_p = gqa.gqa_attn_decode_paged(q, kp, vp, table, sl.to(DEV), w.scale)
+    o_d, l_d = gqa.gqa_attn_decode(q, k, v, sl.to(DEV), w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o_p, o_d) and torch.equal(l_p, l_d)
+
+
+def test_shared_prefix_pages():
+    """Two sequences whose tables share their first pages (a common prompt prefix)."""
+    H_q, H_kv, ps, d = 16, 2, 128, 128
+    q, k, v, _ = gqa_synth.decode_inputs(2, H_q, H_kv, 512, d, seed=42, device=DEV)
+    kp, vp, table = to_pages(k, v, ps, extra_pages=0, seed=1)
+    table[1, :2] = table[0, :2]                  # sequence 1 reuses sequence 0's prefix
+    sl = torch.tensor([512, 300], dtype=torch.int32)
+    o, l = gqa.gqa_attn_decode_paged(q, kp, vp, table, sl.to(DEV), 0.1)
+    torch.cuda.synchronize()
+    # the dense view each sequence actually sees
+    tcpu = table.cpu()
+    k_seen = torch.stack([torch.cat([kp[int(p)] for p in tcpu[b]], dim=1) for b in range(2)])
+    v_seen = torch.stack([torch.cat([vp[int(p)] for p in tcpu[b]], dim=1) for b in range(2)])
+    o_ref, lse_ref = oracle.decode(np64(q), np64(k_seen), np64(v_seen), sl.numpy(), 0.1)
+    compare(o, l, o_ref, lse_ref, "shared prefix")
+
+
+def test_paged_rejects_bad_page_size():
+    q, k, v, sl = gqa_synth.decode_inputs(1, 8, 1, 256, 128, seed=43, device=DEV)
+    kp = k.view(1, 1, 256, 128).reshape(2, 1, 128, 128)[:, :, :100]
+    kp = kp.contiguous()
+    table = torch.zeros((1, 3), dtype=torch.int32, device=DEV)
+    with pytest.raises(gqa.GQAError) as e:
+        gqa.gqa_attn_decode_paged(q, kp, kp, table, sl.to(DEV), 0.1)
+    assert e.value.status == gqa.GQA_ERR_UNSUPPORTED
