@@ -16,6 +16,7 @@ from .attention import (  # noqa: F401
     attend_rows,
     decode,
     decode_pairs,
+    decode_multi,
     prefill_causal,
     prefill_causal_rows,
     partial_triplet,

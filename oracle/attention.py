@@ -111,6 +111,34 @@ def decode(q, k_cache, v_cache, seqlens, scale):
     return o, lse
 
 
+def decode_multi(q, k_cache, v_cache, seqlens, scale):
+    """Decode of T_q new tokens per sequence (speculative / multi-token decode).
+
+    q [B, H_q, T_q, d]; k_cache, v_cache [B, H_kv, S_max, d]; seqlens[b] counts
+    every cached key of sequence b, the T_q new ones included.  New token t
+    sits at absolute position seqlens[b] - T_q + t and sees keys 0..that
+    position (causal among the new tokens; the record's T_q of section 0.5.2
+    and its G*T_q folded rows of section 5.2).  A token whose position is
+    negative sees nothing: O = 0, lse = -inf.
+    Returns O [B, H_q, T_q, d] and lse [B, H_q, T_q] in float64.
+    """
+    B, H_q, T_q, d = q.shape
+    H_kv = k_cache.shape[1]
+    G = _group_size(H_q, H_kv)
+    seqlens = np.asarray(seqlens, dtype=np.int64).reshape(-1)
+    o = np.zeros((B, H_q, T_q, d))
+    lse = np.zeros((B, H_q, T_q))
+    for b in range(B):
+        n = int(seqlens[b])
+        n_visible = np.clip(n - T_q + np.arange(T_q) + 1, 0, None)
+        for kv in range(H_kv):
+            k = _f64(k_cache[b, kv, :n])
+            v = _f64(v_cache[b, kv, :n])
+            for h in range(kv * G, (kv + 1) * G):
+                o[b, h], lse[b, h] = attend_rows(_f64(q[b, h]), k, v, scale, n_visible)
+    return o, lse
+
+
 def decode_pairs(q, k_cache, v_cache, seqlens, scale, pairs):
     """Decode for a sample of (b, h_q) pairs only; returns O [P, d], lse [P]."""
     B, H_q, d = q.shape

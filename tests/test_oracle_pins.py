@@ -168,6 +168,34 @@ def test_decode_matches_torch_sdpa_gqa():
     np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
 
 
+def test_decode_multi_pins():
+    """T_q new tokens: T_q = 1 is decode; equal lengths make it the causal prefill
+    of the last T_q rows (q_offset = S - T_q); brute force on a tiny case; tokens
+    at negative positions see nothing."""
+    B, H_q, H_kv, S, d, T_q = 2, 4, 2, 9, 8, 3
+    q, k, v = rng_inputs(120, (B, H_q, T_q, d), (B, H_kv, S, d), (B, H_kv, S, d))
+    o1, l1 = oracle.decode_multi(q[:, :, :1], k, v, [S, 5], 0.4)
+    od, ld = oracle.decode(q[:, :, 0], k, v, [S, 5], 0.4)
+    np.testing.assert_allclose(o1[:, :, 0], od, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(l1[:, :, 0], ld, rtol=0, atol=1e-14)
+    om, lm = oracle.decode_multi(q, k, v, [S, S], 0.4)
+    op, lp = oracle.prefill_causal(q, k, v, S - T_q, 0.4)
+    np.testing.assert_allclose(om, op, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lm, lp, rtol=0, atol=1e-13)
+    om, lm = oracle.decode_multi(q, k, v, [6, 2], 0.4)
+    for b, n in enumerate([6, 2]):
+        for h in range(H_q):
+            for t in range(T_q):
+                pos = n - T_q + t
+                if pos < 0:
+                    assert np.all(om[b, h, t] == 0) and np.isneginf(lm[b, h, t])
+                    continue
+                bo, bl = brute_row(q[b, h, t].tolist(), k[b, h // 2, :pos + 1].tolist(),
+                                   v[b, h // 2, :pos + 1].tolist(), 0.4)
+                np.testing.assert_allclose(om[b, h, t], bo, rtol=0, atol=1e-12)
+                assert lm[b, h, t] == pytest.approx(bl, abs=1e-12)
+
+
 def test_uniform_scores_give_mean_of_v():
     B, H_q, H_kv, S, d = 2, 4, 1, 9, 8
     _, k, v = rng_inputs(40, (1,), (B, H_kv, S, d), (B, H_kv, S, d))
