@@ -22,6 +22,8 @@ from ._binding import (  # noqa: F401
     gqa_attn_decode,
     gqa_attn_decode_kernel_count,
     gqa_attn_decode_paged,
+    gqa_attn_decode_multi,
+    gqa_attn_decode_multi_workspace_size,
     gqa_attn_decode_split,
     gqa_attn_decode_merge,
     gqa_attn_decode_noalloc,

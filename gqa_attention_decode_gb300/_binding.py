@@ -37,6 +37,9 @@ _SIGNATURES = {
     "gqa_attn_decode_paged": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _c_float, _c_int, _vp, _vp, _vp,
                                        _c_size, _vp]),
+    "gqa_attn_decode_multi_workspace_size": (_c_size, [_c_int] * 8),
+    "gqa_attn_decode_multi": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                       _c_int, _c_float, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "gqa_attn_decode_kernel_count": (_c_int, [_c_int] * 6 + [_ip]),
     "gqa_attn_decode_split": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                        _c_int, _c_float, _c_int, _vp, _c_size, _vp]),
@@ -218,6 +221,45 @@ def gqa_attn_decode_paged(q, k_pages, v_pages, block_table, seqlens, scale, num_
                                        _ptr(lse), _ptr(workspace), workspace.numel(),
                                        _stream_handle(stream, dev))
     _check(rc, "gqa_attn_decode_paged")
+    return o, lse
+
+
+def gqa_attn_decode_multi_workspace_size(B, H_q, H_kv, T_q, S_max, d, num_sms,
+                                         num_splits=0) -> int:
+    return int(load_library().gqa_attn_decode_multi_workspace_size(B, H_q, H_kv, T_q, S_max, d,
+                                                                   num_sms, num_splits))
+
+
+def gqa_attn_decode_multi(q, k_cache, v_cache, seqlens, scale, num_splits=0, o=None, lse=None,
+                          workspace=None, stream=None):
+    """Multi-token decode.  q [B,H_q,T_q,d] bf16 (token t at position seqlens[b]-T_q+t);
+    k_cache, v_cache [B,H_kv,S_max,d] bf16; seqlens [B] int32.  Returns (o, lse)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    B, H_q, T_q, d = q.shape
+    _, H_kv, S_max, _ = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.shape[0] != B:
+        raise ValueError("k_cache/v_cache must be [B,H_kv,S_max,d]")
+    if o is None:
+        o = torch.empty((B, H_q, T_q, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=dev)
+    _need(o, "o", torch.bfloat16, 4, dev)
+    _need(lse, "lse", torch.float32, 3, dev)
+    if workspace is None:
+        nbytes = gqa_attn_decode_multi_workspace_size(B, H_q, H_kv, T_q, S_max, d, _num_sms(dev),
+                                                      num_splits)
+        workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), B,
+                                       H_q, H_kv, T_q, S_max, d, float(scale), int(num_splits),
+                                       _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                       _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_decode_multi")
     return o, lse
 
 

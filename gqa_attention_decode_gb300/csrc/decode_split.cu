@@ -37,7 +37,10 @@ namespace decode {
 constexpr int kD = 128;
 constexpr int kTileKeys = kDecodeTileKeys;          // 64
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 160
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 160: one column group
+constexpr int kMaxColGroups = 2;                     // multi-token decode: G * T_q <= 32
+constexpr int kThreadsWide = (kConsumerWarps * kMaxColGroups + 1) * 32;  // 288
+constexpr int kMaxCols = 16 * kMaxColGroups;         // 32 (head, token) columns
 constexpr int kHalfBytes = kTileKeys * 128;          // 64 keys x 64 d x 2 B = 8 KiB
 constexpr int kStageBytes = 4 * kHalfBytes;          // K lo/hi + V lo/hi = 32 KiB
 // Ring depth: 3 stages (96 KiB) per CTA, two CTAs per SM for plans that run
@@ -66,6 +69,7 @@ struct Params {
   const int32_t *block_table;  // paged variant: [B, max_pages]
   int page_size, max_pages;
   int B, H_q, H_kv, G, S_max, num_splits, chunk;
+  int T_q, n_cols, cgroups;  // new tokens per sequence, G * T_q, column groups of 4 warps
   float scale_log2;  // scale * log2(e)
   WaitCtl wait;
 };
@@ -92,8 +96,14 @@ __device__ __forceinline__ uint32_t tile_offset(int r, int chunk) {
 // of sequence b (page_size a multiple of the 64-key tile, so no tile straddles
 // two pages).  An out-of-range page id addresses outside the tensor map, which
 // TMA fills with zeros.
-template <int kStages, int kMinBlocks, bool kFused, bool kPaged>
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
+// kNT: 8-column MMA n-tiles per consumer warp.  The query rows of one KV head
+// are (head g, new token t) pairs, column n = g * T_q + t, n < G * T_q; with
+// kNT = 1 one group of four warps covers 8 columns (decode, T_q = 1, G <= 8);
+// with kNT = 2 each group covers 16 and p.cgroups groups of four warps split the
+// columns (multi-token decode, G * T_q <= 32).  New token t sits at position
+// seqlen - T_q + t and sees keys up to it.
+template <int kStages, int kMinBlocks, bool kFused, bool kPaged, int kNT>
+__global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -104,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 
   const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_consumers = kConsumerWarps * p.cgroups;  // warps before the producer
   __shared__ int failed;
   // prologue that reads no input: overlaps the previous kernel when this grid
   // was launched as its programmatic dependent
@@ -111,11 +122,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     failed = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), kConsumerWarps);
+      mbar_init(smem_u32(&empty_bar[s]), n_consumers);
     }
     fence_mbar_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
+  if (warp == n_consumers && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
@@ -127,11 +138,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   if (!kFused && key_begin >= key_end) return;  // empty split: the merge never reads it
   // (a fused CTA with no keys still takes part in the cluster merge)
   const int n_tiles = max(0, (key_end - key_begin + kTileKeys - 1) / kTileKeys);
+  // keys every column may see in this split (token 0 is the most restricted)
+  const int key_all = min(key_end, seqlen - p.T_q + 1);
   __syncthreads();
 
-  float m_run[2], l_run[2], o_acc[8][4];
+  constexpr int kCols = 8 * kNT;  // columns per consumer warp
+  float m_run[kNT][2], l_run[kNT][2], o_acc[8][kNT][4];
 
-  if (warp == kConsumerWarps) {
+  if (warp == n_consumers) {
     // ---------------- producer: lane 0 issues all TMA loads ----------------
     // (paged: the whole warp keeps 32 block-table entries in registers, so the
     // page lookup is a shuffle, never a dependent global load per tile)
@@ -177,29 +191,46 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1, p.wait);
       if (issued < n_tiles) atomicExch(&failed, 1);
     }
-  } else {
-    // ---------------- consumers: warps 0..3 ----------------
+  } else if (warp < n_consumers) {
+    // ---------------- consumers: key slice ks of column group cg ----------------
+    const int ks = warp & 3, cg = warp >> 2;
     const int g = lane >> 2, t = lane & 3;
-    // Q^T as the B operand: b0 = Q[head g][16kk + 2t .. +1], b1 = the same + 8.
-    uint32_t qf[8][2];
-    {
-      const bool head_ok = g < p.G;
+    const int col0 = cg * kCols;  // first column of this warp's group
+    // Q^T as the B operand of n-tile j: b0 = Q[column col0 + 8j + g][16kk + 2t .. +1],
+    // b1 = the same + 8; columns past G * T_q are zero.
+    uint32_t qf[8][kNT][2];
+#pragma unroll
+    for (int j = 0; j < kNT; ++j) {
+      const int n = col0 + 8 * j + g;
+      const bool col_ok = n < p.n_cols;
+      const int gh = col_ok ? n / p.T_q : 0, tq = col_ok ? n % p.T_q : 0;
       const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          p.q + ((size_t)b * p.H_q + (size_t)kv * p.G + (head_ok ? g : 0)) * kD);
+          p.q + (((size_t)b * p.H_q + (size_t)kv * p.G + gh) * p.T_q + tq) * kD);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        qf[kk][0] = head_ok ? __ldg(qrow + kk * 8 + t) : 0u;
-        qf[kk][1] = head_ok ? __ldg(qrow + kk * 8 + 4 + t) : 0u;
+        qf[kk][j][0] = col_ok ? __ldg(qrow + kk * 8 + t) : 0u;
+        qf[kk][j][1] = col_ok ? __ldg(qrow + kk * 8 + 4 + t) : 0u;
       }
     }
+    // keys each of this thread's columns may see (split end and causal limit)
+    int lim[kNT][2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) { m_run[j] = -INFINITY; l_run[j] = 0.f; }
+    for (int j = 0; j < kNT; ++j)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int n = col0 + 8 * j + 2 * t + c;
+        lim[j][c] = min(key_end, seqlen - p.T_q + (n % p.T_q) + 1);
+        m_run[j][c] = -INFINITY;
+        l_run[j][c] = 0.f;
+      }
 #pragma unroll
     for (int md = 0; md < 8; ++md)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o_acc[md][j] = 0.f;
+      for (int j = 0; j < kNT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o_acc[md][j][e] = 0.f;
 
-    const int key_w0 = 16 * warp;  // this warp's keys inside a tile
+    const int key_w0 = 16 * ks;  // this warp's keys inside a tile
     // ldmatrix lane roles (see the fragment layouts of mma.m16n8k16)
     const int k_row = key_w0 + (lane & 15), k_chunk_hi = lane >> 4;
     const int v_row = key_w0 + (lane & 7) + ((lane >> 4) << 3), v_chunk_hi = (lane >> 3) & 1;
@@ -217,140 +248,174 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
       const uint32_t vbase = kbase + 2 * kHalfBytes;
       const int tile_key0 = key_begin + i * kTileKeys;
 
-      // S^T[16 keys x 8 heads] = K[16 x 128] * Q^T[128 x 8]
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      // S^T[16 keys x 8 columns] = K[16 x 128] * Q^T[128 x 8], per n-tile
+      float sc[kNT][4];
+#pragma unroll
+      for (int j = 0; j < kNT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(kbase + tile_offset(k_row, 2 * kk + k_chunk_hi), a0, a1, a2, a3);
-        mma_bf16_16816(sacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-      }
-      // scale into the log2 domain; keys past the end of the split are -inf
-      float sc[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sc[j] = sacc[j] * sl2;
-      const bool tail = tile_key0 + kTileKeys > key_end;
-      if (tail) {
-        const int k_lo = tile_key0 + key_w0 + g, k_hi = k_lo + 8;
-        if (k_lo >= key_end) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
-        if (k_hi >= key_end) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+        for (int j = 0; j < kNT; ++j)
+          mma_bf16_16816(sc[j], a0, a1, a2, a3, qf[kk][j][0], qf[kk][j][1]);
       }
-      // online softmax; thread holds heads 2t (j=0) and 2t+1 (j=1)
-      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+      // scale into the log2 domain; keys a column may not see are -inf
+      const bool tail = tile_key0 + kTileKeys > key_all;
+      const int k_lo = tile_key0 + key_w0 + g, k_hi = k_lo + 8;
+      float pr[kNT][4], corr[kNT][2];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-      const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
-      const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
-      const float p0 = fast_exp2(sc[0] - ref0), p1 = fast_exp2(sc[1] - ref1);
-      const float p2 = fast_exp2(sc[2] - ref0), p3 = fast_exp2(sc[3] - ref1);
-      const float c0 = fast_exp2(m_run[0] - ref0), c1 = fast_exp2(m_run[1] - ref1);
-      l_run[0] = l_run[0] * c0 + p0 + p2;
-      l_run[1] = l_run[1] * c1 + p1 + p3;
-      m_run[0] = mn0;
-      m_run[1] = mn1;
+      for (int j = 0; j < kNT; ++j) {
 #pragma unroll
-      for (int md = 0; md < 8; ++md) {
-        o_acc[md][0] *= c0; o_acc[md][1] *= c1;
-        o_acc[md][2] *= c0; o_acc[md][3] *= c1;
+        for (int e = 0; e < 4; ++e) sc[j][e] *= sl2;
+        if (tail) {
+          if (k_lo >= lim[j][0]) sc[j][0] = -INFINITY;
+          if (k_lo >= lim[j][1]) sc[j][1] = -INFINITY;
+          if (k_hi >= lim[j][0]) sc[j][2] = -INFINITY;
+          if (k_hi >= lim[j][1]) sc[j][3] = -INFINITY;
+        }
+        // online softmax; thread holds columns 2t (c = 0) and 2t+1 (c = 1)
+        float mx0 = fmaxf(sc[j][0], sc[j][2]), mx1 = fmaxf(sc[j][1], sc[j][3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m_run[j][0], mx0), mn1 = fmaxf(m_run[j][1], mx1);
+        const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
+        const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        pr[j][0] = fast_exp2(sc[j][0] - ref0);
+        pr[j][1] = fast_exp2(sc[j][1] - ref1);
+        pr[j][2] = fast_exp2(sc[j][2] - ref0);
+        pr[j][3] = fast_exp2(sc[j][3] - ref1);
+        corr[j][0] = fast_exp2(m_run[j][0] - ref0);
+        corr[j][1] = fast_exp2(m_run[j][1] - ref1);
+        l_run[j][0] = l_run[j][0] * corr[j][0] + pr[j][0] + pr[j][2];
+        l_run[j][1] = l_run[j][1] * corr[j][1] + pr[j][1] + pr[j][3];
+        m_run[j][0] = mn0;
+        m_run[j][1] = mn1;
       }
-      // P^T in the B-operand layout: rows (keys g, g+8) x cols (heads 2t, 2t+1)
-      // transposed to keys (2t, 2t+1) [+8] x head g.
-      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
-      // rows of V past the end are zeroed so stale or NaN cache bytes never
+      uint32_t pb[kNT][2];
+#pragma unroll
+      for (int j = 0; j < kNT; ++j) {
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          o_acc[md][j][0] *= corr[j][0]; o_acc[md][j][1] *= corr[j][1];
+          o_acc[md][j][2] *= corr[j][0]; o_acc[md][j][3] *= corr[j][1];
+        }
+        // P^T in the B-operand layout: rows (keys g, g+8) x cols (2t, 2t+1)
+        // transposed to keys (2t, 2t+1) [+8] x column g.
+        pb[j][0] = movmatrix_trans(pack_bf16x2(pr[j][0], pr[j][1]));
+        pb[j][1] = movmatrix_trans(pack_bf16x2(pr[j][2], pr[j][3]));
+      }
+      // rows of V past the split end are zeroed so stale or NaN cache bytes never
       // meet a zero probability
       bool lo0 = true, lo1 = true, hi0 = true, hi1 = true;
-      if (tail) {
+      if (tile_key0 + kTileKeys > key_end) {
         const int kb = tile_key0 + key_w0 + 2 * t;
         lo0 = kb < key_end; lo1 = kb + 1 < key_end;
         hi0 = kb + 8 < key_end; hi1 = kb + 9 < key_end;
       }
-      // O^T[128 x 8] += V^T[128 x 16 keys] * P^T[16 keys x 8]
+      // O^T[128 x 8] += V^T[128 x 16 keys] * P^T[16 keys x 8], per n-tile
 #pragma unroll
       for (int md = 0; md < 8; ++md) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4_trans(vbase + tile_offset(v_row, 2 * md + v_chunk_hi), a0, a1, a2, a3);
-        if (tail) {
+        if (tile_key0 + kTileKeys > key_end) {
           a0 = mask_pair(a0, lo0, lo1); a1 = mask_pair(a1, lo0, lo1);
           a2 = mask_pair(a2, hi0, hi1); a3 = mask_pair(a3, hi0, hi1);
         }
-        mma_bf16_16816(o_acc[md], a0, a1, a2, a3, pb0, pb1);
+#pragma unroll
+        for (int j = 0; j < kNT; ++j)
+          mma_bf16_16816(o_acc[md][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
     }
-    // per-thread partial sums over the 8 lanes that share heads 2t, 2t+1
+    // per-thread partial sums over the 8 lanes that share columns 2t, 2t+1
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
-      l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
-    }
+    for (int j = 0; j < kNT; ++j)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l_run[j][0] += __shfl_xor_sync(0xffffffffu, l_run[j][0], off);
+        l_run[j][1] += __shfl_xor_sync(0xffffffffu, l_run[j][1], off);
+      }
   }
   __syncthreads();
   if (!kFused && failed) return;
 
-  // ---------------- merge the four warp states, write the split partial ----------------
+  // ---------------- merge the four key slices, write the split partial ----------------
   // All loads have landed and been consumed; the stage ring is free.
-  float *red_m = reinterpret_cast<float *>(smem);              // [4][8]
-  float *red_l = red_m + kConsumerWarps * 8;                   // [4][8]
-  float *red_o = red_l + kConsumerWarps * 8;                   // [4][8][kRedStride]
-  if (warp < kConsumerWarps) {
+  const int n_cols_pad = kCols * p.cgroups;                  // <= kMaxCols
+  float *red_m = reinterpret_cast<float *>(smem);              // [4][n_cols_pad]
+  float *red_l = red_m + kConsumerWarps * kMaxCols;            // [4][n_cols_pad]
+  float *red_o = red_l + kConsumerWarps * kMaxCols;            // [4][n_cols_pad][kRedStride]
+  if (warp < n_consumers) {
+    const int ks = warp & 3, cg = warp >> 2;
     const int g = lane >> 2, t = lane & 3;
-    if (g == 0) {
-      red_m[warp * 8 + 2 * t] = m_run[0];
-      red_m[warp * 8 + 2 * t + 1] = m_run[1];
-      red_l[warp * 8 + 2 * t] = l_run[0];
-      red_l[warp * 8 + 2 * t + 1] = l_run[1];
-    }
-    float *ow = red_o + warp * 8 * kRedStride;
 #pragma unroll
-    for (int md = 0; md < 8; ++md) {
-      ow[(2 * t) * kRedStride + 16 * md + g] = o_acc[md][0];
-      ow[(2 * t + 1) * kRedStride + 16 * md + g] = o_acc[md][1];
-      ow[(2 * t) * kRedStride + 16 * md + g + 8] = o_acc[md][2];
-      ow[(2 * t + 1) * kRedStride + 16 * md + g + 8] = o_acc[md][3];
+    for (int j = 0; j < kNT; ++j) {
+      const int n0 = cg * kCols + 8 * j + 2 * t;
+      if (g == 0) {
+        red_m[ks * kMaxCols + n0] = m_run[j][0];
+        red_m[ks * kMaxCols + n0 + 1] = m_run[j][1];
+        red_l[ks * kMaxCols + n0] = l_run[j][0];
+        red_l[ks * kMaxCols + n0 + 1] = l_run[j][1];
+      }
+      float *ow = red_o + (size_t)ks * kMaxCols * kRedStride;
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        ow[n0 * kRedStride + 16 * md + g] = o_acc[md][j][0];
+        ow[(n0 + 1) * kRedStride + 16 * md + g] = o_acc[md][j][1];
+        ow[n0 * kRedStride + 16 * md + g + 8] = o_acc[md][j][2];
+        ow[(n0 + 1) * kRedStride + 16 * md + g + 8] = o_acc[md][j][3];
+      }
     }
   }
   __syncthreads();
-  float *cta_o = red_o + kConsumerWarps * 8 * kRedStride;  // fused: [8][kD] normalised O_s
-  float *cta_lse = cta_o + 8 * kD;                          // fused: [8] lse_s
-  if (threadIdx.x < kD) {
-    const int dd = threadIdx.x;
-    for (int n = 0; n < p.G; ++n) {
-      float mmax = -INFINITY;
+  float *cta_o = red_o + kConsumerWarps * kMaxCols * kRedStride;  // fused: [8][kD] O_s
+  float *cta_lse = cta_o + 8 * kD;                                // fused: [8] lse_s
+  for (int idx = threadIdx.x; idx < n_cols_pad * kD; idx += blockDim.x) {
+    const int n = idx / kD, dd = idx % kD;
+    if (n >= p.n_cols) continue;
+    float mmax = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) mmax = fmaxf(mmax, red_m[w * 8 + n]);
-      float lsum = 0.f, osum = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) mmax = fmaxf(mmax, red_m[w * kMaxCols + n]);
+    float lsum = 0.f, osum = 0.f;
+    if (mmax != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float f = fast_exp2(red_m[w * 8 + n] - mmax);  // warps without keys: 0
-        lsum += red_l[w * 8 + n] * f;
-        osum += red_o[(w * 8 + n) * kRedStride + dd] * f;
+        const float f = fast_exp2(red_m[w * kMaxCols + n] - mmax);  // slices without keys: 0
+        lsum += red_l[w * kMaxCols + n] * f;
+        osum += red_o[((size_t)w * kMaxCols + n) * kRedStride + dd] * f;
       }
-      if (kFused) {
-        const bool empty = failed || mmax == -INFINITY;
-        cta_o[n * kD + dd] = empty ? 0.f : osum / lsum;
-        if (dd == 0) cta_lse[n] = empty ? -INFINITY : mmax * 0.69314718055994531f + logf(lsum);
-      } else {
-        const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + n) * p.num_splits + split;
-        p.o_part[row * kD + dd] = osum / lsum;
-        if (dd == 0) p.lse_part[row] = mmax * 0.69314718055994531f + logf(lsum);
-      }
+    }
+    // a column that saw no key in this split (or a failed CTA) contributes nothing
+    const bool empty = failed || !(lsum > 0.f);
+    const float o_s = empty ? 0.f : osum / lsum;
+    const float lse_s = empty ? -INFINITY : mmax * 0.69314718055994531f + logf(lsum);
+    if (kFused) {
+      cta_o[n * kD + dd] = o_s;
+      if (dd == 0) cta_lse[n] = lse_s;
+    } else {
+      const int gh = n / p.T_q, tq = n % p.T_q;
+      const size_t row =
+          (((size_t)b * p.H_q + (size_t)kv * p.G + gh) * p.T_q + tq) * p.num_splits + split;
+      p.o_part[row * kD + dd] = o_s;
+      if (dd == 0) p.lse_part[row] = lse_s;
     }
   }
   if (kFused) {
-    // log-sum-exp merge across the cluster: CTA r finalises heads r, r + splits, ...
+    // log-sum-exp merge across the cluster: CTA r finalises columns r, r + splits, ...
     cluster_sync();
     const int cs = p.num_splits;
     const uint32_t rank = cluster_ctarank();
     if (threadIdx.x < kD) {
       const int dd = threadIdx.x;
       constexpr float kLog2e = 1.4426950408889634f;
-      for (int n = (int)rank; n < p.G; n += cs) {
+      for (int n = (int)rank; n < p.n_cols; n += cs) {
         const uint32_t lse_at = smem_u32(cta_lse + n), o_at = smem_u32(cta_o + n * kD + dd);
         float mx = -INFINITY;
         for (int c = 0; c < cs; ++c) mx = fmaxf(mx, ld_dsmem_f32(dsmem_addr(lse_at, c)));
@@ -362,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
             acc = fmaf(w, ld_dsmem_f32(dsmem_addr(o_at, c)), acc);
           }
         }
-        const size_t row = (size_t)b * p.H_q + (size_t)kv * p.G + n;
+        const int gh = n / p.T_q, tq = n % p.T_q;
+        const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + gh) * p.T_q + tq;
         const __nv_bfloat16 r = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
         p.o[row * kD + dd] = *reinterpret_cast<const uint16_t *>(&r);
         if (dd == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
@@ -385,18 +451,18 @@ constexpr int kMergeGroups = kMergeThreads / 32;
 __global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
                         const int32_t *__restrict__ seqlens, uint16_t *__restrict__ o,
-                        float *__restrict__ lse, int H_q, int S_max, int num_splits, int chunk) {
+                        float *__restrict__ lse, int S_max, int num_splits, int chunk) {
   __shared__ float4 red_o[kMergeGroups][32];
   __shared__ float red_w[kMergeGroups];
   __shared__ float red_m[kMergeGroups];
   // the next kernel (typically the next layer's split) may start its prologue
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int h = blockIdx.x, b = blockIdx.y;  // h: (query head, new token) row of sequence b
   const int t = threadIdx.x, grp = t >> 5, lane = t & 31;
   const int seqlen = min(max(seqlens[b], 0), S_max);
   const int ns = min((seqlen + chunk - 1) / chunk, num_splits);
-  const size_t row = (size_t)b * H_q + h;
+  const size_t row = (size_t)b * gridDim.x + h;
   if (ns == 0) {  // no visible key
     if (grp == 0) reinterpret_cast<uint2 *>(o + row * kD)[lane] = make_uint2(0u, 0u);
     if (t == 0) lse[row] = -INFINITY;
@@ -412,6 +478,11 @@ __global__ void __launch_bounds__(kMergeThreads)
   mx = red_m[0];
 #pragma unroll
   for (int g = 1; g < kMergeGroups; ++g) mx = fmaxf(mx, red_m[g]);
+  if (mx == -INFINITY) {  // every split empty for this row (a token before the cache start)
+    if (grp == 0) reinterpret_cast<uint2 *>(o + row * kD)[lane] = make_uint2(0u, 0u);
+    if (t == 0) lse[row] = -INFINITY;
+    return;
+  }
 
   constexpr float kLog2e = 1.4426950408889634f;
   const float4 *op = reinterpret_cast<const float4 *>(o_part + row * num_splits * kD) + lane;
@@ -465,32 +536,32 @@ static CUresult make_kv_map(CUtensorMap *map, const uint16_t *base, long long bl
 
 }  // namespace decode
 
-template <int kStages, int kMinBlocks, bool kFused>
+template <int kStages, int kMinBlocks, bool kFused, int kNT>
 static cudaError_t set_smem_attr() {
   using namespace decode;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused, false>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused, false, kNT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem_bytes<kStages>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused, true>,
+  return cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused, true, kNT>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<kStages>());
 }
 
 cudaError_t decode_prepare_device(int *fused_clusters) {
   using namespace decode;
   cudaError_t e;
-  if ((e = set_smem_attr<3, 2, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<kOneWaveStages, 1, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<kOneWaveStages, 1, true>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<3, 2, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<3, 2, false, 1>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<kOneWaveStages, 1, false, 1>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<3, 2, true, 1>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<kOneWaveStages, 1, false, 2>()) != cudaSuccess) return e;
   // For each cluster size (splits per sequence and KV head) the number of
   // clusters of the fused kernel the device runs at once (the 3-stage variant,
   // which may pair two CTAs on an SM); 0 where it cannot.  Sizes above 8 need the
   // non-portable cluster size opt-in.
-  const bool big = cudaFuncSetAttribute(decode_split_kernel<3, 2, true, false>,
+  const bool big = cudaFuncSetAttribute(decode_split_kernel<3, 2, true, false, 1>,
                                         cudaFuncAttributeNonPortableClusterSizeAllowed,
                                         1) == cudaSuccess &&
-                   cudaFuncSetAttribute(decode_split_kernel<3, 2, true, true>,
+                   cudaFuncSetAttribute(decode_split_kernel<3, 2, true, true, 1>,
                                         cudaFuncAttributeNonPortableClusterSizeAllowed,
                                         1) == cudaSuccess;
   for (int cs = 1; cs <= kMaxFusedSplits; ++cs) {
@@ -508,7 +579,7 @@ cudaError_t decode_prepare_device(int *fused_clusters) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_split_kernel<3, 2, true, false>, &cfg) ==
+    if (cudaOccupancyMaxActiveClusters(&n, decode_split_kernel<3, 2, true, false, 1>, &cfg) ==
         cudaSuccess)
       fused_clusters[cs] = n;
   }
@@ -526,17 +597,18 @@ static bool make_maps(const DecodeLaunch &a, PFN_cuTensorMapEncodeTiled_v12000 e
          make_kv_map(tm_v, a.v_cache, blocks, rows, encode) == CUDA_SUCCESS;
 }
 
-// Launches decode_split_kernel<kStages, kMinBlocks, kFused, paged> for a's layout.
-template <int kStages, int kMinBlocks, bool kFused>
+// Launches decode_split_kernel<kStages, kMinBlocks, kFused, paged, kNT> for a's layout.
+template <int kStages, int kMinBlocks, bool kFused, int kNT>
 static cudaError_t launch_variant(cudaLaunchConfig_t *cfg, const CUtensorMap &tm_k,
                                   const CUtensorMap &tm_v, const decode::Params &p, bool paged) {
   using namespace decode;
   cfg->dynamicSmemBytes = smem_bytes<kStages>();
+  cfg->blockDim = dim3(32 * (kConsumerWarps * p.cgroups + 1));
   if (paged)
-    return cudaLaunchKernelEx(cfg, decode_split_kernel<kStages, kMinBlocks, kFused, true>, tm_k,
-                              tm_v, p);
-  return cudaLaunchKernelEx(cfg, decode_split_kernel<kStages, kMinBlocks, kFused, false>, tm_k,
-                            tm_v, p);
+    return cudaLaunchKernelEx(cfg, decode_split_kernel<kStages, kMinBlocks, kFused, true, kNT>,
+                              tm_k, tm_v, p);
+  return cudaLaunchKernelEx(cfg, decode_split_kernel<kStages, kMinBlocks, kFused, false, kNT>,
+                            tm_k, tm_v, p);
 }
 
 static decode::Params make_params(const DecodeLaunch &a) {
@@ -555,6 +627,9 @@ static decode::Params make_params(const DecodeLaunch &a) {
   p.num_splits = a.num_splits;
   p.chunk = a.chunk;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.T_q = a.T_q > 0 ? a.T_q : 1;
+  p.n_cols = p.G * p.T_q;
+  p.cgroups = p.n_cols <= 8 ? 1 : (p.n_cols + 15) / 16;
   p.block_table = a.block_table;
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
@@ -565,6 +640,7 @@ static decode::Params make_params(const DecodeLaunch &a) {
 bool decode_fused_eligible(const DecodeLaunch &a) {
   // one launch only when every (sequence, KV head) cluster runs in a single wave
   if (a.S_max <= 0 || a.num_splits < 1 || a.num_splits > decode::kMaxFusedSplits) return false;
+  if ((long long)(a.H_q / a.H_kv) * (a.T_q > 0 ? a.T_q : 1) > 8) return false;  // one n-tile only
   return (long long)a.B * a.H_kv <= a.fused_clusters[a.num_splits];
 }
 
@@ -588,7 +664,7 @@ cudaError_t decode_fused_launch(const DecodeLaunch &a, cudaStream_t stream,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return launch_variant<3, 2, true>(&cfg, tm_k, tm_v, p, a.block_table != nullptr);
+  return launch_variant<3, 2, true, 1>(&cfg, tm_k, tm_v, p, a.block_table != nullptr);
 }
 
 cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
@@ -609,15 +685,17 @@ cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   cfg.numAttrs = 1;
   const long long ctas = (long long)a.num_splits * a.H_kv * a.B;
   const bool paged = a.block_table != nullptr;
+  if (p.n_cols > 8)  // multi-token decode: two n-tiles per warp, one CTA per SM
+    return launch_variant<kOneWaveStages, 1, false, 2>(&cfg, tm_k, tm_v, p, paged);
   if (ctas <= a.num_sms)  // one wave, one CTA per SM
-    return launch_variant<kOneWaveStages, 1, false>(&cfg, tm_k, tm_v, p, paged);
-  return launch_variant<3, 2, false>(&cfg, tm_k, tm_v, p, paged);
+    return launch_variant<kOneWaveStages, 1, false, 1>(&cfg, tm_k, tm_v, p, paged);
+  return launch_variant<3, 2, false, 1>(&cfg, tm_k, tm_v, p, paged);
 }
 
 cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream) {
   using namespace decode;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.H_q, a.B);
+  cfg.gridDim = dim3(a.H_q * (a.T_q > 0 ? a.T_q : 1), a.B);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -627,7 +705,7 @@ cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_merge_kernel, (const float *)a.o_part,
-                            (const float *)a.lse_part, a.seqlens, a.o, a.lse, a.H_q, a.S_max,
+                            (const float *)a.lse_part, a.seqlens, a.o, a.lse, a.S_max,
                             a.num_splits, a.chunk > 0 ? a.chunk : 1);
 }
 

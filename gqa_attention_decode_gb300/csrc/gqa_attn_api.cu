@@ -111,8 +111,8 @@ int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_split
   return GQA_OK;
 }
 
-size_t decode_ws_bytes(int B, int H_q, int splits, int d) {
-  return round256((size_t)B * H_q * splits * (size_t)(d + 1) * sizeof(float));
+size_t decode_ws_bytes(int B, int H_q, int splits, int d, int T_q = 1) {
+  return round256((size_t)B * H_q * T_q * splits * (size_t)(d + 1) * sizeof(float));
 }
 
 enum DecodePhase { kPhaseSplit = 1, kPhaseMerge = 2, kPhaseBoth = 3 };
@@ -125,8 +125,8 @@ bool finite_scale(float scale) {
 // be null.
 int check_decode_args(int phase, const void *q, const void *k, const void *v,
                       const void *seqlens, int B, int H_q, int H_kv, int S_max, int d,
-                      float scale, int num_splits, const void *o, const void *lse) {
-  if (B < 0 || H_q <= 0 || H_kv <= 0 || S_max < 0 || d <= 0 || num_splits < 0)
+                      float scale, int num_splits, const void *o, const void *lse, int T_q = 1) {
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || S_max < 0 || d <= 0 || num_splits < 0 || T_q <= 0)
     return GQA_ERR_INVALID_ARG;
   if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
   if (!finite_scale(scale)) return GQA_ERR_INVALID_ARG;
@@ -141,7 +141,9 @@ int check_decode_args(int phase, const void *q, const void *k, const void *v,
   }
   if (d != 128) return GQA_ERR_UNSUPPORTED;
   if (H_q / H_kv > gqa::kDecodeMaxG) return GQA_ERR_UNSUPPORTED;
+  if ((long long)(H_q / H_kv) * T_q > gqa::kDecodeMaxCols) return GQA_ERR_UNSUPPORTED;
   if (B > 65535 || H_kv > 65535) return GQA_ERR_UNSUPPORTED;  // grid y/z limits
+  if ((long long)H_q * T_q > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
   return GQA_OK;
 }
 
@@ -224,19 +226,20 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                  const gqa_bf16_t *v_cache, const int32_t *seqlens, int B, int H_q, int H_kv,
                  int S_max, int d, float scale, int num_splits, gqa_bf16_t *o, float *lse,
                  const void *workspace, size_t ws_bytes, gqa_stream_t stream,
-                 const PagedLayout &paged = PagedLayout{nullptr, 0, 0, 0}) {
+                 const PagedLayout &paged = PagedLayout{nullptr, 0, 0, 0}, int T_q = 1) {
   int rc = check_decode_args(phase, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
-                             num_splits, o, lse);
+                             num_splits, o, lse, T_q);
   if (rc != GQA_OK || B == 0) return rc;
   DeviceState *st = nullptr;
   if ((rc = device_state(&st)) != GQA_OK) return rc;
   int splits = 0, chunk = 0;
   if ((rc = plan(B, H_kv, S_max, st->num_sms, num_splits, &splits, &chunk)) != GQA_OK) return rc;
-  const size_t need = decode_ws_bytes(B, H_q, splits, d);
+  const size_t need = decode_ws_bytes(B, H_q, splits, d, T_q);
   if (!workspace || ws_bytes < need) return GQA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return GQA_ERR_INVALID_ARG;
 
   gqa::DecodeLaunch a = {};
+  a.T_q = T_q;
   a.q = q;
   a.block_table = paged.block_table;
   a.num_pages = paged.num_pages;
@@ -255,7 +258,7 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   a.o = o;
   a.lse = lse;
   a.o_part = static_cast<float *>(const_cast<void *>(workspace));
-  a.lse_part = a.o_part + (size_t)B * H_q * splits * d;
+  a.lse_part = a.o_part + (size_t)B * H_q * T_q * splits * d;
   a.num_sms = st->num_sms;
   a.fused_clusters = st->fused_clusters;
   a.wait.status = st->status;
@@ -300,6 +303,25 @@ GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages
   const PagedLayout paged{block_table, num_pages, page_size, max_pages_per_seq};
   return decode_phase(kPhaseBoth, q, k_pages, v_pages, seqlens, B, H_q, H_kv, (int)s_max, d,
                       scale, num_splits, o, lse, workspace, ws_bytes, stream, paged);
+}
+
+GQA_API size_t gqa_attn_decode_multi_workspace_size(int B, int H_q, int H_kv, int T_q, int S_max,
+                                                    int d, int num_sms, int num_splits) {
+  int splits = 0, chunk = 0;
+  if (H_q <= 0 || d <= 0 || T_q <= 0 ||
+      plan(B, H_kv, S_max, num_sms, num_splits, &splits, &chunk) != GQA_OK)
+    return 0;
+  return decode_ws_bytes(B, H_q, splits, d, T_q);
+}
+
+GQA_API int gqa_attn_decode_multi(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
+                                  const gqa_bf16_t *v_cache, const int32_t *seqlens, int B,
+                                  int H_q, int H_kv, int T_q, int S_max, int d, float scale,
+                                  int num_splits, gqa_bf16_t *o, float *lse, void *workspace,
+                                  size_t ws_bytes, gqa_stream_t stream) {
+  return decode_phase(kPhaseBoth, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
+                      num_splits, o, lse, workspace, ws_bytes, stream,
+                      PagedLayout{nullptr, 0, 0, 0}, T_q);
 }
 
 GQA_API int gqa_attn_decode_kernel_count(int B, int H_q, int H_kv, int S_max, int d,

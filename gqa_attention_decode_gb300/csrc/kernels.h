@@ -19,11 +19,12 @@ struct DecodeLaunch {
   int num_pages, page_size, max_pages;  // paged layout (S_max = max_pages * page_size)
   const int32_t *seqlens;   // [B]
   int B, H_q, H_kv, S_max, num_splits, chunk;
+  int T_q;          // new tokens per sequence (1: plain decode); G * T_q <= kDecodeMaxCols
   float scale;
-  uint16_t *o;      // [B, H_q, d]
-  float *lse;       // [B, H_q]
-  float *o_part;    // [B, H_q, num_splits, d]
-  float *lse_part;  // [B, H_q, num_splits]
+  uint16_t *o;      // [B, H_q, T_q, d]
+  float *lse;       // [B, H_q, T_q]
+  float *o_part;    // [B, H_q, T_q, num_splits, d]
+  float *lse_part;  // [B, H_q, T_q, num_splits]
   int num_sms;
   const int *fused_clusters;  // [kDecodeMaxFusedSplits + 1]: co-resident clusters per size
   WaitCtl wait;
@@ -32,6 +33,7 @@ struct DecodeLaunch {
 constexpr int kDecodeTileKeys = 64;  // keys per pipeline stage
 constexpr int kDecodeMaxG = 8;       // query heads per KV head that fit the MMA N dimension
 constexpr int kDecodeMaxFusedSplits = 16;  // largest cluster of the single-kernel decode
+constexpr int kDecodeMaxCols = 32;         // (head, new token) rows per KV head: G * T_q
 
 // One-time per-device kernel attributes (dynamic shared memory, cluster size
 // opt-in); fills fused_clusters[1..kDecodeMaxFusedSplits] with the number of

@@ -184,6 +184,31 @@ GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages
                                   void *workspace, size_t ws_bytes, gqa_stream_t stream);
 
 /*
+ * Multi-token decode: T_q new tokens per sequence (speculative decoding
+ * verification, the record's T_q of section 0.5.2 with the G*T_q rows of one KV
+ * head folded into one product, section 5.2).
+ *
+ *   q        device [B, H_q, T_q, d] bf16; token t of sequence b sits at
+ *            absolute position seqlens[b] - T_q + t.
+ *   k_cache, v_cache, seqlens   as gqa_attn_decode; seqlens[b] counts every
+ *            cached key, the T_q new tokens' keys included.
+ *   Token t sees keys 0..seqlens[b]-T_q+t (causal among the new tokens); a
+ *   token whose position is negative sees nothing (O = 0, lse = -inf).
+ *   o        device [B, H_q, T_q, d] bf16; lse device [B, H_q, T_q] fp32.
+ *   Supported: d = 128, G * T_q <= 32 (T_q <= 4 for G = 8), else
+ *   GQA_ERR_UNSUPPORTED.  K and V are read once per KV head for all G*T_q rows.
+ *   workspace: gqa_attn_decode_multi_workspace_size(...) bytes
+ *   (B*H_q*T_q*splits*(d+1)*4, rounded up to 256).  T_q = 1 is gqa_attn_decode.
+ */
+GQA_API size_t gqa_attn_decode_multi_workspace_size(int B, int H_q, int H_kv, int T_q, int S_max,
+                                                    int d, int num_sms, int num_splits);
+GQA_API int gqa_attn_decode_multi(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
+                                  const gqa_bf16_t *v_cache, const int32_t *seqlens, int B,
+                                  int H_q, int H_kv, int T_q, int S_max, int d, float scale,
+                                  int num_splits, gqa_bf16_t *o, float *lse, void *workspace,
+                                  size_t ws_bytes, gqa_stream_t stream);
+
+/*
  * Number of kernels gqa_attn_decode launches for these arguments on the current
  * device: 1 (single-kernel cluster path), 2 (split + merge), 0 when B == 0.
  * Host only except for the first call on a device, which performs the

@@ -181,3 +181,17 @@ def _raw_paged(lib, **kw):
 ])
 def test_paged_rejects_before_any_cuda_call(lib, kw, expect):
     assert _raw_paged(lib, **kw) == expect
+
+
+def test_multi_token_rejections(lib):
+    v = ctypes.c_void_p
+    p = 1 << 20
+    call = lambda B, H_q, H_kv, T_q, d=128: lib.gqa_attn_decode_multi(
+        v(p), v(p), v(p), v(p), B, H_q, H_kv, T_q, 1024, d, 0.088, 0, v(p), v(p), v(p), 1 << 30,
+        v(0))
+    assert call(1, 64, 8, 5) == gqa.GQA_ERR_UNSUPPORTED      # G * T_q = 40 > 32
+    assert call(1, 64, 8, 0) == gqa.GQA_ERR_INVALID_ARG
+    assert call(1, 64, 8, 2, d=64) == gqa.GQA_ERR_UNSUPPORTED
+    assert call(0, 64, 8, 2) == gqa.GQA_OK
+    assert gqa.gqa_attn_decode_multi_workspace_size(1, 64, 8, 4, 32768, 128, 152) == \
+        4 * gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 152)

@@ -1,0 +1,86 @@
+"""GPU parity of multi-token decode (T_q new tokens per sequence) against the oracle.
+
+Token t of sequence b sits at position seqlens[b] - T_q + t and sees keys up to
+it; the G * T_q (head, token) rows of one KV head share one pass over K and V.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_synth
+import oracle
+import gqa_attention_decode_gb300 as gqa
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_attention_decode_gb300 import build
+    build.build()
+    gqa.load_library()
+    torch.cuda.set_device(0)
+    yield
+    assert gqa.gqa_attn_device_status() == gqa.GQA_OK
+
+
+def np64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def inputs(B, H_q, H_kv, T_q, S_max, seqlens, seed):
+    q = gqa_synth.bf16_normal((B, H_q, T_q, 128), seed, DEV)
+    _, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S_max, 128, seed + 1, DEV, seqlens)
+    return q, k, v, sl
+
+
+@pytest.mark.parametrize("H_q,H_kv,T_q", [(64, 8, 2), (64, 8, 3), (64, 8, 4), (16, 4, 3),
+                                          (16, 4, 8), (8, 8, 5), (12, 3, 2)])
+@pytest.mark.parametrize("num_splits", [0, 7])
+def test_multi_token_decode(H_q, H_kv, T_q, num_splits):
+    seqlens = [2000, 1, 700, 3]              # sequences shorter than T_q included
+    q, k, v, sl = inputs(4, H_q, H_kv, T_q, 2000, seqlens, 51)
+    o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 1 / math.sqrt(128), num_splits)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(),
+                                         1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, f"T_q={T_q} G={H_q // H_kv} splits={num_splits}")
+
+
+def test_single_token_equals_decode():
+    q, k, v, sl = inputs(2, 64, 8, 1, 1500, [1500, 333], 52)
+    o1, l1 = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 0.088)
+    o2, l2 = gqa.gqa_attn_decode(q[:, :, 0].contiguous(), k, v, sl.to(DEV), 0.088)
+    torch.cuda.synchronize()
+    assert torch.equal(o1[:, :, 0], o2) and torch.equal(l1[:, :, 0], l2)
+
+
+def test_llama70b_layer_four_tokens():
+    w = gqa_synth.WORKLOADS["llama70b_decode_32k"]
+    q, k, v, sl = inputs(1, 64, 8, 4, w.S_max, None, 53)
+    o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), w.scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), w.scale)
+    compare(o, lse, o_ref, lse_ref, "llama70b T_q=4")
+
+
+def test_nan_padding_multi():
+    q, k, v, sl = inputs(2, 32, 8, 4, 640, [577, 100], 54)
+    o_ref, l_ref = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 0.1)
+    gqa_synth.fill_padding(k, sl, float("nan"))
+    gqa_synth.fill_padding(v, sl, float("nan"))
+    o, l = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
+def test_too_many_rows_is_unsupported():
+    q, k, v, sl = inputs(1, 64, 8, 5, 256, None, 55)          # G * T_q = 40 > 32
+    with pytest.raises(gqa.GQAError) as e:
+        gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 0.1)
+    assert e.value.status == gqa.GQA_ERR_UNSUPPORTED
