@@ -375,36 +375,61 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     }
   }
   __syncthreads();
-  float *cta_o = red_o + kConsumerWarps * kMaxCols * kRedStride;  // fused: [8][kD] O_s
+  // pass 1, one thread per column: reference max, and the weight of each key
+  // slice with the 1/l normalisation folded in (0 for slices without keys)
+  float *wts = red_o + kConsumerWarps * kMaxCols * kRedStride;  // [4][kMaxCols]
+  float *col_lse = wts + kConsumerWarps * kMaxCols;            // [kMaxCols]
+  int *col_row = reinterpret_cast<int *>(col_lse + kMaxCols);  // [kMaxCols], -1: padding
+  float *cta_o = reinterpret_cast<float *>(col_row + kMaxCols);  // fused: [8][kD] O_s
   float *cta_lse = cta_o + 8 * kD;                                // fused: [8] lse_s
-  for (int idx = threadIdx.x; idx < n_cols_pad * kD; idx += blockDim.x) {
-    const int n = idx / kD, dd = idx % kD;
-    if (n >= p.n_cols) continue;
+  if (threadIdx.x < n_cols_pad) {
+    const int n = threadIdx.x;
     float mmax = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) mmax = fmaxf(mmax, red_m[w * kMaxCols + n]);
-    float lsum = 0.f, osum = 0.f;
-    if (mmax != -INFINITY) {
+    float f[kConsumerWarps], lsum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float f = fast_exp2(red_m[w * kMaxCols + n] - mmax);  // slices without keys: 0
-        lsum += red_l[w * kMaxCols + n] * f;
-        osum += red_o[((size_t)w * kMaxCols + n) * kRedStride + dd] * f;
-      }
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      f[w] = mmax == -INFINITY ? 0.f : fast_exp2(red_m[w * kMaxCols + n] - mmax);
+      lsum += red_l[w * kMaxCols + n] * f[w];
     }
     // a column that saw no key in this split (or a failed CTA) contributes nothing
-    const bool empty = failed || !(lsum > 0.f);
-    const float o_s = empty ? 0.f : osum / lsum;
+    const bool empty = failed || !(lsum > 0.f) || n >= p.n_cols;
+    const float inv = empty ? 0.f : 1.f / lsum;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) wts[w * kMaxCols + n] = f[w] * inv;
     const float lse_s = empty ? -INFINITY : mmax * 0.69314718055994531f + logf(lsum);
+    int row = -1;
+    if (n < p.n_cols)
+      row = (int)(((size_t)b * p.H_q + (size_t)kv * p.G + n / p.T_q) * p.T_q + n % p.T_q);
+    col_row[n] = row;
     if (kFused) {
-      cta_o[n * kD + dd] = o_s;
-      if (dd == 0) cta_lse[n] = lse_s;
+      cta_lse[n] = lse_s;
+    } else if (row >= 0) {
+      p.lse_part[(size_t)row * p.num_splits + split] = lse_s;
+    }
+  }
+  __syncthreads();
+  // pass 2: O_s = sum over key slices of weight * O_slice, four columns per item
+  for (int item = threadIdx.x; item < n_cols_pad * (kD / 4); item += blockDim.x) {
+    const int n = item / (kD / 4), d4 = item % (kD / 4);
+    const int row = col_row[n];
+    if (row < 0) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float wt = wts[w * kMaxCols + n];
+      const float4 x =
+          reinterpret_cast<const float4 *>(red_o + ((size_t)w * kMaxCols + n) * kRedStride)[d4];
+      acc.x = fmaf(wt, x.x, acc.x);
+      acc.y = fmaf(wt, x.y, acc.y);
+      acc.z = fmaf(wt, x.z, acc.z);
+      acc.w = fmaf(wt, x.w, acc.w);
+    }
+    if (kFused) {
+      reinterpret_cast<float4 *>(cta_o + n * kD)[d4] = acc;
     } else {
-      const int gh = n / p.T_q, tq = n % p.T_q;
-      const size_t row =
-          (((size_t)b * p.H_q + (size_t)kv * p.G + gh) * p.T_q + tq) * p.num_splits + split;
-      p.o_part[row * kD + dd] = o_s;
-      if (dd == 0) p.lse_part[row] = lse_s;
+      reinterpret_cast<float4 *>(p.o_part + ((size_t)row * p.num_splits + split) * kD)[d4] = acc;
     }
   }
   if (kFused) {
