@@ -3,10 +3,11 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step = split-KV decode of a Llama3-70B layer over a 32K-token cache
-(B=1, H_q=64, H_kv=8, d=128) for 8 layers, each layer with its own 128 MiB K/V
-cache (so no call finds its K/V in the 126 MB L2), followed by one causal
-prefill of an 8K prompt (same layer shape).  The headline `value` is the
+One step = split-KV decode of one token through the attention of all 80
+Llama3-70B layers over a 32K-token cache (B=1, H_q=64, H_kv=8, d=128), each
+layer with its own 128 MiB K/V cache (10 GiB in all, so no call finds its K/V
+in the 126 MB L2), followed by one causal prefill of an 8K prompt (same layer
+shape).  The headline `value` is the
 decode's HBM throughput in GB/s per gqa_attn_decode call (algorithmic bytes:
 every valid K and V row read once, 2*B*H_kv*S*d*2 bytes); the prefill's
 TFLOP/s (4*H_q*d*sum_i(visible keys of row i)) is reported in the `prefill`
@@ -39,7 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "GQA decode HBM GB/s (% of peak); causal prefill TFLOP/s (% of BF16 peak)"
 DECODE_WORKLOAD = "llama70b_decode_32k"
 PREFILL_WORKLOAD = "causal_prefill_8k"
-LAYERS = 8          # decode calls per step, each on its own 128 MiB K/V copy
+LAYERS = 80         # decode calls per step: one per Llama3-70B layer, each its own K/V cache
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 KERNEL_SOURCES = {
@@ -307,8 +308,8 @@ def run_ours(args, rank, world, device):
     wd = gqa_synth.WORKLOADS[DECODE_WORKLOAD]
     q, k, v, seqlens_cpu = gqa_synth.workload_decode_inputs(wd, device)
     seqlens = seqlens_cpu.to(device)
-    # LAYERS copies of the cache (one per decoded layer), so consecutive calls
-    # never find their K/V in L2
+    # one K/V cache per decoded layer, so consecutive calls never find their K/V
+    # in L2
     layers = max(1, args.layers)
     kv_copies = [(k, v)] + [(k.clone(), v.clone()) for _ in range(layers - 1)]
     splits, chunk = gqa.gqa_attn_decode_plan(wd.B, wd.H_kv, wd.S_max, sms, wd.num_splits)

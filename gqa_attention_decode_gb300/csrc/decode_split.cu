@@ -465,11 +465,12 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// One CTA per (query head, sequence), 256 threads: thread (g, lane) owns columns
-// 4*lane .. 4*lane+3 and splits g, g+8, g+16, ...; the eight groups are summed
-// in shared memory.  lse = max_s lse_s + ln sum_s exp(lse_s - max);
-// O = sum_s exp(lse_s - lse) O_s.  Launched as a programmatic dependent of the
-// split kernel: everything before griddepcontrol.wait overlaps its tail.
+// One CTA per (query head, new token) row of a sequence, 256 threads: thread
+// (g, lane) owns columns 4*lane .. 4*lane+3 and merges splits g, g+8, g+16, ...
+// on the fly (online log-sum-exp, the lse and O loads of all its splits in
+// flight together); the eight group states are then combined once in shared
+// memory.  lse = m + ln sum_s exp(lse_s - m); O = sum_s exp(lse_s - lse) O_s.
+// Launched as a programmatic dependent of the split kernel.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeGroups = kMergeThreads / 32;
 
@@ -488,59 +489,58 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int seqlen = min(max(seqlens[b], 0), S_max);
   const int ns = min((seqlen + chunk - 1) / chunk, num_splits);
   const size_t row = (size_t)b * gridDim.x + h;
-  if (ns == 0) {  // no visible key
-    if (grp == 0) reinterpret_cast<uint2 *>(o + row * kD)[lane] = make_uint2(0u, 0u);
-    if (t == 0) lse[row] = -INFINITY;
-    return;
-  }
   const float *lp = lse_part + row * num_splits;
-  float mx = -INFINITY;
-  for (int s = t; s < ns; s += kMergeThreads) mx = fmaxf(mx, lp[s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if (lane == 0) red_m[grp] = mx;
-  __syncthreads();
-  mx = red_m[0];
-#pragma unroll
-  for (int g = 1; g < kMergeGroups; ++g) mx = fmaxf(mx, red_m[g]);
-  if (mx == -INFINITY) {  // every split empty for this row (a token before the cache start)
-    if (grp == 0) reinterpret_cast<uint2 *>(o + row * kD)[lane] = make_uint2(0u, 0u);
-    if (t == 0) lse[row] = -INFINITY;
-    return;
-  }
-
-  constexpr float kLog2e = 1.4426950408889634f;
   const float4 *op = reinterpret_cast<const float4 *>(o_part + row * num_splits * kD) + lane;
+  constexpr float kLog2e = 1.4426950408889634f;
+  float m = -INFINITY, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
 #pragma unroll 4
   for (int s = grp; s < ns; s += kMergeGroups) {
-    const float w = fast_exp2((lp[s] - mx) * kLog2e);
+    const float ls = lp[s];
     const float4 x = op[(size_t)s * (kD / 4)];
-    wsum += w;
-    acc.x = fmaf(w, x.x, acc.x);
-    acc.y = fmaf(w, x.y, acc.y);
-    acc.z = fmaf(w, x.z, acc.z);
-    acc.w = fmaf(w, x.w, acc.w);
+    if (ls == -INFINITY) continue;  // a split that saw no key of this row
+    const float m_new = fmaxf(m, ls);
+    const float c = fast_exp2((m - m_new) * kLog2e);  // 0 while m is -inf
+    const float w = fast_exp2((ls - m_new) * kLog2e);
+    wsum = wsum * c + w;
+    acc.x = fmaf(w, x.x, acc.x * c);
+    acc.y = fmaf(w, x.y, acc.y * c);
+    acc.z = fmaf(w, x.z, acc.z * c);
+    acc.w = fmaf(w, x.w, acc.w * c);
+    m = m_new;
   }
   red_o[grp][lane] = acc;
-  if (lane == 0) red_w[grp] = wsum;
+  if (lane == 0) {
+    red_w[grp] = wsum;
+    red_m[grp] = m;
+  }
   __syncthreads();
   if (grp == 0) {
-    float4 sum = red_o[0][lane];
-    float W = red_w[0];
+    float mx = -INFINITY;
 #pragma unroll
-    for (int g = 1; g < kMergeGroups; ++g) {
-      const float4 x = red_o[g][lane];
-      sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
-      W += red_w[g];
+    for (int g = 0; g < kMergeGroups; ++g) mx = fmaxf(mx, red_m[g]);
+    uint2 packed = make_uint2(0u, 0u);  // no visible key: O = 0, lse = -inf
+    float lse_out = -INFINITY;
+    if (mx != -INFINITY) {
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      float W = 0.f;
+#pragma unroll
+      for (int g = 0; g < kMergeGroups; ++g) {
+        const float f = fast_exp2((red_m[g] - mx) * kLog2e);  // empty groups: 0
+        const float4 x = red_o[g][lane];
+        sum.x = fmaf(f, x.x, sum.x);
+        sum.y = fmaf(f, x.y, sum.y);
+        sum.z = fmaf(f, x.z, sum.z);
+        sum.w = fmaf(f, x.w, sum.w);
+        W = fmaf(f, red_w[g], W);
+      }
+      const float inv = 1.f / W;
+      packed.x = pack_bf16x2(sum.x * inv, sum.y * inv);
+      packed.y = pack_bf16x2(sum.z * inv, sum.w * inv);
+      lse_out = mx + logf(W);
     }
-    const float inv = 1.f / W;
-    uint2 packed;
-    packed.x = pack_bf16x2(sum.x * inv, sum.y * inv);
-    packed.y = pack_bf16x2(sum.z * inv, sum.w * inv);
     reinterpret_cast<uint2 *>(o + row * kD)[lane] = packed;
-    if (lane == 0) lse[row] = mx + logf(W);
+    if (lane == 0) lse[row] = lse_out;
   }
 }
 
