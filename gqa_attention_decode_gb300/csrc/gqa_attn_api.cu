@@ -143,7 +143,7 @@ int check_decode_args(int phase, const void *q, const void *k, const void *v,
   if (H_q / H_kv > gqa::kDecodeMaxG) return GQA_ERR_UNSUPPORTED;
   if ((long long)(H_q / H_kv) * T_q > gqa::kDecodeMaxCols) return GQA_ERR_UNSUPPORTED;
   if (B > 65535 || H_kv > 65535) return GQA_ERR_UNSUPPORTED;  // grid y/z limits
-  if ((long long)H_q * T_q > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  if ((long long)B * H_q * T_q > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;  // output rows
   return GQA_OK;
 }
 

@@ -192,6 +192,7 @@ def test_multi_token_rejections(lib):
     assert call(1, 64, 8, 5) == gqa.GQA_ERR_UNSUPPORTED      # G * T_q = 40 > 32
     assert call(1, 64, 8, 0) == gqa.GQA_ERR_INVALID_ARG
     assert call(1, 64, 8, 2, d=64) == gqa.GQA_ERR_UNSUPPORTED
+    assert call(65535, 65536, 8192, 1) == gqa.GQA_ERR_UNSUPPORTED  # > 2^31 output rows
     assert call(0, 64, 8, 2) == gqa.GQA_OK
     assert gqa.gqa_attn_decode_multi_workspace_size(1, 64, 8, 4, 32768, 128, 152) == \
         4 * gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 152)
