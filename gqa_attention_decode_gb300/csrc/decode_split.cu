@@ -130,9 +130,11 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs written before us are visible
+  // Inputs written by earlier grids are visible after this wait; they are read
+  // with coherent loads (ld.global.ca), never the non-coherent read-only path.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int seqlen = min(max(p.seqlens[b], 0), p.S_max);
+  const int seqlen = min(max(__ldca(p.seqlens + b), 0), p.S_max);
   const int key_begin = split * p.chunk;
   const int key_end = min(key_begin + p.chunk, seqlen);
   if (!kFused && key_begin >= key_end) return;  // empty split: the merge never reads it
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
         if (page - page_base >= 32 || page < page_base) {
           page_base = page;
           const int idx = page_base + lane;
-          page_reg = idx < p.max_pages ? __ldg(p.block_table + (size_t)b * p.max_pages + idx) : 0;
+          page_reg = idx < p.max_pages ? __ldca(p.block_table + (size_t)b * p.max_pages + idx) : 0;
         }
         const int page_id = __shfl_sync(0xffffffffu, page_reg, page - page_base);
         c2 = key0 - page * p.page_size;
@@ -208,8 +210,8 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
           p.q + (((size_t)b * p.H_q + (size_t)kv * p.G + gh) * p.T_q + tq) * kD);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        qf[kk][j][0] = col_ok ? __ldg(qrow + kk * 8 + t) : 0u;
-        qf[kk][j][1] = col_ok ? __ldg(qrow + kk * 8 + 4 + t) : 0u;
+        qf[kk][j][0] = col_ok ? __ldca(qrow + kk * 8 + t) : 0u;
+        qf[kk][j][1] = col_ok ? __ldca(qrow + kk * 8 + 4 + t) : 0u;
       }
     }
     // keys each of this thread's columns may see (split end and causal limit)
@@ -461,18 +463,23 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     }
     cluster_sync();  // no CTA leaves while others still read its shared memory
   }
-  // this CTA's partial is written: the merge grid may be scheduled
+  // this CTA's partial is written: the merge grid may be scheduled (triggering
+  // at the start instead measured 1 us slower per call: the waiting merge CTAs
+  // slow the streaming ones)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // One CTA per (query head, new token) row of a sequence, 256 threads: thread
 // (g, lane) owns columns 4*lane .. 4*lane+3 and merges splits g, g+8, g+16, ...
-// on the fly (online log-sum-exp, the lse and O loads of all its splits in
-// flight together); the eight group states are then combined once in shared
-// memory.  lse = m + ln sum_s exp(lse_s - m); O = sum_s exp(lse_s - lse) O_s.
-// Launched as a programmatic dependent of the split kernel.
+// with an online log-sum-exp, kMergeRound splits per round whose lse and O
+// loads are all issued before any is used (one L2 round trip for up to 32
+// splits); the eight group states are then combined once in shared memory.
+// lse = m + ln sum_s exp(lse_s - m); O = sum_s exp(lse_s - lse) O_s.
+// Launched as a programmatic dependent of the split kernel; the partials are
+// read through L2 (they were written by the split grid).
 constexpr int kMergeThreads = 256;
 constexpr int kMergeGroups = kMergeThreads / 32;
+constexpr int kMergeRound = 4;
 
 __global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
@@ -486,7 +493,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int h = blockIdx.x, b = blockIdx.y;  // h: (query head, new token) row of sequence b
   const int t = threadIdx.x, grp = t >> 5, lane = t & 31;
-  const int seqlen = min(max(seqlens[b], 0), S_max);
+  const int seqlen = min(max(__ldcg(seqlens + b), 0), S_max);
   const int ns = min((seqlen + chunk - 1) / chunk, num_splits);
   const size_t row = (size_t)b * gridDim.x + h;
   const float *lp = lse_part + row * num_splits;
@@ -494,20 +501,28 @@ __global__ void __launch_bounds__(kMergeThreads)
   constexpr float kLog2e = 1.4426950408889634f;
   float m = -INFINITY, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int s = grp; s < ns; s += kMergeGroups) {
-    const float ls = lp[s];
-    const float4 x = op[(size_t)s * (kD / 4)];
-    if (ls == -INFINITY) continue;  // a split that saw no key of this row
-    const float m_new = fmaxf(m, ls);
-    const float c = fast_exp2((m - m_new) * kLog2e);  // 0 while m is -inf
-    const float w = fast_exp2((ls - m_new) * kLog2e);
-    wsum = wsum * c + w;
-    acc.x = fmaf(w, x.x, acc.x * c);
-    acc.y = fmaf(w, x.y, acc.y * c);
-    acc.z = fmaf(w, x.z, acc.z * c);
-    acc.w = fmaf(w, x.w, acc.w * c);
-    m = m_new;
+  for (int s0 = grp; s0 < ns; s0 += kMergeGroups * kMergeRound) {
+    float ls[kMergeRound];
+    float4 x[kMergeRound];
+#pragma unroll
+    for (int u = 0; u < kMergeRound; ++u) {
+      const int s = s0 + u * kMergeGroups;
+      ls[u] = s < ns ? __ldcg(lp + s) : -INFINITY;
+      x[u] = s < ns ? __ldcg(op + (size_t)s * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeRound; ++u) {
+      if (ls[u] == -INFINITY) continue;  // a split that saw no key of this row
+      const float m_new = fmaxf(m, ls[u]);
+      const float c = fast_exp2((m - m_new) * kLog2e);  // 0 while m is -inf
+      const float w = fast_exp2((ls[u] - m_new) * kLog2e);
+      wsum = wsum * c + w;
+      acc.x = fmaf(w, x[u].x, acc.x * c);
+      acc.y = fmaf(w, x[u].y, acc.y * c);
+      acc.z = fmaf(w, x[u].z, acc.z * c);
+      acc.w = fmaf(w, x[u].w, acc.w * c);
+      m = m_new;
+    }
   }
   red_o[grp][lane] = acc;
   if (lane == 0) {
