@@ -26,6 +26,7 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   int fused_clusters[gqa::kDecodeMaxFusedSplits + 1] = {};
+  int prefill_pairs = 0;  // clusters of two of the CTA-pair prefill kernel resident at once
   int *status = nullptr;
 };
 
@@ -60,6 +61,7 @@ int device_state(DeviceState **out) {
     if (cudaGetSymbolAddress(&status, g_wait_status) != cudaSuccess) return GQA_ERR_CUDA;
     if (gqa::decode_prepare_device(st.fused_clusters) != cudaSuccess) return GQA_ERR_CUDA;
     if (gqa::prefill_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
+    if (gqa::prefill_pair_prepare_device(&st.prefill_pairs) != cudaSuccess) return GQA_ERR_CUDA;
     st.num_sms = sms;
     st.status = static_cast<int *>(status);
     st.ready = true;
@@ -387,9 +389,13 @@ GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
   a.o = o;
   a.lse = lse;
   a.num_sms = st->num_sms;
+  a.max_pairs = st->prefill_pairs;
   a.wait.status = st->status;
   a.wait.timeout_ns = kWaitTimeoutNs;
-  cudaError_t e = gqa::prefill_launch(a, static_cast<cudaStream_t>(stream), g_encode);
+  // group sizes that are multiples of 4: the CTA-pair kernel; others: one CTA per unit
+  cudaError_t e = gqa::prefill_pair_eligible(a)
+                      ? gqa::prefill_pair_launch(a, static_cast<cudaStream_t>(stream), g_encode)
+                      : gqa::prefill_launch(a, static_cast<cudaStream_t>(stream), g_encode);
   if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
   return to_status(e);
 }

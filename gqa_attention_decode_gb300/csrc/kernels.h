@@ -61,12 +61,19 @@ struct PrefillLaunch {
   uint16_t *o;  // [B, H_q, T_q, d]
   float *lse;   // [B, H_q, T_q]
   int num_sms;
+  int max_pairs;  // CTA-pair kernel: clusters of two resident at once (0: not available)
   WaitCtl wait;
 };
 
+// Single-CTA kernel (any group size).
 cudaError_t prefill_prepare_device();
 cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
                            PFN_cuTensorMapEncodeTiled_v12000 encode);
+// CTA-pair kernel (tcgen05 cta_group::2), for group sizes that are multiples of 4.
+cudaError_t prefill_pair_prepare_device(int *max_pairs);
+bool prefill_pair_eligible(const PrefillLaunch &a);
+cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
+                                PFN_cuTensorMapEncodeTiled_v12000 encode);
 
 // ---- diagnostics --------------------------------------------------------------
 cudaError_t selftest_bounded_wait_launch(WaitCtl wait, cudaStream_t stream);

@@ -51,6 +51,8 @@ def run(q, k, v, q_offset, scale):
     (1, 8, 1, 1, 1, 0),           # one query, one key
     (1, 8, 1, 1, 517, 516),       # one query at the end of a long prefix
     (1, 16, 2, 384, 384, 0),      # exact multiple of the tile
+    (2, 8, 2, 300, 1000, 700),    # G = 4: one head quad per KV head, two sequences
+    (1, 12, 1, 200, 200, 0),      # G = 12: three head quads
 ])
 def test_small_cases_full_compare(B, H_q, H_kv, T_q, S_kv, q_offset):
     q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=31, device=DEV)
@@ -90,6 +92,25 @@ def test_prefill_workloads_sampled(name):
     got_o = torch.stack([o[b, h, i] for b, h, i in picks])
     got_lse = torch.stack([lse[b, h, i] for b, h, i in picks])
     compare(got_o, got_lse, ref_o, ref_lse, name)
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (4, 2)])   # G = 4 (CTA pairs), G = 2 (one CTA)
+def test_running_max_paths(H_q, H_kv):
+    """Scores chosen in log2 units (scale = ln 2, q = e_0): key tile 0 scores 0,
+    tile 1 scores 7 (every exp is 2^7, the tile sum far above 2^8, yet the max
+    stays within 8 of the reference: no rescale), tile 2 scores 20 (the max
+    jumps by more than 8: O and the sum are rescaled and the tile redone)."""
+    T = 384
+    q, k, v = gqa_synth.prefill_inputs(1, H_q, H_kv, T, T, 128, seed=33, device=DEV)
+    q.zero_()
+    q[..., 0] = 1.0
+    k.zero_()
+    k[:, :, 128:256, 0] = 7.0
+    k[:, :, 256:, 0] = 20.0
+    scale = math.log(2.0)
+    o, lse = run(q, k, v, 0, scale)
+    o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), 0, scale)
+    compare(o, lse, o_ref, lse_ref, f"running max paths G={H_q // H_kv}")
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.15, 0.3])
