@@ -79,6 +79,13 @@ struct Unit {
   bool second_valid;
 };
 
+// Unit of round k for worker w of P: units are sorted longest first and dealt
+// in snake order (left to right, then right to left), so no worker takes the
+// longest unit of every round; only the last round can be partial.
+__device__ __forceinline__ int snake_unit(int k, int w, int P) {
+  return k * P + ((k & 1) ? P - 1 - w : w);
+}
+
 __device__ __forceinline__ Unit unit_at(const Params &p, int u) {
   Unit w;
   const int per_qt = p.B * p.H_kv * p.n_pairs;
@@ -186,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = l2_policy_evict_last();
       int ld = 0, it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++it) {
+      for (int k = 0; ok; ++k, ++it) {
+        const int u = snake_unit(k, blockIdx.x, gridDim.x);
+        if (u >= p.total_units) break;
         const Unit w = unit_at(p, u);
         if (!wait_abortable(q_empty, (it & 1) ^ 1, p.wait, abort_flag)) { ok = false; break; }
         for (int i = 0; i < 2; ++i) {
@@ -227,7 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_smem[2] = {sbase + kOffQ, sbase + kOffQ + kTileBytes};
       int ld_base = 0, tile_base = 0, it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++it) {
+      for (int k = 0; ok; ++k, ++it) {
+        const int u = snake_unit(k, blockIdx.x, gridDim.x);
+        if (u >= p.total_units) break;
         const Unit w = unit_at(p, u);
         const int n = w.n_kv;
         for (int i = 0; ok && i < 2; ++i)
@@ -295,7 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float mul = pos_scale ? p.sl2 : 1.f;  // multiplier still owed by the held scores
     int tile = 0, it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++it) {
+    for (int k = 0; ok; ++k, ++it) {
+      const int u = snake_unit(k, blockIdx.x, gridDim.x);
+      if (u >= p.total_units) break;
       const Unit w = unit_at(p, u);
       const int q0 = p.q_offset + w.qt * kBM;  // absolute position of row 0 of the tile
       const int qpos = q0 + row;
