@@ -46,7 +46,14 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 KERNEL_SOURCES = {
     "decode_split_kernel": "gqa_attention_decode_gb300/csrc/decode_split.cu",
     "prefill_causal_kernel": "gqa_attention_decode_gb300/csrc/prefill_causal.cu",
+    "prefill_pair_kernel": "gqa_attention_decode_gb300/csrc/prefill_pair.cu",
 }
+
+
+def prefill_kernel_name(G):
+    """The prefill kernel the library runs for group size G: CTA pairs when G is
+    a multiple of 4, one CTA per unit otherwise."""
+    return "prefill_pair_kernel" if G % 4 == 0 else "prefill_causal_kernel"
 
 
 # ---------------------------------------------------------------------------
@@ -471,11 +478,11 @@ def run_ours(args, rank, world, device):
         result["prefill"] = {
             "workload": PREFILL_WORKLOAD, "value": world * tflops, "unit": "TFLOP/s",
             "us_per_call": pms * 1e3, "flops_per_call": flops_prefill,
-            "roofline": {"bound": "tensor", "kernel": "prefill_causal_kernel",
+            "roofline": {"bound": "tensor", "kernel": prefill_kernel_name(wp.G),
                          "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": tflops / peaks["bf16_tflops"],
                          "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
-                         "traffic": recorded_traffic("prefill_causal_kernel"),
+                         "traffic": recorded_traffic(prefill_kernel_name(wp.G)),
                          "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)"}}
         if "decode" not in parts:
             result["value"] = world * tflops
