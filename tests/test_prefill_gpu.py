@@ -94,6 +94,47 @@ def test_prefill_workloads_sampled(name):
     compare(got_o, got_lse, ref_o, ref_lse, name)
 
 
+def _seeded_configs(n, seed):
+    """Random shapes: group sizes that use CTA pairs (4, 8, 12, 16) and one CTA
+    per unit (1, 2, 3, 6), ragged query tiles, q_offset anywhere in a tile."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        G = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16]))
+        H_kv = int(rng.integers(1, 3))
+        B = int(rng.integers(1, 3))
+        T_q = int(rng.integers(1, 400))
+        q_offset = int(rng.integers(0, 300))
+        out.append((B, G * H_kv, H_kv, T_q, q_offset + T_q, q_offset))
+    return out
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,T_q,S_kv,q_offset", _seeded_configs(10, 2024))
+def test_seeded_random_shapes(B, H_q, H_kv, T_q, S_kv, q_offset):
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=37, device=DEV)
+    o, lse = run(q, k, v, q_offset, 0.09)
+    o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), q_offset, 0.09)
+    compare(o, lse, o_ref, lse_ref, f"random {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
+
+
+def test_group_of_16_sampled():
+    """G = 16 (four head quads per KV head), 4K causal, sampled rows."""
+    B, H_q, H_kv, T = 1, 32, 2, 4096
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T, T, 128, seed=38, device=DEV)
+    o, lse = run(q, k, v, 0, 1 / math.sqrt(128))
+    rng = np.random.default_rng(8)
+    picks = [(0, int(h), int(i)) for h, i in zip(rng.integers(0, H_q, 40), rng.integers(0, T, 40))]
+    picks += [(0, 31, T - 1), (0, 16, 0), (0, 15, 128)]
+    ref_o = np.zeros((len(picks), 128))
+    ref_lse = np.zeros(len(picks))
+    for r, (b, h, i) in enumerate(picks):
+        ro, rl = oracle.attend_rows(np64(q[b, h, i])[None], np64(k[b, h // 16, :i + 1]),
+                                    np64(v[b, h // 16, :i + 1]), 1 / math.sqrt(128), [i + 1])
+        ref_o[r], ref_lse[r] = ro[0], rl[0]
+    compare(torch.stack([o[b, h, i] for b, h, i in picks]),
+            torch.stack([lse[b, h, i] for b, h, i in picks]), ref_o, ref_lse, "G = 16")
+
+
 @pytest.mark.parametrize("H_q,H_kv", [(8, 2), (4, 2)])   # G = 4 (CTA pairs), G = 2 (one CTA)
 def test_running_max_paths(H_q, H_kv):
     """Scores chosen in log2 units (scale = ln 2, q = e_0): key tile 0 scores 0,
