@@ -1,0 +1,506 @@
+// decode_tc.cu -- split-KV multi-token GQA decode on tcgen05 tensor cores (sm_103a).
+//
+// What it computes (design record "ADR-0060: AHBM GQA Fused Attention Kernel
+// (Llama3-70B)"): decode with T_q new tokens per sequence, the record's T_q of
+// section 0.5.2 with all G * T_q (head, token) rows of one KV head stacked into
+// one matrix product (section 5.2's fold), so each K/V tile is read from HBM
+// once for every row.  Token t of sequence b sits at position seqlen - T_q + t
+// and sees keys up to it.  The key range is cut into contiguous chunks
+// (section 2.1); each CTA runs the per-tile online softmax of section 3 over its
+// chunk and writes one partial per row (O_s / l_s, lse_s), which the decode
+// merge kernel combines (section 4).  Used for 32 < G * T_q <= 128, where the
+// rows fill a 128-row tensor-core tile.
+//
+// GB300 mapping
+//   * grid (splits, H_kv, B), 320 threads: warp 8 TMA producer (the row block
+//     of Q once, then 128-key K and V tiles through a 5-stage ring), warp 9
+//     TMEM allocation and the single thread issuing tcgen05.mma (M = 128 rows,
+//     N = 128 keys or d, K = 16, bf16 in, fp32 accumulate), warps 0-3 / 4-7
+//     softmax for two slots (one thread per row).  Slot s takes the key tiles
+//     of parity s with its own S and O in tensor memory, so the tensor core
+//     works on one slot's tile while the other slot's softmax runs; the two
+//     slots' (m, l, O) are combined per row at the end.
+//   * Rows past G * T_q in the 128-row tile (other heads' queries, or zeros
+//     past the tensor) are computed and never stored.
+//   * Decode moves 128 flop per byte of K/V here (128 rows): still below the
+//     tensor ridge, so the kernel streams K/V at HBM rate like the T_q = 1 path.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "device_common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace gqa {
+namespace decode_tc {
+
+constexpr int kD = 128;
+constexpr int kRows = 128;                 // tensor-core rows: (head, token) pairs of one KV head
+constexpr int kBN = 128;                   // keys per tile
+constexpr int kStages = 5;                 // ring of 32 KiB stages (a K or a V tile)
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kThreads = 320;
+constexpr int kTileBytes = kRows * kD * 2;  // 32 KiB
+constexpr int kHalfBytes = kTileBytes / 2;  // one 64-column half: [128 rows x 128 B]
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kTileBytes;
+constexpr int kOffBar = kOffStage + kStages * kTileBytes;
+// barriers: kv_full[S], kv_empty[S], q_full, s_full[2], p_full[2], o_final[2], tok[2],
+// slot-1 epilogue, drain, V tail cleared
+constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;        // tmem slot, abort flag
+constexpr int kOffRed = kOffMisc + 16;                  // slot-1 (m, l) per row
+constexpr int kSmemBytes = kOffRed + 2 * kRows * 4 + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kSumTrigger = 256.0f;      // 2^kRescaleThreshold
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Params {
+  const int32_t *seqlens;
+  float *o_part;
+  float *lse_part;
+  int B, H_q, H_kv, G, T_q, S_max, num_splits, chunk;
+  float sl2;  // scale * log2(e)
+  WaitCtl wait;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl &ctl,
+                                         volatile int *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > ctl.timeout_ns) {
+      atomicExch(ctl.status, kStatusTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// k-step kk of a K-major 128-row tile stored as two 128B-swizzled 64-column halves.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+  return tc::smem_desc_sw128(tile + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+}
+// k-step kk (16 keys) of an MN-major V tile (keys x d, d contiguous in two halves).
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
+  return tc::smem_desc_sw128(tile + kk * 2048, kHalfBytes, 1024);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + kOffBar;
+  auto kv_full = [&](int s) { return bar0 + 8u * s; };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t q_full = bar0 + 8u * (2 * kStages);
+  auto s_full = [&](int i) { return bar0 + 8u * (2 * kStages + 1 + i); };
+  auto p_full = [&](int i) { return bar0 + 8u * (2 * kStages + 3 + i); };
+  auto o_final = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + i); };
+  auto tok = [&](int i) { return bar0 + 8u * (2 * kStages + 7 + i); };
+  const uint32_t slot1_done = bar0 + 8u * (2 * kStages + 9);
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 10);
+  const uint32_t v_tail = bar0 + 8u * (2 * kStages + 11);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+  float *red_m = reinterpret_cast<float *>(smem + kOffRed);
+  float *red_l = red_m + kRows;
+
+  const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // inputs written by earlier grids are visible after this wait (coherent loads)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int seqlen = min(max(__ldca(p.seqlens + b), 0), p.S_max);
+  const int key_begin = split * p.chunk;
+  const int key_end = min(key_begin + p.chunk, seqlen);
+  if (key_begin >= key_end) return;  // empty split: the merge never reads it
+  const int n_tiles = (key_end - key_begin + kBN - 1) / kBN;
+  const int n_slot[2] = {(n_tiles + 1) / 2, n_tiles / 2};  // slot s: tiles j with j % 2 == s
+  const int R = p.G * p.T_q;                                 // rows that are stored
+  // the last tile may run past the sequence: its V rows there (cache rows that
+  // may hold any bits) are cleared before P V reads them
+  const int tail_keys = key_begin + n_tiles * kBN - seqlen;  // > 0: rows to clear
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full(i), 1);
+      mbar_init(p_full(i), 128);
+      mbar_init(o_final(i), 1);
+      mbar_init(tok(i), 128);
+    }
+    mbar_init(slot1_done, 128);
+    mbar_init(drain_bar, 1);
+    mbar_init(v_tail, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpTma) {
+    // ------------------------- TMA producer -------------------------
+    int ld = 0;
+    bool ok = true;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol = l2_policy_evict_first();
+      const int q_row0 = (b * p.H_q + kv * p.G) * p.T_q;  // first (head, token) row of the group
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      for (int half = 0; half < 2; ++half)
+        tma_load_4d(sbase + kOffQ + half * kHalfBytes, &tm_q, q_full, 0, half, q_row0, 0, pol);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        for (int which = 0; which < 2; ++which, ++ld) {
+          const int s = ld % kStages;
+          if (!wait_bar(kv_empty(s), ((ld / kStages) & 1) ^ 1, p.wait, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sbase + kOffStage + s * kTileBytes;
+          mbar_arrive_expect_tx(kv_full(s), kTileBytes);
+          const CUtensorMap *map = which == 0 ? &tm_k : &tm_v;
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(dst + half * kHalfBytes, map, kv_full(s), 0, half, key_begin + j * kBN,
+                        b * p.H_kv + kv, pol);
+        }
+      }
+    }
+    ld = __shfl_sync(0xffffffffu, ld, 0);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok && tail_keys > 0) {
+      // last V tile (load ld - 1): the warp zeroes rows [kBN - tail_keys, kBN) of
+      // both halves once the copy has landed
+      const int i = ld - 1;
+      const bool landed = wait_bar(kv_full(i % kStages), (i / kStages) & 1, p.wait, abort_flag);
+      if (__all_sync(0xffffffffu, landed)) {
+        uint8_t *vt = smem + kOffStage + (i % kStages) * kTileBytes;
+        const int first = kBN - tail_keys;
+        for (int idx = lane; idx < tail_keys * 16; idx += 32) {  // 16 chunks of 16 B per row
+          const int r = first + idx / 16, c = idx % 16;
+          *reinterpret_cast<uint4 *>(vt + (c >> 3) * kHalfBytes + r * 128 + (c & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // the tensor core reads these rows
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(v_tail);
+    }
+    if (lane == 0) {
+      for (int i = max(0, ld - kStages); i < ld; ++i)
+        wait_bar(kv_full(i % kStages), (i / kStages) & 1, p.wait, abort_flag);
+      wait_bar(q_full, 0, p.wait, abort_flag);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------- MMA issuer -------------------------
+    // Step j: O_s += P_s(j-2) V(j-2), then S_s(j) = Q K(j)^T, with s = j % 2 (the
+    // P V of a slot must precede the S that overwrites its P).
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kRows, kBN, 0);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, kD, 1);
+      const uint32_t t_s[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t t_o[2] = {tmem + 256u, tmem + 384u};
+      bool ok = wait_bar(q_full, 0, p.wait, abort_flag);
+      tc::fence_after_sync();
+      for (int j = 0; ok && j < n_tiles + 2; ++j) {
+        const int s = j & 1;
+        if (j >= 2) {
+          const int t = j - 2, ldV = 2 * t + 1;
+          if (!wait_bar(kv_full(ldV % kStages), (ldV / kStages) & 1, p.wait, abort_flag) ||
+              (t == n_tiles - 1 && tail_keys > 0 && !wait_bar(v_tail, 0, p.wait, abort_flag)) ||
+              !wait_bar(p_full(s), (t >> 1) & 1, p.wait, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t v_smem = sbase + kOffStage + (ldV % kStages) * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            tc::mma_ts(t_o[s], t_s[s] + kk * 8, desc_mnmajor(v_smem, kk), idesc_pv,
+                       (t >= 2 || kk > 0) ? 1u : 0u);
+          tc::commit(kv_empty(ldV % kStages));
+          if (t + 2 >= n_tiles) tc::commit(o_final(s));  // the slot's last tile
+        }
+        if (j < n_tiles) {
+          const int ldK = 2 * j;
+          if (!wait_bar(kv_full(ldK % kStages), (ldK / kStages) & 1, p.wait, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t k_smem = sbase + kOffStage + (ldK % kStages) * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            tc::mma_ss(t_s[s], desc_kmajor(sbase + kOffQ, kk), desc_kmajor(k_smem, kk), idesc_s,
+                       kk > 0 ? 1u : 0u);
+          tc::commit(s_full(s));
+          tc::commit(kv_empty(ldK % kStages));
+        }
+      }
+      tc::commit(drain_bar);
+      wait_bar(drain_bar, 0, p.wait, abort_flag);
+    }
+  } else {
+    // ------------------------- softmax slots -------------------------
+    const int s = warp >> 2;   // slot: key tiles of parity s
+    const int wq = warp & 3;   // TMEM lane quarter
+    const int row = 32 * wq + lane;
+    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+    const uint32_t t_s = tmem + lane_off + 128u * s;
+    const uint32_t t_o = tmem + lane_off + 256u + 128u * s;
+    // keys this row may see: the causal limit of its token (rows past R see all)
+    const int lim = row < R ? min(key_end, seqlen - p.T_q + row % p.T_q + 1) : key_end;
+    const bool pos_scale = p.sl2 > 0.f;
+    const float mul = pos_scale ? p.sl2 : 1.f;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int k = 0; ok && k < n_slot[s]; ++k) {
+      const int key0 = key_begin + (2 * k + s) * kBN;
+      bool ready = wait_bar(s_full(s), k & 1, p.wait, abort_flag);
+      if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+      tc::fence_after_sync();
+      uint32_t sv[kBN];
+      // S row from tensor memory; keys the row may not see are -inf
+      auto load_s = [&]() {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::ld32(t_s + 32 * c, sv + 32 * c);
+        tc::wait_ld();
+        if (!pos_scale) {
+#pragma unroll
+          for (int e = 0; e < kBN; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * p.sl2);
+        }
+        if (key0 + kBN > lim) {
+#pragma unroll
+          for (int e = 0; e < kBN; ++e)
+            if (key0 + e >= lim) sv[e] = __float_as_uint(-INFINITY);
+        }
+      };
+      load_s();
+      auto row_max = [&]() {
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < kBN; e += 8)
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            mx4[k4] = fmax3(mx4[k4], __uint_as_float(sv[e + 2 * k4]),
+                            __uint_as_float(sv[e + 2 * k4 + 1]));
+        const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+        return pos_scale ? mx * p.sl2 : mx;
+      };
+      uint32_t pk[kBN / 2];
+      // P = exp2(s * scale log2e - ref) as bf16 pairs; ref = 0 while no key was seen
+      auto exp_pass = [&]() {
+        const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
+        const uint64_t mul2 = f32x2(mul, mul), negm2 = f32x2(negm, negm);
+        uint64_t rs2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+#pragma unroll
+        for (int e = 0; e < kBN / 2; ++e) {
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
+                                mul2, negm2),
+                      x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          rs2[e & 1] = add_f32x2(rs2[e & 1], f32x2(p0, p1));
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        float a0, a1, a2, a3;
+        f32x2_split(rs2[0], a0, a1);
+        f32x2_split(rs2[1], a2, a3);
+        return (a0 + a1) + (a2 + a3);
+      };
+      if (k == 0) m_ref = row_max();
+      // exp turn: slot 0's tile k follows slot 1's tile k-1, slot 1's tile k follows
+      // slot 0's tile k
+      if (s == 0) {
+        ready = k == 0 || wait_bar(tok(0), (k - 1) & 1, p.wait, abort_flag);
+      } else {
+        ready = wait_bar(tok(1), k & 1, p.wait, abort_flag);
+      }
+      if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+      float tsum = exp_pass();
+      // the reference max moves only when a score exceeds it by more than the
+      // threshold, which makes the tile's sum exceed 2^threshold (or not finite)
+      if (k > 0 && __any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
+        load_s();  // S is still in tensor memory (P not yet written over it)
+        const float mt = row_max();
+        if (__any_sync(0xffffffffu, mt > m_ref + kRescaleThreshold)) {
+          const float m_new = fmaxf(m_ref, mt);
+          const float corr = m_new == -INFINITY ? 1.f : fast_exp2(m_ref - m_new);  // 0 from -inf
+          l *= corr;
+          // O holds P V up to the slot's previous tile (complete: S was issued after it)
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tc::ld32(t_o + 32 * c, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+            tc::st32(t_o + 32 * c, r);
+          }
+          tc::wait_st();
+          m_ref = m_new;
+          tsum = exp_pass();
+        }
+      }
+      // the other slot may use the exp unit now (slot 1 of an odd tile count has
+      // no tile k = n_slot[0] - 1 to hand the token to: it is simply not awaited)
+      mbar_arrive(tok(1 - s));
+      tc::st32(t_s, pk);
+      tc::st32(t_s + 32, pk + 32);
+      tc::wait_st();
+      l += tsum;
+      tc::fence_before_sync();
+      mbar_arrive(p_full(s));
+    }
+    // ---- epilogue: combine the two slots per row, write the split partial ----
+    if (s == 1) {
+      if (ok && n_slot[1] > 0) {
+        const bool ready = wait_bar(o_final(1), 0, p.wait, abort_flag);
+        ok = __all_sync(0xffffffffu, ready);
+      }
+      red_m[row] = (ok && n_slot[1] > 0) ? m_ref : -INFINITY;
+      red_l[row] = (ok && n_slot[1] > 0) ? l : 0.f;
+      tc::fence_before_sync();
+      mbar_arrive(slot1_done);
+    } else {
+      if (ok) {
+        const bool ready = wait_bar(o_final(0), 0, p.wait, abort_flag) &&
+                           wait_bar(slot1_done, 0, p.wait, abort_flag);
+        ok = __all_sync(0xffffffffu, ready);
+      }
+      if (ok) {
+        tc::fence_after_sync();
+        const float m1 = red_m[row], l1 = red_l[row];
+        const float m0 = l > 0.f ? m_ref : -INFINITY;
+        const float mx = fmaxf(m0, m1);
+        const float w0 = l > 0.f ? fast_exp2(m0 - mx) : 0.f;
+        const float w1 = l1 > 0.f ? fast_exp2(m1 - mx) : 0.f;
+        const float L = w0 * l + w1 * l1;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float c0 = w0 * inv, c1 = w1 * inv;  // 0 for a slot with no visible key
+        const bool use1 = n_slot[1] > 0;            // warp-uniform
+        if (row < R) {
+          const size_t orow = (size_t)(b * p.H_q + kv * p.G) * p.T_q + row;
+          p.lse_part[orow * p.num_splits + split] =
+              L > 0.f ? mx * 0.69314718055994531f + logf(L) : -INFINITY;
+        }
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r0[32], r1[32];
+          tc::ld32(t_o + 32 * c, r0);
+          if (use1) tc::ld32(t_o + 128u + 32 * c, r1);
+          tc::wait_ld();
+          if (row < R) {
+            const size_t orow = (size_t)(b * p.H_q + kv * p.G) * p.T_q + row;
+            float4 *dst =
+                reinterpret_cast<float4 *>(p.o_part + (orow * p.num_splits + split) * kD) + 8 * c;
+            // both slots' O are finite (every slot with a tile wrote its O, and V
+            // rows past the sequence were cleared); a slot with no tile is skipped
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float4 v;
+              v.x = c0 * __uint_as_float(r0[4 * e + 0]);
+              v.y = c0 * __uint_as_float(r0[4 * e + 1]);
+              v.z = c0 * __uint_as_float(r0[4 * e + 2]);
+              v.w = c0 * __uint_as_float(r0[4 * e + 3]);
+              if (use1) {
+                v.x = fmaf(c1, __uint_as_float(r1[4 * e + 0]), v.x);
+                v.y = fmaf(c1, __uint_as_float(r1[4 * e + 1]), v.y);
+                v.z = fmaf(c1, __uint_as_float(r1[4 * e + 2]), v.z);
+                v.w = fmaf(c1, __uint_as_float(r1[4 * e + 3]), v.w);
+              }
+              dst[e] = v;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  // this CTA's partials are written: the merge grid may be scheduled
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// dims (innermost first): 64 columns, 2 column halves, rows, blocks
+CUresult make_map(CUtensorMap *map, const uint16_t *base, long long rows, long long blocks,
+                  PFN_cuTensorMapEncodeTiled_v12000 encode) {
+  const cuuint64_t dims[4] = {64, 2, (cuuint64_t)rows, (cuuint64_t)blocks};
+  const cuuint64_t strides[3] = {128, 256, (cuuint64_t)rows * 256};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(base), dims,
+                strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace decode_tc
+
+cudaError_t decode_tc_prepare_device() {
+  return cudaFuncSetAttribute(decode_tc::decode_tc_kernel,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, decode_tc::kSmemBytes);
+}
+
+cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
+                                   PFN_cuTensorMapEncodeTiled_v12000 encode) {
+  using namespace decode_tc;
+  if (a.S_max <= 0) return cudaSuccess;
+  if (a.chunk % kBN != 0 || a.block_table != nullptr) return cudaErrorInvalidValue;
+  CUtensorMap tm_q, tm_k, tm_v;
+  const long long q_rows = (long long)a.B * a.H_q * a.T_q;
+  if (make_map(&tm_q, a.q, q_rows, 1, encode) != CUDA_SUCCESS ||
+      make_map(&tm_k, a.k_cache, a.S_max, (long long)a.B * a.H_kv, encode) != CUDA_SUCCESS ||
+      make_map(&tm_v, a.v_cache, a.S_max, (long long)a.B * a.H_kv, encode) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  Params p;
+  p.seqlens = a.seqlens;
+  p.o_part = a.o_part;
+  p.lse_part = a.lse_part;
+  p.B = a.B;
+  p.H_q = a.H_q;
+  p.H_kv = a.H_kv;
+  p.G = a.H_q / a.H_kv;
+  p.T_q = a.T_q;
+  p.S_max = a.S_max;
+  p.num_splits = a.num_splits;
+  p.chunk = a.chunk;
+  p.sl2 = a.scale * 1.4426950408889634f;
+  p.wait = a.wait;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_splits, a.H_kv, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, tm_q, tm_k, tm_v, p);
+}
+
+}  // namespace gqa

@@ -61,6 +61,7 @@ int device_state(DeviceState **out) {
     if (cudaGetSymbolAddress(&status, g_wait_status) != cudaSuccess) return GQA_ERR_CUDA;
     if (gqa::decode_prepare_device(st.fused_clusters) != cudaSuccess) return GQA_ERR_CUDA;
     if (gqa::prefill_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
+    if (gqa::decode_tc_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
     if (gqa::prefill_pair_prepare_device(&st.prefill_pairs) != cudaSuccess) return GQA_ERR_CUDA;
     st.num_sms = sms;
     st.status = static_cast<int *>(status);
@@ -113,6 +114,24 @@ int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_split
   return GQA_OK;
 }
 
+// Decode rows per KV head (G * T_q) that the mma.sync split kernel serves; larger
+// row counts (or G > 8) on a dense cache go to the tcgen05 split kernel.
+bool decode_on_tensor_cores(int H_q, int H_kv, int T_q) {
+  const long long G = H_q / H_kv;
+  return G > gqa::kDecodeMaxG || G * T_q > gqa::kDecodeMaxCols;
+}
+
+// plan() plus the tcgen05 kernel's rule that a chunk holds whole 128-key tiles.
+int plan_decode(int B, int H_q, int H_kv, int T_q, int S_max, int num_sms, int num_splits,
+                int *out_splits, int *out_chunk) {
+  int rc = plan(B, H_kv, S_max, num_sms, num_splits, out_splits, out_chunk);
+  if (rc != GQA_OK || H_q <= 0 || H_kv <= 0 || !decode_on_tensor_cores(H_q, H_kv, T_q)) return rc;
+  const int t = gqa::kDecodeTcTileKeys;
+  *out_chunk = (*out_chunk + t - 1) / t * t;
+  *out_splits = S_max > 0 ? ceil_div(S_max, *out_chunk) : 1;
+  return GQA_OK;
+}
+
 size_t decode_ws_bytes(int B, int H_q, int splits, int d, int T_q = 1) {
   return round256((size_t)B * H_q * T_q * splits * (size_t)(d + 1) * sizeof(float));
 }
@@ -127,7 +146,8 @@ bool finite_scale(float scale) {
 // be null.
 int check_decode_args(int phase, const void *q, const void *k, const void *v,
                       const void *seqlens, int B, int H_q, int H_kv, int S_max, int d,
-                      float scale, int num_splits, const void *o, const void *lse, int T_q = 1) {
+                      float scale, int num_splits, const void *o, const void *lse, int T_q = 1,
+                      bool paged = false) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || S_max < 0 || d <= 0 || num_splits < 0 || T_q <= 0)
     return GQA_ERR_INVALID_ARG;
   if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
@@ -142,8 +162,11 @@ int check_decode_args(int phase, const void *q, const void *k, const void *v,
     if (!o || !lse || !aligned16(o) || !aligned16(lse)) return GQA_ERR_INVALID_ARG;
   }
   if (d != 128) return GQA_ERR_UNSUPPORTED;
-  if (H_q / H_kv > gqa::kDecodeMaxG) return GQA_ERR_UNSUPPORTED;
-  if ((long long)(H_q / H_kv) * T_q > gqa::kDecodeMaxCols) return GQA_ERR_UNSUPPORTED;
+  // mma.sync split kernel: G <= 8 and G * T_q <= 32 rows per KV head; otherwise
+  // the tcgen05 split kernel, dense cache only, up to 128 rows
+  if (decode_on_tensor_cores(H_q, H_kv, T_q) &&
+      (paged || (long long)(H_q / H_kv) * T_q > gqa::kDecodeTcRows))
+    return GQA_ERR_UNSUPPORTED;
   if (B > 65535 || H_kv > 65535) return GQA_ERR_UNSUPPORTED;  // grid y/z limits
   if ((long long)B * H_q * T_q > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;  // output rows
   return GQA_OK;
@@ -211,7 +234,8 @@ GQA_API int gqa_attn_decode_plan(int B, int H_kv, int S_max, int num_sms, int nu
 GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_max, int d,
                                               int num_sms, int num_splits) {
   int splits = 0, chunk = 0;
-  if (H_q <= 0 || d <= 0 || plan(B, H_kv, S_max, num_sms, num_splits, &splits, &chunk) != GQA_OK)
+  if (H_q <= 0 || H_kv <= 0 || d <= 0 ||
+      plan_decode(B, H_q, H_kv, 1, S_max, num_sms, num_splits, &splits, &chunk) != GQA_OK)
     return 0;
   return decode_ws_bytes(B, H_q, splits, d);
 }
@@ -230,12 +254,15 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                  const void *workspace, size_t ws_bytes, gqa_stream_t stream,
                  const PagedLayout &paged = PagedLayout{nullptr, 0, 0, 0}, int T_q = 1) {
   int rc = check_decode_args(phase, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
-                             num_splits, o, lse, T_q);
+                             num_splits, o, lse, T_q, paged.block_table != nullptr);
   if (rc != GQA_OK || B == 0) return rc;
   DeviceState *st = nullptr;
   if ((rc = device_state(&st)) != GQA_OK) return rc;
   int splits = 0, chunk = 0;
-  if ((rc = plan(B, H_kv, S_max, st->num_sms, num_splits, &splits, &chunk)) != GQA_OK) return rc;
+  if ((rc = plan_decode(B, H_q, H_kv, T_q, S_max, st->num_sms, num_splits, &splits, &chunk)) !=
+      GQA_OK)
+    return rc;
+  const bool tensor_cores = decode_on_tensor_cores(H_q, H_kv, T_q);
   const size_t need = decode_ws_bytes(B, H_q, splits, d, T_q);
   if (!workspace || ws_bytes < need) return GQA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return GQA_ERR_INVALID_ARG;
@@ -266,11 +293,13 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   a.wait.status = st->status;
   a.wait.timeout_ns = kWaitTimeoutNs;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (phase == kPhaseBoth && gqa::decode_fused_eligible(a)) {
+  if (phase == kPhaseBoth && !tensor_cores && gqa::decode_fused_eligible(a)) {
     return gqa::decode_fused_launch(a, s, g_encode) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
   }
   if (phase & kPhaseSplit) {
-    if (gqa::decode_split_launch(a, s, g_encode) != cudaSuccess) return GQA_ERR_CUDA;
+    const cudaError_t e = tensor_cores ? gqa::decode_tc_split_launch(a, s, g_encode)
+                                       : gqa::decode_split_launch(a, s, g_encode);
+    if (e != cudaSuccess) return GQA_ERR_CUDA;
   }
   if (phase & kPhaseMerge) {
     if (gqa::decode_merge_launch(a, s) != cudaSuccess) return GQA_ERR_CUDA;
@@ -310,8 +339,8 @@ GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages
 GQA_API size_t gqa_attn_decode_multi_workspace_size(int B, int H_q, int H_kv, int T_q, int S_max,
                                                     int d, int num_sms, int num_splits) {
   int splits = 0, chunk = 0;
-  if (H_q <= 0 || d <= 0 || T_q <= 0 ||
-      plan(B, H_kv, S_max, num_sms, num_splits, &splits, &chunk) != GQA_OK)
+  if (H_q <= 0 || H_kv <= 0 || d <= 0 || T_q <= 0 ||
+      plan_decode(B, H_q, H_kv, T_q, S_max, num_sms, num_splits, &splits, &chunk) != GQA_OK)
     return 0;
   return decode_ws_bytes(B, H_q, splits, d, T_q);
 }
@@ -347,7 +376,8 @@ GQA_API int gqa_attn_decode_kernel_count(int B, int H_q, int H_kv, int S_max, in
   a.S_max = S_max;
   a.num_splits = splits;
   a.fused_clusters = st->fused_clusters;
-  *out_kernels = gqa::decode_fused_eligible(a) ? 1 : (S_max > 0 ? 2 : 1);
+  const bool single = !decode_on_tensor_cores(H_q, H_kv, 1) && gqa::decode_fused_eligible(a);
+  *out_kernels = single ? 1 : (S_max > 0 ? 2 : 1);
   return GQA_OK;
 }
 

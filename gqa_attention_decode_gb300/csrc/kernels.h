@@ -51,6 +51,16 @@ cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
 // Launches the log-sum-exp merge of the split partials.
 cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream);
 
+// Split kernel on tcgen05 tensor cores for many (head, token) rows per KV head:
+// 32 < G * T_q <= kDecodeTcRows, or G > kDecodeMaxG (dense cache, chunk a
+// multiple of 128 keys).  Writes the same partials as decode_split_launch, for
+// decode_merge_launch.
+constexpr int kDecodeTcRows = 128;
+constexpr int kDecodeTcTileKeys = 128;
+cudaError_t decode_tc_prepare_device();
+cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
+                                   PFN_cuTensorMapEncodeTiled_v12000 encode);
+
 // ---- causal prefill ----------------------------------------------------------
 struct PrefillLaunch {
   const uint16_t *q;  // [B, H_q, T_q, d]

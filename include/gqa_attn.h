@@ -127,7 +127,10 @@ GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_ma
  *             used and may hold any bits (NaN included).  Values outside
  *             [0, S_max] are clamped on the device.
  *   B, H_q, H_kv, S_max, d   sizes; d must be 128; H_q % H_kv == 0 and
- *             G = H_q / H_kv <= 8 (the G heads fill the 8-wide MMA dimension).
+ *             G = H_q / H_kv <= 128.  G <= 8: the G heads fill the 8-wide
+ *             dimension of the warp-level MMA; 8 < G <= 128: the tcgen05 split
+ *             kernel (one 128-row tensor-core tile per KV head), always split +
+ *             merge.
  *   scale     softmax scale (the record uses 1/sqrt(d)); any finite value.
  *   num_splits 0 = automatic plan, else the requested split count (see
  *             gqa_attn_decode_plan; the plan uses this device's SM count).
@@ -174,7 +177,8 @@ GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
  *                      page_size (clamped on the device).
  *   page_size          a positive multiple of 64 (else GQA_ERR_UNSUPPORTED).
  * Everything else, including the plan and the workspace size, is that of
- * gqa_attn_decode with S_max = max_pages_per_seq * page_size.
+ * gqa_attn_decode with S_max = max_pages_per_seq * page_size, except that G
+ * must be <= 8 (the tcgen05 path serves dense caches only).
  */
 GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages,
                                   const gqa_bf16_t *v_pages, const int32_t *block_table,
@@ -195,8 +199,11 @@ GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages
  *   Token t sees keys 0..seqlens[b]-T_q+t (causal among the new tokens); a
  *   token whose position is negative sees nothing (O = 0, lse = -inf).
  *   o        device [B, H_q, T_q, d] bf16; lse device [B, H_q, T_q] fp32.
- *   Supported: d = 128, G * T_q <= 32 (T_q <= 4 for G = 8), else
- *   GQA_ERR_UNSUPPORTED.  K and V are read once per KV head for all G*T_q rows.
+ *   Supported: d = 128 and G * T_q <= 128 (T_q <= 16 for G = 8), else
+ *   GQA_ERR_UNSUPPORTED.  K and V are read once per KV head for all G*T_q rows:
+ *   up to 32 rows with warp-level MMAs, 33..128 rows (or G > 8) as one 128-row
+ *   tcgen05 tile per KV head, whose split plan uses chunks of whole 128-key
+ *   tiles (gqa_attn_decode_multi_workspace_size accounts for it).
  *   workspace: gqa_attn_decode_multi_workspace_size(...) bytes
  *   (B*H_q*T_q*splits*(d+1)*4, rounded up to 256).  T_q = 1 is gqa_attn_decode.
  */

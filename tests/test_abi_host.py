@@ -111,7 +111,7 @@ def _raw_decode(lib, **kw):
     (dict(k=(1 << 20) + 2), gqa.GQA_ERR_INVALID_ARG),          # misaligned pointer
     (dict(H_q=60), gqa.GQA_ERR_INVALID_ARG),                   # H_q % H_kv != 0
     (dict(d=64), gqa.GQA_ERR_UNSUPPORTED),                     # only d = 128
-    (dict(H_q=72, H_kv=4), gqa.GQA_ERR_UNSUPPORTED),           # G = 18 > 8
+    (dict(H_q=576, H_kv=4), gqa.GQA_ERR_UNSUPPORTED),          # G = 144 > 128 rows
     (dict(num_splits=-1), gqa.GQA_ERR_INVALID_ARG),
     (dict(S_max=-5), gqa.GQA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), gqa.GQA_ERR_INVALID_ARG),
@@ -177,6 +177,7 @@ def _raw_paged(lib, **kw):
     (dict(num_pages=0), gqa.GQA_ERR_INVALID_ARG),
     (dict(max_pages=-1), gqa.GQA_ERR_INVALID_ARG),
     (dict(d=64), gqa.GQA_ERR_UNSUPPORTED),
+    (dict(H_q=128, H_kv=8), gqa.GQA_ERR_UNSUPPORTED),          # G = 16: dense cache only
     (dict(B=0), gqa.GQA_OK),
 ])
 def test_paged_rejects_before_any_cuda_call(lib, kw, expect):
@@ -189,10 +190,14 @@ def test_multi_token_rejections(lib):
     call = lambda B, H_q, H_kv, T_q, d=128: lib.gqa_attn_decode_multi(
         v(p), v(p), v(p), v(p), B, H_q, H_kv, T_q, 1024, d, 0.088, 0, v(p), v(p), v(p), 1 << 30,
         v(0))
-    assert call(1, 64, 8, 5) == gqa.GQA_ERR_UNSUPPORTED      # G * T_q = 40 > 32
+    assert call(1, 64, 8, 17) == gqa.GQA_ERR_UNSUPPORTED     # G * T_q = 136 > 128
     assert call(1, 64, 8, 0) == gqa.GQA_ERR_INVALID_ARG
     assert call(1, 64, 8, 2, d=64) == gqa.GQA_ERR_UNSUPPORTED
     assert call(65535, 65536, 8192, 1) == gqa.GQA_ERR_UNSUPPORTED  # > 2^31 output rows
     assert call(0, 64, 8, 2) == gqa.GQA_OK
     assert gqa.gqa_attn_decode_multi_workspace_size(1, 64, 8, 4, 32768, 128, 152) == \
         4 * gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 152)
+    # more than 32 rows per KV head: tensor-core split kernel, chunks of whole
+    # 128-key tiles (1728 keys -> 1792, still 19 splits for 32K keys)
+    assert gqa.gqa_attn_decode_multi_workspace_size(1, 64, 8, 16, 32768, 128, 152) == \
+        (64 * 16 * 19 * 129 * 4 + 255) // 256 * 256

@@ -80,7 +80,56 @@ def test_nan_padding_multi():
 
 
 def test_too_many_rows_is_unsupported():
-    q, k, v, sl = inputs(1, 64, 8, 5, 256, None, 55)          # G * T_q = 40 > 32
+    q, k, v, sl = inputs(1, 64, 8, 17, 256, None, 55)         # G * T_q = 136 > 128
     with pytest.raises(gqa.GQAError) as e:
         gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 0.1)
     assert e.value.status == gqa.GQA_ERR_UNSUPPORTED
+
+
+# ---- more than 32 rows per KV head: the tcgen05 split kernel (128-row tiles) ----
+
+@pytest.mark.parametrize("H_q,H_kv,T_q", [(64, 8, 5), (64, 8, 8), (64, 8, 16), (32, 2, 8),
+                                          (96, 8, 10), (48, 1, 2)])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_multi_token_decode_tensor_cores(H_q, H_kv, T_q, num_splits):
+    # short sequences (fewer keys than tokens), a tile-exact one, and ragged tails
+    seqlens = [2000, 1, 700, 3, 256, 129]
+    q, k, v, sl = inputs(6, H_q, H_kv, T_q, 2000, seqlens, 56)
+    o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 1 / math.sqrt(128), num_splits)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(),
+                                         1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, f"tc T_q={T_q} G={H_q // H_kv} splits={num_splits}")
+
+
+def test_group_of_16_decode_uses_tensor_cores():
+    """gqa_attn_decode with G = 16 (> 8): the tensor-core split kernel."""
+    B, H_q, H_kv, S = 3, 64, 4, 1500
+    q, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S, 128, seed=57, device=DEV,
+                                          seqlens=[1500, 77, 640])
+    o, lse = gqa.gqa_attn_decode(q, k, v, sl.to(DEV), 0.088)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode(np64(q), np64(k), np64(v), sl.numpy(), 0.088)
+    compare(o, lse, o_ref, lse_ref, "decode G=16")
+    assert gqa.gqa_attn_decode_kernel_count(B, H_q, H_kv, S, 128, 0) == 2
+
+
+def test_llama70b_layer_sixteen_tokens():
+    w = gqa_synth.WORKLOADS["llama70b_decode_32k"]
+    q, k, v, sl = inputs(1, 64, 8, 16, w.S_max, None, 58)
+    o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), w.scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), w.scale)
+    compare(o, lse, o_ref, lse_ref, "llama70b T_q=16")
+
+
+def test_nan_padding_tensor_cores():
+    """Cache rows past each sequence hold NaN; the V rows of the last tile past
+    the sequence are cleared before P V, so nothing changes."""
+    q, k, v, sl = inputs(2, 64, 8, 8, 640, [577, 100], 59)
+    o_ref, l_ref = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 0.1)
+    gqa_synth.fill_padding(k, sl, float("nan"))
+    gqa_synth.fill_padding(v, sl, float("nan"))
+    o, l = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
