@@ -67,7 +67,7 @@ struct Params {
   uint16_t *o;  // fused variant: final outputs
   float *lse;
   const int32_t *block_table;  // paged variant: [B, max_pages]
-  int page_size, max_pages;
+  int page_size, max_pages, num_pages;
   int B, H_q, H_kv, G, S_max, num_splits, chunk;
   int T_q, n_cols, cgroups;  // new tokens per sequence, G * T_q, column groups of 4 warps
   float scale_log2;  // scale * log2(e)
@@ -134,7 +134,11 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   // with coherent loads (ld.global.ca), never the non-coherent read-only path.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int seqlen = min(max(__ldca(p.seqlens + b), 0), p.S_max);
+  const int seqlen_in = __ldca(p.seqlens + b);
+  // out-of-range lengths are clamped and reported through the status word
+  if ((seqlen_in < 0 || seqlen_in > p.S_max) && threadIdx.x == 0 && split == 0)
+    atomicExch(p.wait.status, kStatusInvalidArg);
+  const int seqlen = min(max(seqlen_in, 0), p.S_max);
   const int key_begin = split * p.chunk;
   const int key_end = min(key_begin + p.chunk, seqlen);
   if (!kFused && key_begin >= key_end) return;  // empty split: the merge never reads it
@@ -166,6 +170,9 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
           page_reg = idx < p.max_pages ? __ldca(p.block_table + (size_t)b * p.max_pages + idx) : 0;
         }
         const int page_id = __shfl_sync(0xffffffffu, page_reg, page - page_base);
+        // a page id outside the pool reads zeros (TMA out-of-bounds fill); report it
+        if ((page_id < 0 || page_id >= p.num_pages) && lane == 0)
+          atomicExch(p.wait.status, kStatusInvalidArg);
         c2 = key0 - page * p.page_size;
         c3 = page_id * p.H_kv + kv;
       }
@@ -673,6 +680,7 @@ static decode::Params make_params(const DecodeLaunch &a) {
   p.block_table = a.block_table;
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   p.wait = a.wait;
   return p;
 }

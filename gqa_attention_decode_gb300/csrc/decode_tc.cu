@@ -119,7 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // inputs written by earlier grids are visible after this wait (coherent loads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int seqlen = min(max(__ldca(p.seqlens + b), 0), p.S_max);
+  const int seqlen_in = __ldca(p.seqlens + b);
+  // out-of-range lengths are clamped and reported through the status word
+  if ((seqlen_in < 0 || seqlen_in > p.S_max) && threadIdx.x == 0 && split == 0)
+    atomicExch(p.wait.status, kStatusInvalidArg);
+  const int seqlen = min(max(seqlen_in, 0), p.S_max);
   const int key_begin = split * p.chunk;
   const int key_end = min(key_begin + p.chunk, seqlen);
   if (key_begin >= key_end) return;  // empty split: the merge never reads it

@@ -10,6 +10,7 @@
 namespace gqa {
 
 // Status word values (mirrors gqa_status_t).
+constexpr int kStatusInvalidArg = 1;  // a device-side input out of range (clamped)
 constexpr int kStatusTimeout = 5;
 
 // Bounded-wait control passed to every kernel: where to record a timeout and

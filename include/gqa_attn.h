@@ -125,7 +125,8 @@ GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_ma
  *   seqlens   device [B] int32, 0 <= seqlens[b] <= S_max: sequence b sees keys
  *             0..seqlens[b]-1.  Cache rows at or past seqlens[b] are never
  *             used and may hold any bits (NaN included).  Values outside
- *             [0, S_max] are clamped on the device.
+ *             [0, S_max] are clamped on the device and reported as
+ *             GQA_ERR_INVALID_ARG by gqa_attn_device_status.
  *   B, H_q, H_kv, S_max, d   sizes; d must be 128; H_q % H_kv == 0 and
  *             G = H_q / H_kv <= 128.  G <= 8: the G heads fill the 8-wide
  *             dimension of the warp-level MMA; 8 < G <= 128: the tcgen05 split
@@ -172,7 +173,9 @@ GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
  *                      [i*page_size, (i+1)*page_size) of sequence b are in page
  *                      block_table[b*max_pages_per_seq + i]; entries past the
  *                      sequence's last key are never read.  An entry outside
- *                      [0, num_pages) reads zeros (wrong result, no fault).
+ *                      [0, num_pages) reads zeros (wrong result, no fault)
+ *                      and is reported as GQA_ERR_INVALID_ARG by
+ *                      gqa_attn_device_status.
  *   seqlens            device [B] int32, 0 <= seqlens[b] <= max_pages_per_seq *
  *                      page_size (clamped on the device).
  *   page_size          a positive multiple of 64 (else GQA_ERR_UNSUPPORTED).
@@ -347,8 +350,11 @@ GQA_API int gqa_attn_prefill_causal_from_host(const gqa_bf16_t *q_host, const gq
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
- * word that bounded waits set when they run out.  *out_status receives GQA_OK
- * or GQA_ERR_TIMEOUT.  Returns GQA_ERR_CUDA if a CUDA call fails.
+ * word.  Kernels set it when a bounded wait runs out (GQA_ERR_TIMEOUT) or when a
+ * decode finds a device-side input out of range (GQA_ERR_INVALID_ARG): a seqlens
+ * entry outside [0, S_max] (used clamped) or a block-table entry outside
+ * [0, num_pages) (its keys read as zeros).  *out_status receives GQA_OK or that
+ * code.  Returns GQA_ERR_CUDA if a CUDA call fails.
  */
 GQA_API int gqa_attn_device_status(gqa_stream_t stream, int *out_status);
 

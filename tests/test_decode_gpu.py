@@ -197,3 +197,17 @@ def test_bounded_wait_reports_timeout_without_hanging():
     assert gqa.gqa_attn_device_status() == gqa.GQA_OK   # cleared by the read
     # the context is still usable afterwards
     test_tiny_decode_workload()
+
+
+def test_out_of_range_seqlens_are_clamped_and_reported():
+    """seqlens outside [0, S_max]: used clamped (0 -> no key, S_max -> all
+    keys) and reported as GQA_ERR_INVALID_ARG through the device status."""
+    B, H_q, H_kv, S = 2, 16, 2, 500
+    q, k, v, _ = gqa_synth.decode_inputs(B, H_q, H_kv, S, 128, seed=22, device=DEV)
+    bad = torch.tensor([-7, S + 100], dtype=torch.int32)
+    assert gqa.gqa_attn_device_status() == gqa.GQA_OK
+    o, lse = run_decode(q, k, v, bad, 0.088)
+    assert gqa.gqa_attn_device_status() == gqa.GQA_ERR_INVALID_ARG
+    o_ref, lse_ref = oracle.decode(np64(q), np64(k), np64(v), np.array([0, S]), 0.088)
+    compare(o, lse, o_ref, lse_ref, "clamped seqlens")
+    assert gqa.gqa_attn_device_status() == gqa.GQA_OK      # cleared by the read

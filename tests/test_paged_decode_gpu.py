@@ -109,3 +109,21 @@ def test_paged_rejects_bad_page_size():
     with pytest.raises(gqa.GQAError) as e:
         gqa.gqa_attn_decode_paged(q, kp, kp, table, sl.to(DEV), 0.1)
     assert e.value.status == gqa.GQA_ERR_UNSUPPORTED
+
+
+def test_page_id_outside_pool_is_reported():
+    """A block-table entry past the pool reads zeros and is reported as
+    GQA_ERR_INVALID_ARG through the device status; the other sequence is exact."""
+    B, H_q, H_kv, S, ps = 2, 16, 2, 512, 128
+    q, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S, 128, seed=44, device=DEV)
+    kp, vp, table = to_pages(k, v, ps, extra_pages=0, seed=3)
+    table[0, 1] = kp.shape[0] + 3                     # sequence 0, keys 128..255
+    assert gqa.gqa_attn_device_status() == gqa.GQA_OK
+    o, l = gqa.gqa_attn_decode_paged(q, kp, vp, table, sl.to(DEV), 0.1)
+    torch.cuda.synchronize()
+    assert gqa.gqa_attn_device_status() == gqa.GQA_ERR_INVALID_ARG
+    tcpu = table.cpu()
+    k1 = torch.stack([torch.cat([kp[int(p)] for p in tcpu[1]], dim=1)])
+    v1 = torch.stack([torch.cat([vp[int(p)] for p in tcpu[1]], dim=1)])
+    o_ref, lse_ref = oracle.decode(np64(q[1:]), np64(k1), np64(v1), sl.numpy()[1:], 0.1)
+    compare(o[1:], l[1:], o_ref, lse_ref, "sequence with valid pages")
