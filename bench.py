@@ -72,6 +72,9 @@ def parse_args():
                     help="decode calls per step, each on its own K/V copy")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="one JSON line per workload (the five configurations, multi-token "
+                         "and paged decode) instead of the step line")
     return ap.parse_args()
 
 
@@ -567,6 +570,105 @@ def _max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def run_all_configs(device):
+    """Times every workload on its own (CUDA graphs of calls, CUDA events) and
+    prints one JSON line each with its roofline fraction."""
+    import torch
+    import gqa_synth
+    import gqa_attention_decode_gb300 as gqa
+    from gqa_attention_decode_gb300 import build as gbuild
+    gbuild.build()
+    gqa.load_library()
+    peaks, peak_src = load_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
+
+    def time_graph(fn, calls, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(device)
+        if gqa.gqa_attn_device_status() != 0:
+            raise RuntimeError("device status not OK")
+        return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
+    def emit(d):
+        d["peak_source"] = peak_src
+        print(json.dumps(d), flush=True)
+
+    def decode_line(name, T_q=1, page_size=0):
+        w = gqa_synth.WORKLOADS[name]
+        q, k, v, sl = gqa_synth.workload_decode_inputs(w, device)
+        if T_q > 1:
+            q = gqa_synth.bf16_normal((w.B, w.H_q, T_q, w.d), w.seed, device)
+        nbytes = decode_bytes(w, sl.tolist())
+        kv_bytes = 2 * k.numel() * k.element_size()
+        # enough distinct K/V copies that consecutive calls never find theirs in L2
+        copies = 1 if kv_bytes > 2 * l2_bytes else min(16, -(-(1 << 30) // kv_bytes))
+        kvs = [(k, v)] + [(k.clone(), v.clone()) for _ in range(copies - 1)]
+        sld = sl.to(device)
+        ns = w.num_splits or 0
+        if page_size:
+            mp = w.S_max // page_size
+            pages = []
+            for kc, vc in kvs:
+                kp = kc.view(w.B, w.H_kv, mp, page_size, w.d).permute(0, 2, 1, 3, 4).reshape(
+                    w.B * mp, w.H_kv, page_size, w.d).contiguous()
+                vp = vc.view(w.B, w.H_kv, mp, page_size, w.d).permute(0, 2, 1, 3, 4).reshape(
+                    w.B * mp, w.H_kv, page_size, w.d).contiguous()
+                pages.append((kp, vp))
+            table = torch.arange(w.B * mp, dtype=torch.int32, device=device).view(w.B, mp)
+            fn = lambda: [gqa.gqa_attn_decode_paged(q, kp, vp, table, sld, w.scale, ns)
+                          for kp, vp in pages]
+        elif T_q > 1:
+            fn = lambda: [gqa.gqa_attn_decode_multi(q, kc, vc, sld, w.scale, ns) for kc, vc in kvs]
+        else:
+            fn = lambda: [gqa.gqa_attn_decode(q, kc, vc, sld, w.scale, ns) for kc, vc in kvs]
+        us = time_graph(fn, len(kvs), 20)
+        gbs = nbytes / us / 1e3
+        label = name + (f" T_q={T_q}" if T_q > 1 else "") + (f" paged({page_size})" if page_size else "")
+        emit({"workload": label, "us_per_call": us, "value": gbs, "unit": "GB/s",
+              "bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+              "bytes_per_call": nbytes, "kv_copies": len(kvs),
+              "l2": ("K/V larger than L2" if kv_bytes > 2 * l2_bytes else
+                     f"{len(kvs)} K/V copies rotate ({len(kvs) * kv_bytes >> 20} MiB)"
+                     if len(kvs) * kv_bytes > 2 * l2_bytes else
+                     "L2 resident (latency-bound)")})
+
+    def prefill_line(name):
+        w = gqa_synth.WORKLOADS[name]
+        q, k, v = gqa_synth.workload_prefill_inputs(w, device)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H_q, w.T_q), dtype=torch.float32, device=device)
+        fn = lambda: gqa.gqa_attn_prefill_causal(q, k, v, w.scale, w.q_offset, o, lse)
+        us = time_graph(fn, 1, 10)
+        tf = prefill_flops(w) / us / 1e6
+        emit({"workload": name, "us_per_call": us, "value": tf, "unit": "TFLOP/s",
+              "bound": "tensor", "kernel": prefill_kernel_name(w.G),
+              "peak": peaks["bf16_tflops"], "frac": tf / peaks["bf16_tflops"],
+              "frac_of_sustained": tf / peaks["bf16_tflops_sustained"],
+              "flops_per_call": prefill_flops(w)})
+
+    decode_line("tiny_decode")
+    decode_line("llama70b_decode_32k")
+    decode_line("ragged_decode_b16")
+    prefill_line("causal_prefill_8k")
+    prefill_line("chunked_prefill_32k")
+    decode_line("llama70b_decode_32k", T_q=4)
+    decode_line("llama70b_decode_32k", T_q=16)
+    decode_line("llama70b_decode_32k", page_size=256)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -582,6 +684,10 @@ def main():
         raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
+    if args.all_configs:
+        if rank == 0:
+            run_all_configs(device)
+        return
     if world > 1:
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         torch.distributed.init_process_group("nccl", device_id=device)
