@@ -59,11 +59,7 @@ constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base slot, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + 1024 alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units (a factor of 256)
-// 1: the two softmax warpgroups alternate their exp phases (a token passed
-// through shared-memory barriers); 0: they run them whenever their S is ready.
-#ifndef GQA_PREFILL_EXP_TURN
-#define GQA_PREFILL_EXP_TURN 1
-#endif
+constexpr float kSumTrigger = 256.0f;      // 2^kRescaleThreshold
 
 struct Params {
   uint16_t *o;
@@ -317,48 +313,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ready = wait_abortable(s_full(i), tile & 1, p.wait, abort_flag);
         if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
         tc::fence_after_sync();
+        const bool masked = (j * kBN + kBN - 1 > q0) || (j * kBN + kBN > p.S_kv);
+        const int lim = min(qpos + 1, p.S_kv) - j * kBN;  // keys [0, lim) of the tile visible
+        // scores of chunk c (32 keys) as held: times sl2 unless that is still owed,
+        // keys the row may not see set to -inf
+        auto prep = [&](uint32_t *v, int c) {
+          if (!pos_scale) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * p.sl2);
+          }
+          if (masked) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e >= lim) v[e] = __float_as_uint(-INFINITY);
+          }
+        };
+        // row max over the 128 scores, re-read from tensor memory, in the units of m_ref
+        auto row_max = [&]() {
+          uint32_t va[32], vb[32];
+          float mx = -INFINITY;
+          tc::ld32(t_s, va);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t *v = (c & 1) ? vb : va;
+            tc::wait_ld32(v);
+            prep(v, c);
+            if (c + 1 < 4) tc::ld32(t_s + 32 * (c + 1), (c & 1) ? va : vb);
+            float m2[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+#pragma unroll
+              for (int k2 = 0; k2 < 2; ++k2)
+                m2[k2] = fmax3(m2[k2], __uint_as_float(v[e + 2 * k2]), __uint_as_float(v[e + 2 * k2 + 1]));
+            mx = fmax3(mx, m2[0], m2[1]);
+          }
+          return pos_scale ? mx * p.sl2 : mx;
+        };
+        // P = exp2(s * mul - m_ref) as bf16 pairs for the 32 scores of chunk c, with
+        // their sum; argument and sums in packed fp32x2 instructions (two keys each)
+        uint32_t pk[kBN / 2];
+        auto exp_chunk = [&](const uint32_t *v, int c) {
+          const float negm = -m_ref;
+          const uint64_t mul2 = f32x2(mul, mul), negm2 = f32x2(negm, negm);
+          uint64_t rs2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                  mul2, negm2),
+                        x0, x1);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            rs2[e & 1] = add_f32x2(rs2[e & 1], f32x2(p0, p1));
+            pk[16 * c + e] = pack_bf16x2(p0, p1);
+          }
+          float a, b, c2, d;
+          f32x2_split(rs2[0], a, b);
+          f32x2_split(rs2[1], c2, d);
+          return (a + b) + (c2 + d);
+        };
+        // the same over the whole row, streamed from tensor memory chunk by chunk
+        auto exp_streamed = [&]() {
+          uint32_t va[32], vb[32];
+          float sum = 0.f;
+          tc::ld32(t_s, va);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t *v = (c & 1) ? vb : va;
+            tc::wait_ld32(v);
+            prep(v, c);
+            if (c + 1 < 4) tc::ld32(t_s + 32 * (c + 1), (c & 1) ? va : vb);
+            sum += exp_chunk(v, c);
+          }
+          return sum;
+        };
+        // common path: the whole row in registers (one load wait), before the exp turn
         uint32_t sv[kBN];
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) tc::ld32(t_s + 32 * c, sv + 32 * c);
+        for (int c = 0; c < 4; ++c) tc::ld32(t_s + 32 * c, sv + 32 * c);
         tc::wait_ld();
-        if (!pos_scale) {
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * p.sl2);
+        for (int c = 0; c < 4; ++c) prep(sv + 32 * c, c);
+        if (j == 0) {  // key 0 is visible to every row: finite
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int e = 0; e < kBN; e += 8)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              mx4[k4] = fmax3(mx4[k4], __uint_as_float(sv[e + 2 * k4]),
+                              __uint_as_float(sv[e + 2 * k4 + 1]));
+          const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+          m_ref = pos_scale ? mx * p.sl2 : mx;
         }
-        const bool masked = (j * kBN + kBN - 1 > q0) || (j * kBN + kBN > p.S_kv);
-        if (masked) {
-          const int lim = min(qpos + 1, p.S_kv) - j * kBN;  // keys [0, lim) of the tile visible
-#pragma unroll
-          for (int e = 0; e < kBN; ++e)
-            if (e >= lim) sv[e] = __float_as_uint(-INFINITY);
-        }
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int e = 0; e < kBN; e += 4)
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) mx4[k4] = fmaxf(mx4[k4], __uint_as_float(sv[e + k4]));
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float mt = pos_scale ? mx * p.sl2 : mx;
-        if (j == 0) {
-          m_ref = mt;  // key 0 is visible to every row: finite
-        } else if (__any_sync(0xffffffffu, mt > m_ref + kRescaleThreshold)) {
-          const float m_new = fmaxf(m_ref, mt);
-          const float corr = fast_exp2(m_ref - m_new);
-          l *= corr;
-          // O_i holds P V up to tile j-1 (complete: S_i(j) was issued after it)
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tc::ld32(t_o + 32 * c, r);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
-            tc::st32(t_o + 32 * c, r);
-          }
-          tc::wait_st();
-          m_ref = m_new;
-        }
-#if GQA_PREFILL_EXP_TURN
         // exp turn: head 0's tile k follows head 1's tile k-1, head 1's tile k follows
         // head 0's tile k, so only one warpgroup feeds the exp unit at a time
         if (i == 0) {
@@ -367,28 +412,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           ready = wait_abortable(tok(1), tile & 1, p.wait, abort_flag);
         }
         if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
-#endif
-        // P = exp2(s * scale log2e - m_ref) -> bf16 pairs over columns 0..63 of S_i
-        const float negm = -m_ref;
-        float rs0 = 0.f, rs1 = 0.f;
-        uint32_t pk[kBN / 2];
+        float tsum = 0.f;
 #pragma unroll
-        for (int e = 0; e < kBN / 2; ++e) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * e]), mul, negm));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), mul, negm));
-          rs0 += p0;
-          rs1 += p1;
-          pk[e] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 4; ++c) tsum += exp_chunk(sv + 32 * c, c);
+        // The reference max only moves when a score exceeds it by more than the
+        // threshold; such a score alone makes the tile's sum exceed 2^threshold,
+        // so the row max is computed only when a sum does (or is not finite).
+        if (j > 0 && __any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
+          const float mt = row_max();  // S is still in tensor memory (P not yet written)
+          if (__any_sync(0xffffffffu, mt > m_ref + kRescaleThreshold)) {
+            const float m_new = fmaxf(m_ref, mt);
+            const float corr = fast_exp2(m_ref - m_new);
+            l *= corr;
+            // O_i holds P V up to tile j-1 (complete: S_i(j) was issued after it)
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r[32];
+              tc::ld32(t_o + 32 * c, r);
+              tc::wait_ld32(r);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+              tc::st32(t_o + 32 * c, r);
+            }
+            tc::wait_st();
+            m_ref = m_new;
+            tsum = exp_streamed();
+          }
         }
+        mbar_arrive(tok(1 - i));  // the exp unit is free: the other warpgroup may start
         tc::st32(t_s, pk);
         tc::st32(t_s + 32, pk + 32);
         tc::wait_st();
-        l += rs0 + rs1;
+        l += tsum;
         tc::fence_before_sync();
         mbar_arrive(p_full(i));
-#if GQA_PREFILL_EXP_TURN
-        mbar_arrive(tok(1 - i));
-#endif
       }
       if (!ok) break;
       // epilogue: O / l -> bf16, lse = m_ref ln2 + ln l
