@@ -336,6 +336,10 @@ def run_ours(args, rank, world, device):
         pq, pk, pv = gqa_synth.workload_prefill_inputs(wp, device)
         po = torch.empty_like(pq)
         plse = torch.empty((wp.B, wp.H_q, wp.T_q), dtype=torch.float32, device=device)
+        pws = torch.empty(gqa.gqa_attn_prefill_causal_workspace_size(
+            wp.B, wp.H_q, wp.H_kv, wp.T_q, wp.S_kv, wp.d, wp.q_offset,
+            torch.cuda.get_device_properties(device).multi_processor_count),
+            dtype=torch.uint8, device=device)
     flops_prefill = prefill_flops(wp)
 
     # kernels one gqa_attn_decode call launches: 1 (cluster-merged single kernel)
@@ -346,7 +350,8 @@ def run_ours(args, rank, world, device):
     if "decode" in parts:
         launches_per_step += layers * call_kernels + (layers if call_kernels == 2 else 0)
     if "prefill" in parts:
-        launches_per_step += 1
+        launches_per_step += gqa.gqa_attn_prefill_causal_kernel_count(
+            wp.B, wp.H_q, wp.H_kv, wp.T_q, wp.S_kv, wp.d, wp.q_offset, pws.numel(), device)
 
     # The calls of a step are captured once into CUDA graphs; the timed loop
     # replays the graphs with timing events between them, so host overhead
@@ -360,7 +365,7 @@ def run_ours(args, rank, world, device):
             gqa.gqa_attn_decode_split(q, kc, vc, seqlens, wd.scale, wd.num_splits, ws)
 
     def call_prefill():
-        gqa.gqa_attn_prefill_causal(pq, pk, pv, wp.scale, wp.q_offset, po, plse)
+        gqa.gqa_attn_prefill_causal(pq, pk, pv, wp.scale, wp.q_offset, po, plse, pws)
 
     calls = {}
     if "decode" in parts:
@@ -650,11 +655,16 @@ def run_all_configs(device):
         q, k, v = gqa_synth.workload_prefill_inputs(w, device)
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.H_q, w.T_q), dtype=torch.float32, device=device)
-        fn = lambda: gqa.gqa_attn_prefill_causal(q, k, v, w.scale, w.q_offset, o, lse)
+        nb = gqa.gqa_attn_prefill_causal_workspace_size(w.B, w.H_q, w.H_kv, w.T_q, w.S_kv, w.d,
+                                                        w.q_offset, sms)
+        ws = torch.empty(nb, dtype=torch.uint8, device=device)
+        kernels = gqa.gqa_attn_prefill_causal_kernel_count(w.B, w.H_q, w.H_kv, w.T_q, w.S_kv,
+                                                           w.d, w.q_offset, nb, device)
+        fn = lambda: gqa.gqa_attn_prefill_causal(q, k, v, w.scale, w.q_offset, o, lse, ws)
         us = time_graph(fn, 1, 10)
         tf = prefill_flops(w) / us / 1e6
         emit({"workload": name, "us_per_call": us, "value": tf, "unit": "TFLOP/s",
-              "bound": "tensor", "kernel": prefill_kernel_name(w.G),
+              "bound": "tensor", "kernel": prefill_kernel_name(w.G), "kernels_per_call": kernels,
               "peak": peaks["bf16_tflops"], "frac": tf / peaks["bf16_tflops"],
               "frac_of_sustained": tf / peaks["bf16_tflops_sustained"],
               "flops_per_call": prefill_flops(w)})

@@ -49,6 +49,12 @@ _SIGNATURES = {
                                          _c_int, _c_float, _c_int, _vp, _vp, _vp]),
     "gqa_attn_prefill_causal": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                          _c_int, _c_int, _c_float, _vp, _vp, _vp]),
+    "gqa_attn_prefill_causal_workspace_size": (_c_size, [_c_int] * 8),
+    "gqa_attn_prefill_causal_ws": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                            _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp,
+                                            _c_size, _vp]),
+    "gqa_attn_prefill_causal_kernel_count": (_c_int, [_c_int] * 7 + [_c_size, _ip]),
+    "gqa_attn_prefill_causal_plan": (_c_int, [_c_int] * 8 + [_c_size, _ip, _ip, _ip]),
     "gqa_attn_decode_from_host_arena_size": (_c_size, [_c_int] * 7),
     "gqa_attn_decode_from_host": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                            _c_int, _c_float, _c_int, _vp, _vp, _vp, _c_size,
@@ -339,9 +345,41 @@ def gqa_attn_decode_noalloc(q, k_cache, v_cache, seqlens, scale, num_splits=0, o
 # causal prefill
 # ---------------------------------------------------------------------------
 
-def gqa_attn_prefill_causal(q, k, v, scale, q_offset=0, o=None, lse=None, stream=None):
+def gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, d, q_offset, num_sms) -> int:
+    return int(load_library().gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, d,
+                                                                      q_offset, num_sms))
+
+
+def gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, d, q_offset, num_pairs, ws_bytes):
+    """Host-only work plan of the CTA-pair prefill: (units, split units, pieces per unit)."""
+    u, su, ps = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = load_library().gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, d, q_offset,
+                                                     num_pairs, ws_bytes, ctypes.byref(u),
+                                                     ctypes.byref(su), ctypes.byref(ps))
+    _check(rc, "gqa_attn_prefill_causal_plan")
+    return u.value, su.value, ps.value
+
+
+def gqa_attn_prefill_causal_kernel_count(B, H_q, H_kv, T_q, S_kv, d, q_offset, ws_bytes,
+                                         device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    out = ctypes.c_int(0)
+    with torch.cuda.device(dev):
+        rc = load_library().gqa_attn_prefill_causal_kernel_count(B, H_q, H_kv, T_q, S_kv, d,
+                                                                 q_offset, ws_bytes,
+                                                                 ctypes.byref(out))
+    _check(rc, "gqa_attn_prefill_causal_kernel_count")
+    return out.value
+
+
+def gqa_attn_prefill_causal(q, k, v, scale, q_offset=0, o=None, lse=None, workspace=None,
+                            stream=None):
     """Causal GQA prefill.  q [B,H_q,T_q,d]; k, v [B,H_kv,S_kv,d] (bf16).
-    Row i of q is at absolute position q_offset + i.  Returns (o, lse)."""
+    Row i of q is at absolute position q_offset + i.  Returns (o, lse).
+
+    workspace: CUDA uint8 scratch for key-range splitting of a partial last
+    round of work; None allocates gqa_attn_prefill_causal_workspace_size bytes,
+    an empty tensor runs without splitting."""
     lib = load_library()
     _need(q, "q", torch.bfloat16, 4)
     dev = q.device
@@ -357,11 +395,18 @@ def gqa_attn_prefill_causal(q, k, v, scale, q_offset=0, o=None, lse=None, stream
         lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=dev)
     _need(o, "o", torch.bfloat16, 4, dev)
     _need(lse, "lse", torch.float32, 3, dev)
+    if workspace is None:
+        nbytes = gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, d,
+                                                        int(q_offset), _num_sms(dev))
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, 1, dev)
+    ws_ptr = _ptr(workspace) if workspace.numel() > 0 else None
     with torch.cuda.device(dev):
-        rc = lib.gqa_attn_prefill_causal(_ptr(q), _ptr(k), _ptr(v), B, H_q, H_kv, T_q, S_kv, d,
-                                         int(q_offset), float(scale), _ptr(o), _ptr(lse),
-                                         _stream_handle(stream, dev))
-    _check(rc, "gqa_attn_prefill_causal")
+        rc = lib.gqa_attn_prefill_causal_ws(_ptr(q), _ptr(k), _ptr(v), B, H_q, H_kv, T_q, S_kv,
+                                            d, int(q_offset), float(scale), _ptr(o), _ptr(lse),
+                                            ws_ptr, workspace.numel(),
+                                            _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_prefill_causal_ws")
     return o, lse
 
 

@@ -397,15 +397,13 @@ GQA_API int gqa_attn_decode_merge(const int32_t *seqlens, int B, int H_q, int H_
                       1.0f, num_splits, o, lse, workspace, ws_bytes, stream);
 }
 
-GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
-                                    const gqa_bf16_t *v, int B, int H_q, int H_kv, int T_q,
-                                    int S_kv, int d, int q_offset, float scale, gqa_bf16_t *o,
-                                    float *lse, gqa_stream_t stream) {
-  int rc = check_prefill_args(q, k, v, B, H_q, H_kv, T_q, S_kv, d, q_offset, scale, o, lse);
-  if (rc != GQA_OK || B == 0 || T_q == 0) return rc;
-  DeviceState *st = nullptr;
-  if ((rc = device_state(&st)) != GQA_OK) return rc;
-  gqa::PrefillLaunch a;
+namespace {
+gqa::PrefillLaunch prefill_launch_args(const gqa_bf16_t *q, const gqa_bf16_t *k,
+                                       const gqa_bf16_t *v, int B, int H_q, int H_kv, int T_q,
+                                       int S_kv, int q_offset, float scale, gqa_bf16_t *o,
+                                       float *lse, void *workspace, size_t ws_bytes,
+                                       const DeviceState *st) {
+  gqa::PrefillLaunch a = {};
   a.q = q;
   a.k = k;
   a.v = v;
@@ -420,14 +418,104 @@ GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
   a.lse = lse;
   a.num_sms = st->num_sms;
   a.max_pairs = st->prefill_pairs;
+  a.ws = workspace;
+  a.ws_bytes = workspace ? ws_bytes : 0;
   a.wait.status = st->status;
   a.wait.timeout_ns = kWaitTimeoutNs;
+  return a;
+}
+}  // namespace
+
+GQA_API size_t gqa_attn_prefill_causal_workspace_size(int B, int H_q, int H_kv, int T_q,
+                                                      int S_kv, int d, int q_offset,
+                                                      int num_sms) {
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0 ||
+      num_sms <= 0 || H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
+    return 0;
+  if ((H_q / H_kv) % 4 != 0) return 0;  // one CTA per unit: never split
+  const long long units = (long long)((T_q + 127) / 128) * B * H_kv * (H_q / H_kv / 4);
+  const size_t bytes = gqa::prefill_pair_workspace_bound(units, num_sms);
+  return (bytes + 255) / 256 * 256;
+}
+
+GQA_API int gqa_attn_prefill_causal_plan(int B, int H_q, int H_kv, int T_q, int S_kv, int d,
+                                         int q_offset, int num_pairs, size_t ws_bytes,
+                                         int *out_units, int *out_split_units,
+                                         int *out_pieces_per_unit) {
+  if (!out_units || !out_split_units || !out_pieces_per_unit) return GQA_ERR_INVALID_ARG;
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0 ||
+      num_pairs <= 0 || H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
+    return GQA_ERR_INVALID_ARG;
+  *out_units = *out_split_units = 0;
+  *out_pieces_per_unit = 1;
+  if ((H_q / H_kv) % 4 != 0 || B == 0 || T_q == 0) return GQA_OK;
+  gqa::PrefillLaunch a = {};
+  a.B = B;
+  a.H_q = H_q;
+  a.H_kv = H_kv;
+  a.T_q = T_q;
+  a.S_kv = S_kv;
+  a.q_offset = q_offset;
+  a.max_pairs = num_pairs;
+  a.ws = ws_bytes > 0 ? reinterpret_cast<void *>(uintptr_t(256)) : nullptr;  // size decides
+  a.ws_bytes = ws_bytes;
+  const gqa::PrefillPairPlan pl = gqa::prefill_pair_plan(a);
+  *out_units = pl.units;
+  *out_split_units = pl.units - pl.n_full;
+  *out_pieces_per_unit = pl.split_s;
+  return GQA_OK;
+}
+
+GQA_API int gqa_attn_prefill_causal_ws(const gqa_bf16_t *q, const gqa_bf16_t *k,
+                                       const gqa_bf16_t *v, int B, int H_q, int H_kv, int T_q,
+                                       int S_kv, int d, int q_offset, float scale, gqa_bf16_t *o,
+                                       float *lse, void *workspace, size_t ws_bytes,
+                                       gqa_stream_t stream) {
+  int rc = check_prefill_args(q, k, v, B, H_q, H_kv, T_q, S_kv, d, q_offset, scale, o, lse);
+  if (rc != GQA_OK || B == 0 || T_q == 0) return rc;
+  if ((ws_bytes > 0 && !workspace) || (workspace && !aligned16(workspace)))
+    return GQA_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  if ((rc = device_state(&st)) != GQA_OK) return rc;
+  const gqa::PrefillLaunch a = prefill_launch_args(q, k, v, B, H_q, H_kv, T_q, S_kv, q_offset,
+                                                   scale, o, lse, workspace, ws_bytes, st);
   // group sizes that are multiples of 4: the CTA-pair kernel; others: one CTA per unit
   cudaError_t e = gqa::prefill_pair_eligible(a)
                       ? gqa::prefill_pair_launch(a, static_cast<cudaStream_t>(stream), g_encode)
                       : gqa::prefill_launch(a, static_cast<cudaStream_t>(stream), g_encode);
   if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
   return to_status(e);
+}
+
+GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
+                                    const gqa_bf16_t *v, int B, int H_q, int H_kv, int T_q,
+                                    int S_kv, int d, int q_offset, float scale, gqa_bf16_t *o,
+                                    float *lse, gqa_stream_t stream) {
+  return gqa_attn_prefill_causal_ws(q, k, v, B, H_q, H_kv, T_q, S_kv, d, q_offset, scale, o, lse,
+                                    nullptr, 0, stream);
+}
+
+GQA_API int gqa_attn_prefill_causal_kernel_count(int B, int H_q, int H_kv, int T_q, int S_kv,
+                                                 int d, int q_offset, size_t ws_bytes,
+                                                 int *out_kernels) {
+  if (!out_kernels) return GQA_ERR_INVALID_ARG;
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0 ||
+      H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
+    return GQA_ERR_INVALID_ARG;
+  if (B == 0 || T_q == 0) {
+    *out_kernels = 0;
+    return GQA_OK;
+  }
+  DeviceState *st = nullptr;
+  int rc = device_state(&st);
+  if (rc != GQA_OK) return rc;
+  // a non-null stand-in: only the size decides whether the plan splits
+  void *ws = ws_bytes > 0 ? reinterpret_cast<void *>(uintptr_t(256)) : nullptr;
+  const gqa::PrefillLaunch a = prefill_launch_args(nullptr, nullptr, nullptr, B, H_q, H_kv, T_q,
+                                                   S_kv, q_offset, 1.f, nullptr, nullptr, ws,
+                                                   ws_bytes, st);
+  *out_kernels = gqa::prefill_pair_eligible(a) && gqa::prefill_pair_plan(a).pieces > 0 ? 2 : 1;
+  return GQA_OK;
 }
 
 // ---- host-buffer variants ------------------------------------------------------

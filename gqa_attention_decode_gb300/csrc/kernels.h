@@ -72,7 +72,19 @@ struct PrefillLaunch {
   float *lse;   // [B, H_q, T_q]
   int num_sms;
   int max_pairs;  // CTA-pair kernel: clusters of two resident at once (0: not available)
+  void *ws;         // optional scratch for key-split pieces (nullptr: no split)
+  size_t ws_bytes;
   WaitCtl wait;
+};
+
+// CTA-pair kernel work plan (host only).
+struct PrefillPairPlan {
+  int units = 0;    // 128-row query tiles x head quads
+  int n_full = 0;   // units run whole
+  int split_s = 1;  // pieces per split unit
+  int pieces = 0;   // (units - n_full) * split_s
+  int n_items = 0;  // n_full + pieces
+  int n_pairs = 0;  // clusters launched
 };
 
 // Single-CTA kernel (any group size).
@@ -82,6 +94,9 @@ cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
 // CTA-pair kernel (tcgen05 cta_group::2), for group sizes that are multiples of 4.
 cudaError_t prefill_pair_prepare_device(int *max_pairs);
 bool prefill_pair_eligible(const PrefillLaunch &a);
+PrefillPairPlan prefill_pair_plan(const PrefillLaunch &a);
+// Workspace that lets every partial round split (at most one piece per pair).
+size_t prefill_pair_workspace_bound(long long units, int num_sms);
 cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
                                 PFN_cuTensorMapEncodeTiled_v12000 encode);
 

@@ -71,24 +71,46 @@ struct Params {
   uint16_t *o;
   float *lse;
   int B, H_q, H_kv, G, T_q, S_kv, q_offset;
-  int n_qtiles, n_quads, total_units, n_pairs;
-  float sl2;  // scale * log2(e)
+  int n_qtiles, n_quads, n_items, n_pairs;
+  // Key-range split of the last round: items [0, n_full) are whole units; the
+  // units after them are each cut into split_s pieces (items n_full + t, piece
+  // t), whose partials go to ws_o / ws_ml and are combined by the merge kernel.
+  int n_full, split_s;
+  float *ws_o;   // [piece][4 heads][128 rows][128] fp32, O not yet divided by l
+  float *ws_ml;  // [piece][4 heads][128 rows][2] fp32: m (log2 units), l
+  float sl2;     // scale * log2(e)
   WaitCtl wait;
 };
 
 struct Unit {
   int b, kv, qt, quad, n_kv;
+  int kv_lo, kv_hi;  // key tiles of this item: [kv_lo, kv_hi)
+  int piece;         // -1: a whole unit, O and lse final; else its partial slot
 };
 
-// Unit of round k for worker w of P: units are sorted longest first and dealt
+// Item of round k for worker w of P: items are sorted longest first and dealt
 // in snake order (left to right, then right to left), so no worker takes the
-// longest unit of every round; only the last round can be partial.
+// longest item of every round; only the last round can be partial.
 __device__ __forceinline__ int snake_unit(int k, int w, int P) {
   return k * P + ((k & 1) ? P - 1 - w : w);
 }
 
-__device__ __forceinline__ Unit unit_at(const Params &p, int u) {
+// Key tile where piece i of s of an n-tile range starts.  With at least two
+// tiles per piece every piece but the first starts at or before the tile of
+// the unit's first query row, so its first tile has a visible key in every row.
+__host__ __device__ __forceinline__ int piece_start(int i, int s, int n) {
+  return (int)((long long)i * n / s);
+}
+
+__device__ __forceinline__ Unit unit_at(const Params &p, int item) {
   Unit w;
+  int u = item;
+  w.piece = -1;
+  if (item >= p.n_full) {
+    const int t = item - p.n_full;
+    u = p.n_full + t / p.split_s;
+    w.piece = t;
+  }
   const int per_qt = p.B * p.H_kv * p.n_quads;
   w.qt = p.n_qtiles - 1 - u / per_qt;  // latest (longest) query tiles first
   int r = u % per_qt;
@@ -98,6 +120,13 @@ __device__ __forceinline__ Unit unit_at(const Params &p, int u) {
   w.b = r / p.H_kv;
   const int qe = min((w.qt + 1) * kBM, p.T_q);
   w.n_kv = (p.q_offset + qe - 1) / kBN + 1;
+  w.kv_lo = 0;
+  w.kv_hi = w.n_kv;
+  if (w.piece >= 0) {
+    const int i = w.piece % p.split_s;
+    w.kv_lo = piece_start(i, p.split_s, w.n_kv);
+    w.kv_hi = piece_start(i + 1, p.split_s, w.n_kv);
+  }
   return w;
 }
 
@@ -202,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int k = 0; ok; ++k, ++it) {
         const int u = snake_unit(k, pair_id, p.n_pairs);
-        if (u >= p.total_units) break;
+        if (u >= p.n_items) break;
         const Unit w = unit_at(p, u);
         if (!wait_bar(q_empty, (it & 1) ^ 1, p.wait, abort_flag)) { ok = false; break; }
         for (int i = 0; i < 2; ++i) {
@@ -215,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              w.b * p.H_q + h, pol_q);
         }
         const int kv_row = w.b * p.H_kv + w.kv;
-        for (int j = 0; ok && j < w.n_kv; ++j) {
+        for (int j = w.kv_lo; ok && j < w.kv_hi; ++j) {
           for (int which = 0; which < 2; ++which, ++ld) {
             const int s = ld % kStages;
             if (!wait_bar(kv_empty(s), ((ld / kStages) & 1) ^ 1, p.wait, abort_flag)) {
@@ -258,9 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int k = 0; ok; ++k, ++it) {
         const int u = snake_unit(k, pair_id, p.n_pairs);
-        if (u >= p.total_units) break;
+        if (u >= p.n_items) break;
         const Unit w = unit_at(p, u);
-        const int n = w.n_kv;
+        const int n = w.kv_hi - w.kv_lo;
         for (int i = 0; ok && i < 2; ++i)
           if (!wait_bar(q_full(i), it & 1, p.wait, abort_flag)) ok = false;
         tc::fence_after_sync();
@@ -325,12 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = 0; ok; ++k, ++it) {
       const int u = snake_unit(k, pair_id, p.n_pairs);
-      if (u >= p.total_units) break;
+      if (u >= p.n_items) break;
       const Unit w = unit_at(p, u);
       const int q0 = p.q_offset + w.qt * kBM;  // absolute position of row 0 of the tile
       const int qpos = q0 + row;
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < w.n_kv; ++j, ++tile) {
+      for (int j = w.kv_lo; j < w.kv_hi; ++j, ++tile) {
         bool ready = wait_bar(s_full(i), tile & 1, p.wait, abort_flag);
         if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
         tc::fence_after_sync();
@@ -426,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (32 * c + e >= lim) sv[32 * c + e] = __float_as_uint(-INFINITY);
           }
         }
-        if (j == 0) {  // key 0 is visible to every row: finite
+        if (j == w.kv_lo) {  // its first key is visible to every row: finite
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int e = 0; e < kBN; e += 8)
@@ -451,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The reference max only moves when a score exceeds it by more than the
         // threshold; such a score alone makes the tile's sum exceed 2^threshold,
         // so the row max is computed only when a sum does (or is not finite).
-        if (j > 0 && __any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
+        if (j > w.kv_lo && __any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
           const float mt = row_max();  // S is still in tensor memory (P not yet written)
           if (__any_sync(0xffffffffu, mt > m_ref + kRescaleThreshold)) {
             const float m_new = fmaxf(m_ref, mt);
@@ -497,7 +526,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) tc::ld32(t_o + 32 * c, ov + 32 * c);
       tc::wait_ld();
-      if (qrow < p.T_q) {
+      if (qrow < p.T_q && w.piece >= 0) {
+        // a piece of a split unit: its partial (O not yet divided, m, l) for the merge
+        const size_t prow = ((size_t)w.piece * 4 + 2 * i + rank) * kBM + row;
+        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * kD);
+#pragma unroll
+        for (int v4 = 0; v4 < kD / 4; ++v4)
+          dst[v4] = make_float4(__uint_as_float(ov[4 * v4 + 0]), __uint_as_float(ov[4 * v4 + 1]),
+                                __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+        reinterpret_cast<float2 *>(p.ws_ml)[prow] = make_float2(m_ref, l);
+      } else if (qrow < p.T_q) {
         const float inv_l = 1.f / l;
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD);
 #pragma unroll
@@ -525,6 +563,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc_pair(tmem, kTmemCols);
   }
+}
+
+// Merge of a split unit's pieces (the log-sum-exp combination of partial
+// softmax states), one warp per (split unit, head, query row):
+//   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,
+//   O = sum_i 2^(m_i - M) O_i / L,  lse = M ln 2 + ln L.
+// Lane i < s reads piece i's (m, l); every lane owns 4 of the 128 columns.
+// Launched as a programmatic dependent of the pair kernel: the partials are
+// read through L2 after the grid-dependency wait.
+constexpr int kMergeThreads = 256;
+constexpr int kMaxPieces = 32;      // pieces per unit (one lane each in the merge)
+constexpr int kMinPieceTiles = 8;   // key tiles per piece at least
+constexpr size_t kPieceBytes = (size_t)4 * kBM * (kD + 2) * sizeof(float);
+
+__global__ void __launch_bounds__(kMergeThreads) prefill_pair_merge_kernel(const Params p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
+  const int row = gw % kBM;
+  const int hl = (gw / kBM) % 4;  // head within the unit: 2 * slot + rank
+  const int su = gw / (4 * kBM);  // split unit
+  const int s = p.split_s;
+  if (su >= (p.n_items - p.n_full) / s) return;
+  const Unit w = unit_at(p, p.n_full + su * s);
+  const int qrow = w.qt * kBM + row;
+  if (qrow >= p.T_q) return;
+  const int h = head_of(p, w, hl & 1, hl >> 1);
+  const size_t orow = ((size_t)w.b * p.H_q + h) * p.T_q + qrow;
+  auto prow = [&](int i) { return ((size_t)(su * s + i) * 4 + hl) * kBM + row; };
+  float m = -INFINITY, l = 0.f;
+  if (lane < s) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml) + prow(lane));
+    m = ml.x;
+    l = ml.y;
+  }
+  float M = m;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float wgt = m > -INFINITY ? fast_exp2(m - M) : 0.f;
+  float L = wgt * l;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int i = 0; i < s; ++i) {
+    const float wi = __shfl_sync(0xffffffffu, wgt, i);
+    const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + prow(i) * kD) + lane);
+    acc.x = fmaf(wi, x.x, acc.x);
+    acc.y = fmaf(wi, x.y, acc.y);
+    acc.z = fmaf(wi, x.z, acc.z);
+    acc.w = fmaf(wi, x.w, acc.w);
+  }
+  const float inv_l = L > 0.f ? 1.f / L : 0.f;
+  uint2 pk;
+  pk.x = pack_bf16x2(acc.x * inv_l, acc.y * inv_l);
+  pk.y = pack_bf16x2(acc.z * inv_l, acc.w * inv_l);
+  reinterpret_cast<uint2 *>(p.o + orow * kD)[lane] = pk;
+  if (lane == 0) p.lse[orow] = L > 0.f ? M * 0.69314718055994531f + logf(L) : -INFINITY;
 }
 
 // dims (innermost first): 64 columns, 2 column halves, rows, heads; box of
@@ -570,10 +667,53 @@ bool prefill_pair_eligible(const PrefillLaunch &a) {
   return a.H_kv > 0 && (a.H_q / a.H_kv) % 4 == 0 && a.max_pairs > 0;
 }
 
+// Work plan: units of one 128-row query tile of four heads; with a workspace,
+// the units of the last, partial round (all units when there are fewer than
+// pairs) are cut into pieces of contiguous key tiles so the round fills the
+// pairs.  Pieces per unit: pairs / such units, at most kMaxPieces, at least
+// kMinPieceTiles tiles each (the shortest unit is the one of query tile 0).
+PrefillPairPlan prefill_pair_plan(const PrefillLaunch &a) {
+  using namespace prefill_pair;
+  PrefillPairPlan pl;
+  const int G = a.H_q / a.H_kv;
+  const int n_qtiles = (a.T_q + kBM - 1) / kBM;
+  const long long units = (long long)n_qtiles * a.B * a.H_kv * (G / 4);
+  if (units <= 0 || units > 0x7fffffffLL || a.max_pairs <= 0) return pl;
+  const int U = (int)units, P = a.max_pairs;
+  pl.units = U;
+  pl.n_full = U;
+  pl.split_s = 1;
+  const int r = U % P;  // units of the last round
+  if (a.ws != nullptr && r > 0) {
+    const int n_kv_min = (a.q_offset + (a.T_q < kBM ? a.T_q : kBM) - 1) / kBN + 1;
+    int sp = P / r;
+    if (sp > kMaxPieces) sp = kMaxPieces;
+    if (sp > n_kv_min / kMinPieceTiles) sp = n_kv_min / kMinPieceTiles;
+    if (sp >= 2 && (size_t)r * sp * kPieceBytes <= a.ws_bytes) {
+      pl.n_full = U - r;
+      pl.split_s = sp;
+    }
+  }
+  pl.pieces = (U - pl.n_full) * pl.split_s;
+  pl.n_items = pl.n_full + pl.pieces;
+  pl.n_pairs = pl.n_items < P ? pl.n_items : P;
+  return pl;
+}
+
+size_t prefill_pair_workspace_bound(long long units, int num_sms) {
+  using namespace prefill_pair;
+  // never more pieces than pairs, nor than kMaxPieces per unit
+  const long long pairs = num_sms / 2, most = units * kMaxPieces;
+  const long long pieces = most < pairs ? most : pairs;
+  return pieces > 0 ? (size_t)pieces * kPieceBytes : 0;
+}
+
 cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
                                 PFN_cuTensorMapEncodeTiled_v12000 encode) {
   using namespace prefill_pair;
   if (!prefill_pair_eligible(a)) return cudaErrorNotSupported;
+  const PrefillPairPlan pl = prefill_pair_plan(a);
+  if (pl.units <= 0) return cudaErrorNotSupported;
   CUtensorMap tm_q, tm_k, tm_v;
   if (make_map(&tm_q, a.q, a.T_q, a.B * a.H_q, kBM, encode) != CUDA_SUCCESS ||
       make_map(&tm_k, a.k, a.S_kv, a.B * a.H_kv, kHalfKeys, encode) != CUDA_SUCCESS ||
@@ -591,10 +731,12 @@ cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
   p.q_offset = a.q_offset;
   p.n_qtiles = (a.T_q + kBM - 1) / kBM;
   p.n_quads = p.G / 4;
-  const long long units = (long long)p.n_qtiles * a.B * a.H_kv * p.n_quads;
-  if (units > 0x7fffffffLL) return cudaErrorNotSupported;
-  p.total_units = (int)units;
-  p.n_pairs = (int)(units < a.max_pairs ? units : a.max_pairs);
+  p.n_items = pl.n_items;
+  p.n_pairs = pl.n_pairs;
+  p.n_full = pl.n_full;
+  p.split_s = pl.split_s;
+  p.ws_o = pl.pieces > 0 ? static_cast<float *>(a.ws) : nullptr;
+  p.ws_ml = pl.pieces > 0 ? p.ws_o + (size_t)pl.pieces * 4 * kBM * kD : nullptr;
   p.sl2 = a.scale * 1.4426950408889634f;
   p.wait = a.wait;
   cudaLaunchConfig_t cfg = {};
@@ -609,7 +751,20 @@ cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tm_q, tm_k, tm_v, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tm_q, tm_k, tm_v, p);
+  if (e != cudaSuccess || pl.pieces == 0) return e;
+  // the pieces' merge, a programmatic dependent of the pair kernel
+  const long long warps = (long long)(pl.pieces / pl.split_s) * 4 * kBM;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3((unsigned)((warps + kMergeThreads / 32 - 1) / (kMergeThreads / 32)), 1, 1);
+  mcfg.blockDim = dim3(kMergeThreads, 1, 1);
+  mcfg.stream = stream;
+  cudaLaunchAttribute mattr[1];
+  mattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  mattr[0].val.programmaticStreamSerializationAllowed = 1;
+  mcfg.attrs = mattr;
+  mcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&mcfg, prefill_pair_merge_kernel, p);
 }
 
 }  // namespace gqa

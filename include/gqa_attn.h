@@ -304,6 +304,65 @@ GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
                                     int S_kv, int d, int q_offset, float scale, gqa_bf16_t *o,
                                     float *lse, gqa_stream_t stream);
 
+/*
+ * Bytes of device workspace that let gqa_attn_prefill_causal_ws split key
+ * ranges (host only, no CUDA call).  Work is dealt in rounds of units (a
+ * 128-row query tile of four heads of a KV group) over the device's CTA
+ * pairs; when the last round is partial -- or there are fewer units than
+ * pairs, as for a short chunk after a long prefix -- its units are cut into
+ * pieces of contiguous key tiles (at least 8 tiles each, at most one piece per
+ * pair), each piece's partial softmax state (O before division, m, l) goes to
+ * the workspace and a log-sum-exp merge kernel combines them: the record's
+ * split-and-reduce (sections 2.2 and 4) applied to prefill.  The bound is one
+ * piece per pair, at most 32 per unit: min(32 * units, num_sms / 2) * 266240
+ * bytes, rounded up to 256.
+ * Returns 0 when nothing would split (G not a multiple of 4) or for invalid
+ * arguments.
+ */
+GQA_API size_t gqa_attn_prefill_causal_workspace_size(int B, int H_q, int H_kv, int T_q,
+                                                      int S_kv, int d, int q_offset,
+                                                      int num_sms);
+
+/*
+ * The CTA-pair prefill work plan for `num_pairs` resident pairs and `ws_bytes`
+ * of workspace (host only, no CUDA call): writes the number of units, how
+ * many of them (the last round's) are split, and the pieces per split unit
+ * (1 if none).  Piece i of s of a unit with n key tiles covers tiles
+ * [i*n/s, (i+1)*n/s).  Units are dealt longest first, so the split ones are
+ * the shortest.  G not a multiple of 4 (one CTA per unit): 0 units, no split.
+ * Returns GQA_OK or GQA_ERR_INVALID_ARG.
+ */
+GQA_API int gqa_attn_prefill_causal_plan(int B, int H_q, int H_kv, int T_q, int S_kv, int d,
+                                         int q_offset, int num_pairs, size_t ws_bytes,
+                                         int *out_units, int *out_split_units,
+                                         int *out_pieces_per_unit);
+
+/*
+ * gqa_attn_prefill_causal with a workspace for key-range splitting.
+ *   workspace  device scratch, 16-byte aligned, contents on entry irrelevant
+ *              (overwritten); nullptr with ws_bytes == 0 is the plain call.
+ *   ws_bytes   its size.  The plan splits only if the pieces it wants fit;
+ *              otherwise it runs whole units (never an error for being small).
+ * With a split, two kernels run on `stream`: the pair kernel and the merge
+ * (a programmatic dependent).  Results agree with the plain call within
+ * rounding (the split changes the fp32 summation order); repeated calls with
+ * the same sizes and workspace size are bit-identical.
+ */
+GQA_API int gqa_attn_prefill_causal_ws(const gqa_bf16_t *q, const gqa_bf16_t *k,
+                                       const gqa_bf16_t *v, int B, int H_q, int H_kv, int T_q,
+                                       int S_kv, int d, int q_offset, float scale, gqa_bf16_t *o,
+                                       float *lse, void *workspace, size_t ws_bytes,
+                                       gqa_stream_t stream);
+
+/*
+ * Kernels one gqa_attn_prefill_causal_ws call with `ws_bytes` of workspace
+ * launches on the current device: 1, 2 (split + merge), 0 for an empty
+ * problem.  Initialises the library's per-device state (a CUDA call).
+ */
+GQA_API int gqa_attn_prefill_causal_kernel_count(int B, int H_q, int H_kv, int T_q, int S_kv,
+                                                 int d, int q_offset, size_t ws_bytes,
+                                                 int *out_kernels);
+
 /* ------------------------------------------------------------------------- */
 /* Host-buffer variants (whole-call end-to-end path)                           */
 /* ------------------------------------------------------------------------- */

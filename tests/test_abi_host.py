@@ -86,6 +86,76 @@ def test_workspace_size(lib):
     assert gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 0, 0) == 0  # bad num_sms
 
 
+PIECE_BYTES = 4 * 128 * 130 * 4   # per piece: 4 heads x 128 rows x (O[128], m, l) fp32
+
+
+@pytest.mark.parametrize("shape,pairs,expect", [
+    # chunked 32K (last 2K): 256 units on 76 pairs, the 28 of the fourth round cut in 2
+    ((1, 64, 8, 2048, 32768, 30720), 76, (256, 28, 2)),
+    # 8K causal: the last round's units are 1-3 key tiles long, nothing to split
+    ((1, 64, 8, 8192, 8192, 0), 76, (1024, 0, 1)),
+    # a 128-token chunk after 32K keys: 16 units, each cut in 4 (76 // 16)
+    ((1, 64, 8, 128, 32768, 32640), 76, (16, 16, 4)),
+    # two units of 32 tiles: at most 32 // 8 = 4 pieces each
+    ((1, 8, 2, 128, 4096, 3968), 76, (2, 2, 4)),
+    # units fill whole rounds: no split
+    ((1, 64, 8, 2048, 32768, 30720), 64, (256, 0, 1)),
+    # one unit, 300 pairs: capped at 32 pieces
+    ((1, 4, 1, 100, 65536, 65436), 300, (1, 1, 32)),
+    # G not a multiple of 4 runs one CTA per unit: no plan
+    ((1, 6, 2, 2048, 32768, 30720), 76, (0, 0, 1)),
+])
+def test_prefill_split_plan(lib, shape, pairs, expect):
+    B, H_q, H_kv, T_q, S_kv, q_off = shape
+    got = gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, pairs, 1 << 30)
+    assert got == expect
+    units, split_units, s = got
+    if split_units:
+        # the workspace the plan needs is within the size query's bound
+        bound = gqa.gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, 128, q_off,
+                                                           2 * pairs)
+        assert split_units * s * PIECE_BYTES <= bound
+        # too small a workspace: no split, never an error
+        assert gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, pairs,
+                                                split_units * s * PIECE_BYTES - 1)[1] == 0
+        # no workspace: no split
+        assert gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, pairs,
+                                                0)[1] == 0
+
+
+@pytest.mark.parametrize("q_off,T_q,s", [(30720, 2048, 2), (32640, 128, 4), (3968, 128, 4),
+                                         (1000, 300, 3), (65436, 100, 32)])
+def test_prefill_pieces_cover_the_key_range(q_off, T_q, s):
+    """Piece i of s covers key tiles [i*n/s, (i+1)*n/s) of a unit with n tiles:
+    together exactly [0, n), each at least 8 tiles when s <= n // 8, and every
+    piece but the first starts at or before the tile of the unit's first query
+    row, so each piece's first tile has a visible key in every row."""
+    for qt in range((T_q + 127) // 128):
+        q0 = q_off + 128 * qt
+        qe = min(128 * (qt + 1), T_q)
+        n = (q_off + qe - 1) // 128 + 1
+        if s > n // 8:
+            continue
+        starts = [i * n // s for i in range(s + 1)]
+        assert starts[0] == 0 and starts[-1] == n
+        assert all(b - a >= 8 for a, b in zip(starts, starts[1:]))
+        assert all(starts[i] * 128 <= q0 for i in range(s))
+
+
+def test_prefill_workspace_size(lib):
+    # one piece per pair at most: 76 pairs on 152 SMs
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 2048, 32768, 128, 30720,
+                                                      152) == 76 * PIECE_BYTES
+    # fewer units than pairs: up to 32 pieces per unit, never more than the pairs
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 8, 2, 128, 4096, 128, 3968,
+                                                      152) == 64 * PIECE_BYTES
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 4, 1, 100, 4096, 128, 3996,
+                                                      152) == 32 * PIECE_BYTES
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 6, 2, 128, 4096, 128, 3968, 152) == 0
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 100, 128, 0, 152) == 0
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 256, 128, 0, 0) == 0
+
+
 def test_plan_rejects_bad_arguments(lib):
     with pytest.raises(gqa.GQAError) as e:
         gqa.gqa_attn_decode_plan(-1, 8, 100, 152, 0)

@@ -154,6 +154,86 @@ def test_running_max_paths(H_q, H_kv):
     compare(o, lse, o_ref, lse_ref, f"running max paths G={H_q // H_kv}")
 
 
+# Shapes whose last round of units is split by key range (76 CTA pairs on a
+# GB300): (B, H_q, H_kv, T_q, S_kv, q_offset).
+SPLIT_CASES = [
+    (1, 8, 2, 128, 4096, 3968),     # 2 units, 4 pieces each (fewer units than pairs)
+    (1, 16, 2, 200, 3000, 2800),    # G = 8, 8 units, ragged second query tile
+    (1, 8, 1, 300, 4300, 4000),     # 6 units, 4 pieces each, q_offset not tile aligned
+    (1, 32, 8, 1280, 3328, 2048),   # 80 units: one full round, the 4 left cut in 2
+    (2, 16, 2, 256, 2304, 2048),    # two sequences
+]
+
+
+def _run_ws(q, k, v, q_offset, scale, ws):
+    o, lse = gqa.gqa_attn_prefill_causal(q, k, v, scale, q_offset, workspace=ws)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,T_q,S_kv,q_offset", SPLIT_CASES)
+def test_key_split_full_compare(B, H_q, H_kv, T_q, S_kv, q_offset):
+    """Pieces of the last round's units write partial (O, m, l); the merge
+    kernel combines them; compared in full with the oracle."""
+    nb = gqa.gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, 128, q_offset,
+                                                    torch.cuda.get_device_properties(0).multi_processor_count)
+    assert gqa.gqa_attn_prefill_causal_kernel_count(B, H_q, H_kv, T_q, S_kv, 128, q_offset,
+                                                    nb, DEV) == 2
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=41, device=DEV)
+    scale = 1 / math.sqrt(128)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    ws.fill_(0xFF)                     # contents on entry must not matter (NaN bit patterns)
+    o, lse = _run_ws(q, k, v, q_offset, scale, ws)
+    o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), q_offset, scale)
+    compare(o, lse, o_ref, lse_ref, f"split {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
+    # the same call without a workspace runs whole units: equal within rounding
+    o1, l1 = _run_ws(q, k, v, q_offset, scale, torch.empty(0, dtype=torch.uint8, device=DEV))
+    assert (o.float() - o1.float()).abs().max().item() <= 2 ** -7
+    assert (lse - l1).abs().max().item() <= 1e-5
+    # deterministic with the split
+    o2, l2 = _run_ws(q, k, v, q_offset, scale, ws)
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+
+
+def test_key_split_scores_jump_between_pieces():
+    """Keys of the second half score 20 (log2 units) above the first: the pieces'
+    reference maxima differ by 20 and the merge's weights 2^(m_i - M) carry it."""
+    B, H_q, H_kv, T_q, S_kv, q_offset = SPLIT_CASES[0]
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=42, device=DEV)
+    q.zero_()
+    q[..., 0] = 1.0
+    k.zero_()
+    k[:, :, 2048:, 0] = 20.0
+    k[:, :, 3000:, 0] = -30.0
+    scale = math.log(2.0)
+    o, lse = gqa.gqa_attn_prefill_causal(q, k, v, scale, q_offset)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), q_offset, scale)
+    compare(o, lse, o_ref, lse_ref, "split, scores jump between pieces")
+
+
+def test_short_chunk_after_long_prefix_sampled():
+    """A 128-token chunk after 32K keys (Llama3-70B layer): 16 units on 76 pairs,
+    each cut in 4 pieces; sampled rows against the oracle."""
+    B, H_q, H_kv, T_q, S_kv = 1, 64, 8, 128, 32768
+    q_offset = S_kv - T_q
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=43, device=DEV)
+    o, lse = gqa.gqa_attn_prefill_causal(q, k, v, 1 / math.sqrt(128), q_offset)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(9)
+    picks = [(0, int(h), int(i)) for h, i in zip(rng.integers(0, H_q, 24), rng.integers(0, T_q, 24))]
+    picks += [(0, 0, 0), (0, 63, 127), (0, 7, 64)]
+    ref_o = np.zeros((len(picks), 128))
+    ref_lse = np.zeros(len(picks))
+    for r, (b, h, i) in enumerate(picks):
+        n = q_offset + i + 1
+        ro, rl = oracle.attend_rows(np64(q[b, h, i])[None], np64(k[b, h // 8, :n]),
+                                    np64(v[b, h // 8, :n]), 1 / math.sqrt(128), [n])
+        ref_o[r], ref_lse[r] = ro[0], rl[0]
+    compare(torch.stack([o[b, h, i] for b, h, i in picks]),
+            torch.stack([lse[b, h, i] for b, h, i in picks]), ref_o, ref_lse, "128 after 32K")
+
+
 @pytest.mark.parametrize("scale", [0.0, -0.15, 0.3])
 def test_scale_values(scale):
     q, k, v = gqa_synth.prefill_inputs(1, 8, 1, 200, 260, 128, seed=32, device=DEV)
