@@ -13,7 +13,10 @@
  *   gqa_attn_prefill_causal  causal prefill with online softmax and fully masked
  *                            tiles skipped (section 3 "Per-tile op sequence",
  *                            section 5.4 "PREFILL, no SP"), with q_offset for
- *                            chunked prefill (section 0.5.3 "q_block_meta").
+ *                            chunked prefill (section 0.5.3 "q_block_meta");
+ *                            gqa_attn_prefill_causal_ws adds a workspace so
+ *                            the last round of work can be split by key range
+ *                            and merged like decode's chunks.
  *
  * Both compute, for query head h, KV head h / G (G = H_q / H_kv) and the keys
  * visible to the query,
