@@ -633,8 +633,12 @@ def run_all_configs(device):
                     w.B * mp, w.H_kv, page_size, w.d).contiguous()
                 pages.append((kp, vp))
             table = torch.arange(w.B * mp, dtype=torch.int32, device=device).view(w.B, mp)
-            fn = lambda: [gqa.gqa_attn_decode_paged(q, kp, vp, table, sld, w.scale, ns)
-                          for kp, vp in pages]
+            if T_q > 1:
+                fn = lambda: [gqa.gqa_attn_decode_paged_multi(q, kp, vp, table, sld, w.scale, ns)
+                              for kp, vp in pages]
+            else:
+                fn = lambda: [gqa.gqa_attn_decode_paged(q, kp, vp, table, sld, w.scale, ns)
+                              for kp, vp in pages]
         elif T_q > 1:
             fn = lambda: [gqa.gqa_attn_decode_multi(q, kc, vc, sld, w.scale, ns) for kc, vc in kvs]
         else:
@@ -677,6 +681,7 @@ def run_all_configs(device):
     decode_line("llama70b_decode_32k", T_q=4)
     decode_line("llama70b_decode_32k", T_q=16)
     decode_line("llama70b_decode_32k", page_size=256)
+    decode_line("llama70b_decode_32k", T_q=16, page_size=256)
 
 
 def main():

@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     gqa_attn_decode_kernel_count,
     gqa_attn_decode_paged,
     gqa_attn_decode_multi,
+    gqa_attn_decode_paged_multi,
     gqa_attn_decode_multi_workspace_size,
     gqa_attn_decode_split,
     gqa_attn_decode_merge,

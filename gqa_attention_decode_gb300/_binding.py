@@ -37,6 +37,9 @@ _SIGNATURES = {
     "gqa_attn_decode_paged": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _c_float, _c_int, _vp, _vp, _vp,
                                        _c_size, _vp]),
+    "gqa_attn_decode_paged_multi": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                             _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "gqa_attn_decode_multi_workspace_size": (_c_size, [_c_int] * 8),
     "gqa_attn_decode_multi": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                        _c_int, _c_float, _c_int, _vp, _vp, _vp, _c_size, _vp]),
@@ -227,6 +230,44 @@ def gqa_attn_decode_paged(q, k_pages, v_pages, block_table, seqlens, scale, num_
                                        _ptr(lse), _ptr(workspace), workspace.numel(),
                                        _stream_handle(stream, dev))
     _check(rc, "gqa_attn_decode_paged")
+    return o, lse
+
+
+def gqa_attn_decode_paged_multi(q, k_pages, v_pages, block_table, seqlens, scale, num_splits=0,
+                                o=None, lse=None, workspace=None, stream=None):
+    """Multi-token decode over a paged cache.  q [B,H_q,T_q,d] bf16 (token t at position
+    seqlens[b]-T_q+t); k_pages, v_pages [num_pages,H_kv,page_size,d] bf16; block_table
+    [B, max_pages_per_seq] int32; seqlens [B] int32.  Returns (o, lse)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    _need(k_pages, "k_pages", torch.bfloat16, 4, dev)
+    _need(v_pages, "v_pages", torch.bfloat16, 4, dev)
+    _need(block_table, "block_table", torch.int32, 2, dev)
+    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    B, H_q, T_q, d = q.shape
+    num_pages, H_kv, page_size, _ = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or k_pages.shape[3] != d:
+        raise ValueError("k_pages/v_pages must be [num_pages, H_kv, page_size, d]")
+    if block_table.shape[0] != B or seqlens.shape[0] != B:
+        raise ValueError("block_table and seqlens need B rows")
+    max_pages = block_table.shape[1]
+    if o is None:
+        o = torch.empty((B, H_q, T_q, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=dev)
+    if workspace is None:
+        nbytes = gqa_attn_decode_multi_workspace_size(B, H_q, H_kv, T_q, max_pages * page_size, d,
+                                                      _num_sms(dev), num_splits)
+        workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_decode_paged_multi(_ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                             _ptr(block_table), _ptr(seqlens), B, H_q, H_kv, T_q,
+                                             num_pages, page_size, max_pages, d, float(scale),
+                                             int(num_splits), _ptr(o), _ptr(lse),
+                                             _ptr(workspace), workspace.numel(),
+                                             _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_decode_paged_multi")
     return o, lse
 
 

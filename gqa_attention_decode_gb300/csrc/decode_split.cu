@@ -171,10 +171,10 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
         }
         const int page_id = __shfl_sync(0xffffffffu, page_reg, page - page_base);
         // a page id outside the pool reads zeros (TMA out-of-bounds fill); report it
-        if ((page_id < 0 || page_id >= p.num_pages) && lane == 0)
-          atomicExch(p.wait.status, kStatusInvalidArg);
+        const bool bad = page_id < 0 || page_id >= p.num_pages;
+        if (bad && lane == 0) atomicExch(p.wait.status, kStatusInvalidArg);
         c2 = key0 - page * p.page_size;
-        c3 = page_id * p.H_kv + kv;
+        c3 = bad ? p.num_pages * p.H_kv : page_id * p.H_kv + kv;  // bad: one block past the map
       }
       bool ok = true;
       if (lane == 0) {

@@ -58,9 +58,11 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
   const int32_t *seqlens;
+  const int32_t *block_table;  // paged cache: [B, max_pages]; nullptr: dense cache
   float *o_part;
   float *lse_part;
   int B, H_q, H_kv, G, T_q, S_max, num_splits, chunk;
+  int page_size, max_pages, num_pages;
   float sl2;  // scale * log2(e)
   WaitCtl wait;
 };
@@ -163,18 +165,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     // ------------------------- TMA producer -------------------------
+    // Lane 0 issues every copy.  With a paged cache the whole warp keeps 32
+    // block-table entries in registers, so a tile's page is a shuffle away (a
+    // 128-key tile never straddles pages: page sizes are multiples of 128).
     int ld = 0;
     bool ok = true;
+    const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const uint64_t pol = l2_policy_evict_first();
       const int q_row0 = (b * p.H_q + kv * p.G) * p.T_q;  // first (head, token) row of the group
       mbar_arrive_expect_tx(q_full, kTileBytes);
       for (int half = 0; half < 2; ++half)
         tma_load_4d(sbase + kOffQ + half * kHalfBytes, &tm_q, q_full, 0, half, q_row0, 0, pol);
-      for (int j = 0; ok && j < n_tiles; ++j) {
+    }
+    int page_base = -(1 << 30), page_reg = 0;
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int key0 = key_begin + j * kBN;
+      int c2 = key0, c3 = b * p.H_kv + kv;  // tensor-map coordinates of the tile's first key
+      if (p.block_table != nullptr) {
+        const int page = key0 / p.page_size;
+        if (page - page_base >= 32 || page < page_base) {
+          page_base = page;
+          const int idx = page_base + lane;
+          page_reg = idx < p.max_pages ? __ldca(p.block_table + (size_t)b * p.max_pages + idx) : 0;
+        }
+        const int page_id = __shfl_sync(0xffffffffu, page_reg, page - page_base);
+        // a page id outside the pool reads zeros (a block past the tensor map:
+        // TMA out-of-bounds fill); it is reported through the status word
+        const bool bad = page_id < 0 || page_id >= p.num_pages;
+        if (bad && lane == 0) atomicExch(p.wait.status, kStatusInvalidArg);
+        c2 = key0 - page * p.page_size;
+        c3 = bad ? p.num_pages * p.H_kv : page_id * p.H_kv + kv;
+      }
+      if (lane == 0) {
         for (int which = 0; which < 2; ++which, ++ld) {
           const int s = ld % kStages;
           if (!wait_bar(kv_empty(s), ((ld / kStages) & 1) ^ 1, p.wait, abort_flag)) {
@@ -185,10 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(kv_full(s), kTileBytes);
           const CUtensorMap *map = which == 0 ? &tm_k : &tm_v;
           for (int half = 0; half < 2; ++half)
-            tma_load_4d(dst + half * kHalfBytes, map, kv_full(s), 0, half, key_begin + j * kBN,
-                        b * p.H_kv + kv, pol);
+            tma_load_4d(dst + half * kHalfBytes, map, kv_full(s), 0, half, c2, c3, pol);
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     ld = __shfl_sync(0xffffffffu, ld, 0);
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -473,15 +498,25 @@ cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
                                    PFN_cuTensorMapEncodeTiled_v12000 encode) {
   using namespace decode_tc;
   if (a.S_max <= 0) return cudaSuccess;
-  if (a.chunk % kBN != 0 || a.block_table != nullptr) return cudaErrorInvalidValue;
+  const bool paged = a.block_table != nullptr;
+  if (a.chunk % kBN != 0 || (paged && (a.page_size <= 0 || a.page_size % kBN != 0)))
+    return cudaErrorInvalidValue;
+  // K/V blocks of rows: one per (sequence, KV head) of S_max keys, or one per
+  // (page, KV head) of page_size keys
+  const long long kv_blocks = paged ? (long long)a.num_pages * a.H_kv : (long long)a.B * a.H_kv;
+  const int kv_rows = paged ? a.page_size : a.S_max;
   CUtensorMap tm_q, tm_k, tm_v;
   const long long q_rows = (long long)a.B * a.H_q * a.T_q;
   if (make_map(&tm_q, a.q, q_rows, 1, encode) != CUDA_SUCCESS ||
-      make_map(&tm_k, a.k_cache, a.S_max, (long long)a.B * a.H_kv, encode) != CUDA_SUCCESS ||
-      make_map(&tm_v, a.v_cache, a.S_max, (long long)a.B * a.H_kv, encode) != CUDA_SUCCESS)
+      make_map(&tm_k, a.k_cache, kv_rows, kv_blocks, encode) != CUDA_SUCCESS ||
+      make_map(&tm_v, a.v_cache, kv_rows, kv_blocks, encode) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   Params p;
   p.seqlens = a.seqlens;
+  p.block_table = a.block_table;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   p.o_part = a.o_part;
   p.lse_part = a.lse_part;
   p.B = a.B;

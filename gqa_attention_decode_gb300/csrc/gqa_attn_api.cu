@@ -147,7 +147,7 @@ bool finite_scale(float scale) {
 int check_decode_args(int phase, const void *q, const void *k, const void *v,
                       const void *seqlens, int B, int H_q, int H_kv, int S_max, int d,
                       float scale, int num_splits, const void *o, const void *lse, int T_q = 1,
-                      bool paged = false) {
+                      int page_size = 0) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || S_max < 0 || d <= 0 || num_splits < 0 || T_q <= 0)
     return GQA_ERR_INVALID_ARG;
   if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
@@ -163,9 +163,11 @@ int check_decode_args(int phase, const void *q, const void *k, const void *v,
   }
   if (d != 128) return GQA_ERR_UNSUPPORTED;
   // mma.sync split kernel: G <= 8 and G * T_q <= 32 rows per KV head; otherwise
-  // the tcgen05 split kernel, dense cache only, up to 128 rows
+  // the tcgen05 split kernel, up to 128 rows, 128-key tiles (pages of a paged
+  // cache: multiples of 128 keys)
   if (decode_on_tensor_cores(H_q, H_kv, T_q) &&
-      (paged || (long long)(H_q / H_kv) * T_q > gqa::kDecodeTcRows))
+      ((long long)(H_q / H_kv) * T_q > gqa::kDecodeTcRows ||
+       page_size % gqa::kDecodeTcTileKeys != 0))
     return GQA_ERR_UNSUPPORTED;
   if (B > 65535 || H_kv > 65535) return GQA_ERR_UNSUPPORTED;  // grid y/z limits
   if ((long long)B * H_q * T_q > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;  // output rows
@@ -254,7 +256,7 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                  const void *workspace, size_t ws_bytes, gqa_stream_t stream,
                  const PagedLayout &paged = PagedLayout{nullptr, 0, 0, 0}, int T_q = 1) {
   int rc = check_decode_args(phase, q, k_cache, v_cache, seqlens, B, H_q, H_kv, S_max, d, scale,
-                             num_splits, o, lse, T_q, paged.block_table != nullptr);
+                             num_splits, o, lse, T_q, paged.page_size);
   if (rc != GQA_OK || B == 0) return rc;
   DeviceState *st = nullptr;
   if ((rc = device_state(&st)) != GQA_OK) return rc;
@@ -319,21 +321,46 @@ GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
                       num_splits, o, lse, workspace, ws_bytes, stream);
 }
 
+namespace {
+int decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages, const gqa_bf16_t *v_pages,
+                 const int32_t *block_table, const int32_t *seqlens, int B, int H_q, int H_kv,
+                 int T_q, int num_pages, int page_size, int max_pages_per_seq, int d,
+                 float scale, int num_splits, gqa_bf16_t *o, float *lse, void *workspace,
+                 size_t ws_bytes, gqa_stream_t stream) {
+  if (num_pages < 0 || max_pages_per_seq < 0 || page_size <= 0) return GQA_ERR_INVALID_ARG;
+  if (page_size % gqa::kDecodeTileKeys != 0) return GQA_ERR_UNSUPPORTED;
+  const long long s_max = (long long)max_pages_per_seq * page_size;
+  if (s_max > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  if (H_kv > 0 && (long long)num_pages * H_kv >= 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  if (B > 0 && (!block_table || !aligned16(block_table))) return GQA_ERR_INVALID_ARG;
+  if (B > 0 && s_max > 0 && num_pages == 0) return GQA_ERR_INVALID_ARG;
+  const PagedLayout paged{block_table, num_pages, page_size, max_pages_per_seq};
+  return decode_phase(kPhaseBoth, q, k_pages, v_pages, seqlens, B, H_q, H_kv, (int)s_max, d,
+                      scale, num_splits, o, lse, workspace, ws_bytes, stream, paged, T_q);
+}
+}  // namespace
+
 GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages,
                                   const gqa_bf16_t *v_pages, const int32_t *block_table,
                                   const int32_t *seqlens, int B, int H_q, int H_kv,
                                   int num_pages, int page_size, int max_pages_per_seq, int d,
                                   float scale, int num_splits, gqa_bf16_t *o, float *lse,
                                   void *workspace, size_t ws_bytes, gqa_stream_t stream) {
-  if (num_pages < 0 || max_pages_per_seq < 0 || page_size <= 0) return GQA_ERR_INVALID_ARG;
-  if (page_size % gqa::kDecodeTileKeys != 0) return GQA_ERR_UNSUPPORTED;
-  const long long s_max = (long long)max_pages_per_seq * page_size;
-  if (s_max > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
-  if (B > 0 && (!block_table || !aligned16(block_table))) return GQA_ERR_INVALID_ARG;
-  if (B > 0 && s_max > 0 && num_pages == 0) return GQA_ERR_INVALID_ARG;
-  const PagedLayout paged{block_table, num_pages, page_size, max_pages_per_seq};
-  return decode_phase(kPhaseBoth, q, k_pages, v_pages, seqlens, B, H_q, H_kv, (int)s_max, d,
-                      scale, num_splits, o, lse, workspace, ws_bytes, stream, paged);
+  return decode_paged(q, k_pages, v_pages, block_table, seqlens, B, H_q, H_kv, 1, num_pages,
+                      page_size, max_pages_per_seq, d, scale, num_splits, o, lse, workspace,
+                      ws_bytes, stream);
+}
+
+GQA_API int gqa_attn_decode_paged_multi(const gqa_bf16_t *q, const gqa_bf16_t *k_pages,
+                                        const gqa_bf16_t *v_pages, const int32_t *block_table,
+                                        const int32_t *seqlens, int B, int H_q, int H_kv,
+                                        int T_q, int num_pages, int page_size,
+                                        int max_pages_per_seq, int d, float scale,
+                                        int num_splits, gqa_bf16_t *o, float *lse,
+                                        void *workspace, size_t ws_bytes, gqa_stream_t stream) {
+  return decode_paged(q, k_pages, v_pages, block_table, seqlens, B, H_q, H_kv, T_q, num_pages,
+                      page_size, max_pages_per_seq, d, scale, num_splits, o, lse, workspace,
+                      ws_bytes, stream);
 }
 
 GQA_API size_t gqa_attn_decode_multi_workspace_size(int B, int H_q, int H_kv, int T_q, int S_max,

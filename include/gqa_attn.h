@@ -181,10 +181,13 @@ GQA_API int gqa_attn_decode(const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
  *                      gqa_attn_device_status.
  *   seqlens            device [B] int32, 0 <= seqlens[b] <= max_pages_per_seq *
  *                      page_size (clamped on the device).
- *   page_size          a positive multiple of 64 (else GQA_ERR_UNSUPPORTED).
+ *   page_size          a positive multiple of 64 (else GQA_ERR_UNSUPPORTED); a
+ *                      multiple of 128 where the tcgen05 split kernel runs
+ *                      (G > 8, or G * T_q > 32 rows in gqa_attn_decode_paged_multi),
+ *                      whose 128-key tiles must not straddle pages.
+ *   num_pages * H_kv   below 2^31 (else GQA_ERR_UNSUPPORTED).
  * Everything else, including the plan and the workspace size, is that of
- * gqa_attn_decode with S_max = max_pages_per_seq * page_size, except that G
- * must be <= 8 (the tcgen05 path serves dense caches only).
+ * gqa_attn_decode with S_max = max_pages_per_seq * page_size.
  */
 GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages,
                                   const gqa_bf16_t *v_pages, const int32_t *block_table,
@@ -192,6 +195,21 @@ GQA_API int gqa_attn_decode_paged(const gqa_bf16_t *q, const gqa_bf16_t *k_pages
                                   int num_pages, int page_size, int max_pages_per_seq, int d,
                                   float scale, int num_splits, gqa_bf16_t *o, float *lse,
                                   void *workspace, size_t ws_bytes, gqa_stream_t stream);
+
+/*
+ * Multi-token decode over a paged KV cache: the arguments of
+ * gqa_attn_decode_paged plus T_q, with q, o, lse and the token positions of
+ * gqa_attn_decode_multi (token t of sequence b at seqlens[b] - T_q + t).  The
+ * workspace is gqa_attn_decode_multi_workspace_size(B, H_q, H_kv, T_q,
+ * max_pages_per_seq * page_size, d, num_sms, num_splits) bytes.
+ */
+GQA_API int gqa_attn_decode_paged_multi(const gqa_bf16_t *q, const gqa_bf16_t *k_pages,
+                                        const gqa_bf16_t *v_pages, const int32_t *block_table,
+                                        const int32_t *seqlens, int B, int H_q, int H_kv,
+                                        int T_q, int num_pages, int page_size,
+                                        int max_pages_per_seq, int d, float scale,
+                                        int num_splits, gqa_bf16_t *o, float *lse,
+                                        void *workspace, size_t ws_bytes, gqa_stream_t stream);
 
 /*
  * Multi-token decode: T_q new tokens per sequence (speculative decoding

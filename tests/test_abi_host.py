@@ -247,11 +247,24 @@ def _raw_paged(lib, **kw):
     (dict(num_pages=0), gqa.GQA_ERR_INVALID_ARG),
     (dict(max_pages=-1), gqa.GQA_ERR_INVALID_ARG),
     (dict(d=64), gqa.GQA_ERR_UNSUPPORTED),
-    (dict(H_q=128, H_kv=8), gqa.GQA_ERR_UNSUPPORTED),          # G = 16: dense cache only
+    (dict(H_q=128, H_kv=8, page_size=64), gqa.GQA_ERR_UNSUPPORTED),  # G = 16 (tensor cores): 128-key pages
+    (dict(H_q=8, H_kv=8, num_pages=1 << 28), gqa.GQA_ERR_UNSUPPORTED),  # pool blocks >= 2^31
     (dict(B=0), gqa.GQA_OK),
 ])
 def test_paged_rejects_before_any_cuda_call(lib, kw, expect):
     assert _raw_paged(lib, **kw) == expect
+
+
+def test_paged_multi_rejections(lib):
+    v = ctypes.c_void_p
+    p = 1 << 20
+    call = lambda H_q, H_kv, T_q, page_size, B=1: lib.gqa_attn_decode_paged_multi(
+        v(p), v(p), v(p), v(p), v(p), B, H_q, H_kv, T_q, 64, page_size, 8, 128, 0.088, 0, v(p),
+        v(p), v(p), 1 << 30, v(0))
+    assert call(64, 8, 17, 256) == gqa.GQA_ERR_UNSUPPORTED   # G * T_q = 136 > 128
+    assert call(64, 8, 16, 64) == gqa.GQA_ERR_UNSUPPORTED    # tensor cores: 128-key pages
+    assert call(64, 8, 0, 256) == gqa.GQA_ERR_INVALID_ARG
+    assert call(64, 8, 16, 256, B=0) == gqa.GQA_OK
 
 
 def test_multi_token_rejections(lib):

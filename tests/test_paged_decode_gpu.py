@@ -127,3 +127,78 @@ def test_page_id_outside_pool_is_reported():
     v1 = torch.stack([torch.cat([vp[int(p)] for p in tcpu[1]], dim=1)])
     o_ref, lse_ref = oracle.decode(np64(q[1:]), np64(k1), np64(v1), sl.numpy()[1:], 0.1)
     compare(o[1:], l[1:], o_ref, lse_ref, "sequence with valid pages")
+
+
+# ---- paged cache on the tcgen05 split kernel and with T_q new tokens ----
+
+@pytest.mark.parametrize("H_q,H_kv,T_q,page_size,seqlens", [
+    (16, 2, 1, 128, [1000, 1024, 3]),     # G = 8 < rows: warp MMAs, one token (plain paged)
+    (16, 2, 4, 128, [1000, 130, 1024]),   # G * T_q = 32 rows: warp MMAs, wide variant
+    (16, 2, 16, 256, [1000, 17, 768]),    # 128 rows: tcgen05 kernel
+    (32, 2, 1, 128, [900, 1024, 5]),      # G = 16: tcgen05 kernel, one token
+    (48, 1, 2, 512, [1024, 300, 600]),    # G = 48, 96 rows, a 2-page sequence
+])
+def test_paged_multi_equals_dense_and_oracle(H_q, H_kv, T_q, page_size, seqlens):
+    B, S_max, d = 3, 1024, 128
+    q = gqa_synth.bf16_normal((B, H_q, T_q, d), 61, DEV)
+    _, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S_max, d, seed=62, device=DEV,
+                                          seqlens=seqlens)
+    sl_dev = sl.to(DEV)
+    kp, vp, table = to_pages(k, v, page_size, extra_pages=2, seed=page_size + T_q)
+    o_p, l_p = gqa.gqa_attn_decode_paged_multi(q, kp, vp, table, sl_dev, 0.088)
+    o_d, l_d = gqa.gqa_attn_decode_multi(q, k, v, sl_dev, 0.088)
+    torch.cuda.synchronize()
+    assert torch.equal(o_p, o_d) and torch.equal(l_p, l_d)
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 0.088)
+    compare(o_p, l_p, o_ref, lse_ref, f"paged multi G={H_q // H_kv} T_q={T_q} ps={page_size}")
+    if T_q == 1:   # the single-token entry point gives the same result
+        o1, l1 = gqa.gqa_attn_decode_paged(q[:, :, 0], kp, vp, table, sl_dev, 0.088)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o_p[:, :, 0]) and torch.equal(l1, l_p[:, :, 0])
+
+
+def test_paged_multi_llama70b_layer_16_tokens():
+    """Llama3-70B layer, 32K keys in 256-key pages, 16 new tokens (tcgen05 kernel)."""
+    w = gqa_synth.WORKLOADS["llama70b_decode_32k"]
+    q = gqa_synth.bf16_normal((1, w.H_q, 16, w.d), 63, DEV)
+    _, k, v, sl = gqa_synth.workload_decode_inputs(w, DEV)
+    kp, vp, table = to_pages(k, v, 256, extra_pages=0, seed=8)
+    o_p, l_p = gqa.gqa_attn_decode_paged_multi(q, kp, vp, table, sl.to(DEV), w.scale)
+    o_d, l_d = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o_p, o_d) and torch.equal(l_p, l_d)
+
+
+def test_paged_tensor_core_path_needs_128_key_pages():
+    """The tcgen05 kernel's 128-key tiles must not straddle pages: 64-key pages are
+    refused there (and still served by the warp-MMA kernel)."""
+    B, H_q, H_kv, T_q, S = 1, 16, 2, 16, 256
+    q = gqa_synth.bf16_normal((B, H_q, T_q, 128), 64, DEV)
+    _, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S, 128, seed=65, device=DEV)
+    kp, vp, table = to_pages(k, v, 64, extra_pages=0, seed=2)
+    with pytest.raises(gqa.GQAError) as e:
+        gqa.gqa_attn_decode_paged_multi(q, kp, vp, table, sl.to(DEV), 0.1)
+    assert e.value.status == gqa.GQA_ERR_UNSUPPORTED
+    o, l = gqa.gqa_attn_decode_paged_multi(q[:, :, :4].contiguous(), kp, vp, table, sl.to(DEV),
+                                           0.1)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q[:, :, :4]), np64(k), np64(v), sl.numpy(), 0.1)
+    compare(o, l, o_ref, lse_ref, "64-key pages, 32 rows")
+
+
+def test_page_id_outside_pool_is_reported_tensor_core_path():
+    B, H_q, H_kv, T_q, S, ps = 2, 16, 2, 16, 512, 128
+    q = gqa_synth.bf16_normal((B, H_q, T_q, 128), 66, DEV)
+    _, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S, 128, seed=67, device=DEV)
+    kp, vp, table = to_pages(k, v, ps, extra_pages=0, seed=4)
+    table[0, 2] = -7                                   # sequence 0, keys 256..383
+    assert gqa.gqa_attn_device_status() == gqa.GQA_OK
+    o, l = gqa.gqa_attn_decode_paged_multi(q, kp, vp, table, sl.to(DEV), 0.1)
+    torch.cuda.synchronize()
+    assert gqa.gqa_attn_device_status() == gqa.GQA_ERR_INVALID_ARG
+    assert torch.isfinite(o.float()).all()
+    tcpu = table.cpu()
+    k1 = torch.stack([torch.cat([kp[int(p)] for p in tcpu[1]], dim=1)])
+    v1 = torch.stack([torch.cat([vp[int(p)] for p in tcpu[1]], dim=1)])
+    o_ref, lse_ref = oracle.decode_multi(np64(q[1:]), np64(k1), np64(v1), sl.numpy()[1:], 0.1)
+    compare(o[1:], l[1:], o_ref, lse_ref, "sequence with valid pages (tensor cores)")
