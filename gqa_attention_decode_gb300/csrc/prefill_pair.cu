@@ -154,18 +154,28 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   }
 }
 
-// k-step kk (16 columns of d) of a Q tile: K-major, two 64-column halves of 128 rows.
-__device__ __forceinline__ uint64_t desc_q(uint32_t tile, int kk) {
-  return tc::smem_desc_sw128(tile + (kk >> 2) * kQHalfBytes + (kk & 3) * 32, 16, 1024);
+// Operand descriptors: built once per tile, then advanced by the k-step's byte
+// offset (a compile-time constant), which keeps the MMA thread's work between
+// tensor-core instructions to a single add.
+// Q tile: K-major, two 64-column halves of 128 rows; k-step kk = 16 columns of d.
+__device__ __forceinline__ uint64_t desc_q_base(uint32_t tile) {
+  return tc::smem_desc_sw128(tile, 16, 1024);
 }
-// k-step kk of a K half (64 keys): K-major, two 64-column halves of 64 rows.
-__device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk) {
-  return tc::smem_desc_sw128(tile + (kk >> 2) * kKHalfColBytes + (kk & 3) * 32, 16, 1024);
+__device__ __forceinline__ constexpr uint32_t q_step(int kk) {
+  return (kk >> 2) * kQHalfBytes + (kk & 3) * 32;
 }
-// k-step kk (16 keys) of a V half: MN-major, 128 key rows of 64 d (one 64-element block).
-__device__ __forceinline__ uint64_t desc_v(uint32_t tile, int kk) {
-  return tc::smem_desc_sw128(tile + kk * 2048, kStageBytes, 1024);
+// K half (64 keys): K-major, two 64-column halves of 64 rows.
+__device__ __forceinline__ uint64_t desc_k_base(uint32_t tile) {
+  return tc::smem_desc_sw128(tile, 16, 1024);
 }
+__device__ __forceinline__ constexpr uint32_t k_step(int kk) {
+  return (kk >> 2) * kKHalfColBytes + (kk & 3) * 32;
+}
+// V half: MN-major, 128 key rows of 64 d (one 64-element block); k-step kk = 16 keys.
+__device__ __forceinline__ uint64_t desc_v_base(uint32_t tile) {
+  return tc::smem_desc_sw128(tile, kStageBytes, 1024);
+}
+__device__ __forceinline__ constexpr uint32_t v_step(int kk) { return kk * 2048; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(2 * kBM, kD, 1);
       const uint32_t t_s[2] = {tmem + 0u, tmem + 128u};
       const uint32_t t_o[2] = {tmem + 256u, tmem + 384u};
-      const uint32_t q_smem[2] = {sbase + kOffQ, sbase + kOffQ + kQBytes};
+      const uint64_t dq0 = desc_q_base(sbase + kOffQ), dq1 = desc_q_base(sbase + kOffQ + kQBytes);
       int ld_base = 0, tile_base = 0, it = 0;
       bool ok = true;
       for (int k = 0; ok; ++k, ++it) {
@@ -295,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         for (int j = 0; ok && j <= n; ++j) {
           const int ldK = ld_base + 2 * j, ldV = ld_base + 2 * (j - 1) + 1;
-          const uint32_t k_smem = sbase + kOffStage + (ldK % kStages) * kStageBytes;
-          const uint32_t v_smem = sbase + kOffStage + (ldV % kStages) * kStageBytes;
+          const uint64_t dk = desc_k_base(sbase + kOffStage + (ldK % kStages) * kStageBytes);
+          const uint64_t dv = desc_v_base(sbase + kOffStage + (ldV % kStages) * kStageBytes);
           if (j < n && !wait_bar(kv_full(ldK % kStages), (ldK / kStages) & 1, p.wait, abort_flag)) {
             ok = false;
             break;
@@ -314,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::fence_after_sync();
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
-                tc::mma_ts_pair(t_o[i], t_s[i] + kk * 8, desc_v(v_smem, kk), idesc_pv,
+                tc::mma_ts_pair(t_o[i], t_s[i] + kk * 8, tc::desc_advance(dv, v_step(kk)), idesc_pv,
                                 (j > 1 || kk > 0) ? 1u : 0u);
               if (i == 1) tc::commit_pair(kv_empty(ldV % kStages), kBothCtas);
               if (j == n) tc::commit_pair(o_final(i), kBothCtas);
@@ -322,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j < n) {  // S_i = Q_i K_j^T
 #pragma unroll
               for (int kk = 0; kk < kD / 16; ++kk)
-                tc::mma_ss_pair(t_s[i], desc_q(q_smem[i], kk), desc_k(k_smem, kk), idesc_s,
-                                kk > 0 ? 1u : 0u);
+                tc::mma_ss_pair(t_s[i], tc::desc_advance(i == 0 ? dq0 : dq1, q_step(kk)),
+                                tc::desc_advance(dk, k_step(kk)), idesc_s, kk > 0 ? 1u : 0u);
               tc::commit_pair(s_full(i), kBothCtas);
               if (i == 1) {
                 tc::commit_pair(kv_empty(ldK % kStages), kBothCtas);

@@ -47,6 +47,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The descriptor of an operand `bytes` further on in shared memory: the start
+// address field (bits 0..13, address >> 4) advanced, the rest unchanged.  Valid
+// while the address stays below 256 KiB (no carry out of the field), which
+// holds for every shared-memory address of a CTA.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (bytes >> 4);
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16: bf16 A and B, fp32 accumulator,
 // dense, A K-major; B K-major (b_mn_major = 0) or MN-major (1).  N>>3 in bits
 // 17..22, M>>4 in bits 24..28.
