@@ -84,14 +84,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   }
 }
 
-// k-step kk of a K-major 128-row tile stored as two 128B-swizzled 64-column halves.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
-  return tc::smem_desc_sw128(tile + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+// Operand descriptors, built once per tile and advanced per k-step by a
+// compile-time byte offset.  K-major 128-row tile stored as two 128B-swizzled
+// 64-column halves (k-step kk = 16 columns); MN-major V tile (keys x d, d
+// contiguous in two halves; k-step kk = 16 keys).
+__device__ __forceinline__ uint64_t desc_kmajor_base(uint32_t tile) {
+  return tc::smem_desc_sw128(tile, 16, 1024);
 }
-// k-step kk (16 keys) of an MN-major V tile (keys x d, d contiguous in two halves).
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
-  return tc::smem_desc_sw128(tile + kk * 2048, kHalfBytes, 1024);
+__device__ __forceinline__ constexpr uint32_t kmajor_step(int kk) {
+  return (kk >> 2) * kHalfBytes + (kk & 3) * 32;
 }
+__device__ __forceinline__ uint64_t desc_mnmajor_base(uint32_t tile) {
+  return tc::smem_desc_sw128(tile, kHalfBytes, 1024);
+}
+__device__ __forceinline__ constexpr uint32_t mnmajor_step(int kk) { return kk * 2048; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -249,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, kD, 1);
       const uint32_t t_s[2] = {tmem + 0u, tmem + 128u};
       const uint32_t t_o[2] = {tmem + 256u, tmem + 384u};
+      const uint64_t dq = desc_kmajor_base(sbase + kOffQ);
       bool ok = wait_bar(q_full, 0, p.wait, abort_flag);
       tc::fence_after_sync();
       for (int j = 0; ok && j < n_tiles + 2; ++j) {
@@ -262,10 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::fence_after_sync();
-          const uint32_t v_smem = sbase + kOffStage + (ldV % kStages) * kTileBytes;
+          const uint64_t dv = desc_mnmajor_base(sbase + kOffStage + (ldV % kStages) * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            tc::mma_ts(t_o[s], t_s[s] + kk * 8, desc_mnmajor(v_smem, kk), idesc_pv,
+            tc::mma_ts(t_o[s], t_s[s] + kk * 8, tc::desc_advance(dv, mnmajor_step(kk)), idesc_pv,
                        (t >= 2 || kk > 0) ? 1u : 0u);
           tc::commit(kv_empty(ldV % kStages));
           if (t + 2 >= n_tiles) tc::commit(o_final(s));  // the slot's last tile
@@ -276,11 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t k_smem = sbase + kOffStage + (ldK % kStages) * kTileBytes;
+          const uint64_t dk = desc_kmajor_base(sbase + kOffStage + (ldK % kStages) * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
-            tc::mma_ss(t_s[s], desc_kmajor(sbase + kOffQ, kk), desc_kmajor(k_smem, kk), idesc_s,
-                       kk > 0 ? 1u : 0u);
+            tc::mma_ss(t_s[s], tc::desc_advance(dq, kmajor_step(kk)),
+                       tc::desc_advance(dk, kmajor_step(kk)), idesc_s, kk > 0 ? 1u : 0u);
           tc::commit(s_full(s));
           tc::commit(kv_empty(ldK % kStages));
         }

@@ -116,16 +116,22 @@ __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity, co
   }
 }
 
-// Descriptor of 16 consecutive K-columns (k-step kk) of a K-major 128x128 bf16 tile
-// stored as two 128B-swizzled 64-column halves.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
-  return tc::smem_desc_sw128(tile + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+// Operand descriptors, built once per tile and advanced per k-step by a
+// compile-time byte offset (one add between tensor-core instructions).
+// K-major 128x128 bf16 tile stored as two 128B-swizzled 64-column halves; k-step
+// kk = 16 consecutive K-columns.
+__device__ __forceinline__ uint64_t desc_kmajor_base(uint32_t tile) {
+  return tc::smem_desc_sw128(tile, 16, 1024);
 }
-// Descriptor of 16 consecutive K-rows (k-step kk) of an MN-major tile (V: keys x d,
-// d contiguous); the two 64-column halves are the two MN blocks (lbo).
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
-  return tc::smem_desc_sw128(tile + kk * 2048, kHalfBytes, 1024);
+__device__ __forceinline__ constexpr uint32_t kmajor_step(int kk) {
+  return (kk >> 2) * kHalfBytes + (kk & 3) * 32;
 }
+// MN-major tile (V: keys x d, d contiguous); the two 64-column halves are the two
+// MN blocks (lbo); k-step kk = 16 consecutive K-rows.
+__device__ __forceinline__ uint64_t desc_mnmajor_base(uint32_t tile) {
+  return tc::smem_desc_sw128(tile, kHalfBytes, 1024);
+}
+__device__ __forceinline__ constexpr uint32_t mnmajor_step(int kk) { return kk * 2048; }
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -229,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kBM, kD, 1);
       const uint32_t t_s[2] = {tmem + 0u, tmem + 128u};
       const uint32_t t_o[2] = {tmem + 256u, tmem + 384u};
-      const uint32_t q_smem[2] = {sbase + kOffQ, sbase + kOffQ + kTileBytes};
+      const uint64_t dq0 = desc_kmajor_base(sbase + kOffQ);
+      const uint64_t dq1 = desc_kmajor_base(sbase + kOffQ + kTileBytes);
       int ld_base = 0, tile_base = 0, it = 0;
       bool ok = true;
       for (int k = 0; ok; ++k, ++it) {
@@ -242,8 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         for (int j = 0; ok && j <= n; ++j) {
           const int ldK = ld_base + 2 * j, ldV = ld_base + 2 * (j - 1) + 1;
-          const uint32_t k_smem = sbase + kOffStage + (ldK % kStages) * kTileBytes;
-          const uint32_t v_smem = sbase + kOffStage + (ldV % kStages) * kTileBytes;
+          const uint64_t dk = desc_kmajor_base(sbase + kOffStage + (ldK % kStages) * kTileBytes);
+          const uint64_t dv = desc_mnmajor_base(sbase + kOffStage + (ldV % kStages) * kTileBytes);
           if (j < n) {
             if (!wait_abortable(kv_full(ldK % kStages), (ldK / kStages) & 1, p.wait, abort_flag)) {
               ok = false;
@@ -265,16 +272,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::fence_after_sync();
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
-                tc::mma_ts(t_o[i], t_s[i] + kk * 8, desc_mnmajor(v_smem, kk), idesc_pv,
-                           (j > 1 || kk > 0) ? 1u : 0u);
+                tc::mma_ts(t_o[i], t_s[i] + kk * 8, tc::desc_advance(dv, mnmajor_step(kk)),
+                           idesc_pv, (j > 1 || kk > 0) ? 1u : 0u);
               if (i == 1) tc::commit(kv_empty(ldV % kStages));
               if (j == n) tc::commit(o_final(i));
             }
             if (j < n) {  // S_i = Q_i K_j^T
 #pragma unroll
               for (int kk = 0; kk < kD / 16; ++kk)
-                tc::mma_ss(t_s[i], desc_kmajor(q_smem[i], kk), desc_kmajor(k_smem, kk), idesc_s,
-                           kk > 0 ? 1u : 0u);
+                tc::mma_ss(t_s[i], tc::desc_advance(i == 0 ? dq0 : dq1, kmajor_step(kk)),
+                           tc::desc_advance(dk, kmajor_step(kk)), idesc_s, kk > 0 ? 1u : 0u);
               tc::commit(s_full(i));
               if (i == 1) {
                 tc::commit(kv_empty(ldK % kStages));
