@@ -211,3 +211,30 @@ def test_out_of_range_seqlens_are_clamped_and_reported():
     o_ref, lse_ref = oracle.decode(np64(q), np64(k), np64(v), np.array([0, S]), 0.088)
     compare(o, lse, o_ref, lse_ref, "clamped seqlens")
     assert gqa.gqa_attn_device_status() == gqa.GQA_OK      # cleared by the read
+
+
+def test_one_million_keys_sampled():
+    """One sequence of 2^20 - 37 keys in a 2^20-key cache (Llama3-70B heads): each
+    of K and V is 2 GiB, so element offsets pass 2^31, and the plan cuts the keys
+    into hundreds of splits that the merge combines.  Sampled heads of the first
+    and the last KV head against the oracle."""
+    B, H_q, H_kv, S = 1, 64, 8, 1 << 20
+    n = S - 37
+    q, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S, 128, seed=71, device=DEV,
+                                          seqlens=[n])
+    splits, chunk = gqa.gqa_attn_decode_plan(B, H_kv, S, torch.cuda.get_device_properties(0)
+                                             .multi_processor_count, 0)
+    assert splits * chunk >= S and splits >= 256
+    o, lse = run_decode(q, k, v, sl, 1 / math.sqrt(128))
+    picks = [0, 5, 56, 63]                      # KV heads 0 and 7
+    ref_o = np.zeros((len(picks), 128))
+    ref_lse = np.zeros(len(picks))
+    for kv in (0, 7):
+        kk, vv = np64(k[0, kv, :n]), np64(v[0, kv, :n])
+        for i, h in enumerate(picks):
+            if h // 8 == kv:
+                ro, rl = oracle.attend_rows(np64(q[0, h])[None], kk, vv, 1 / math.sqrt(128), [n])
+                ref_o[i], ref_lse[i] = ro[0], rl[0]
+        del kk, vv
+    compare(torch.stack([o[0, h] for h in picks]), torch.stack([lse[0, h] for h in picks]),
+            ref_o, ref_lse, "2^20 keys")

@@ -283,3 +283,27 @@ def test_rejects_bad_q_offset_and_misalignment():
     with pytest.raises(gqa.GQAError) as e:
         gqa.gqa_attn_prefill_causal(q, k_off, v, 0.1)
     assert e.value.status == gqa.GQA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T_q,S_kv", [(256, 131072), (32768, 32768)])
+def test_long_context_sampled(T_q, S_kv):
+    """A 256-token chunk after 128K keys (32 units on the CTA pairs, each split by
+    key range) and a 32K square causal prefill; sampled rows against the oracle."""
+    B, H_q, H_kv = 1, 64, 8
+    q_offset = S_kv - T_q
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=72, device=DEV)
+    o, lse = run(q, k, v, q_offset, 1 / math.sqrt(128))
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(10)
+    rows = sorted({0, 127, 128, T_q - 1} | set(int(x) for x in rng.integers(0, T_q, 6)))
+    picks = [(0, int(rng.integers(0, H_q)), i) for i in rows]
+    ref_o = np.zeros((len(picks), 128))
+    ref_lse = np.zeros(len(picks))
+    for r, (b, h, i) in enumerate(picks):
+        n = q_offset + i + 1
+        ro, rl = oracle.attend_rows(np64(q[b, h, i])[None], np64(k[b, h // 8, :n]),
+                                    np64(v[b, h // 8, :n]), 1 / math.sqrt(128), [n])
+        ref_o[r], ref_lse[r] = ro[0], rl[0]
+    compare(torch.stack([o[b, h, i] for b, h, i in picks]),
+            torch.stack([lse[b, h, i] for b, h, i in picks]), ref_o, ref_lse,
+            f"T_q={T_q} after {q_offset}")
