@@ -52,6 +52,10 @@ constexpr int kStageBytes = 4 * kHalfBytes;          // K lo/hi + V lo/hi = 32 K
 #define GQA_DECODE_ONE_WAVE_STAGES 4
 #endif
 constexpr int kOneWaveStages = GQA_DECODE_ONE_WAVE_STAGES;
+// K/V tiles of its chunk a CTA prefetches into L2 before the grid-dependency wait
+#ifndef GQA_DECODE_L2_PREFETCH_TILES
+#define GQA_DECODE_L2_PREFETCH_TILES 3
+#endif
 template <int kStages>
 constexpr int smem_bytes() {
   return kStages * kStageBytes + 2 * kStages * 8 + 1024;  // ring + barriers + alignment slack
@@ -129,6 +133,19 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   if (warp == n_consumers && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    // Dense cache: pull the first tiles of this split's key range into L2 while
+    // the preceding grid finishes (its length is not known yet, so the range is
+    // the split's whole chunk; keys past the sequence are masked later).
+    if (!kPaged) {
+      const int tiles = min(GQA_DECODE_L2_PREFETCH_TILES, p.chunk / kTileKeys);
+      for (int i = 0; i < tiles; ++i) {
+        const int key0 = split * p.chunk + i * kTileKeys;
+        for (int half = 0; half < 2; ++half) {
+          tma_prefetch_l2_4d(&tm_k, 0, half, key0, b * p.H_kv + kv);
+          tma_prefetch_l2_4d(&tm_v, 0, half, key0, b * p.H_kv + kv);
+        }
+      }
+    }
   }
   // Inputs written by earlier grids are visible after this wait; they are read
   // with coherent loads (ld.global.ca), never the non-coherent read-only path.

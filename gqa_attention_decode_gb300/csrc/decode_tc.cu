@@ -125,6 +125,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Dense cache: the first key tile of this split's chunk is pulled into L2
+  // while the preceding grid finishes (L2 is the point of coherence, so this is
+  // safe ahead of the wait; the sequence length is not known yet).
+  if (p.block_table == nullptr && warp == kWarpTma && lane == 0 && p.chunk >= kBN) {
+    for (int half = 0; half < 2; ++half) {
+      tma_prefetch_l2_4d(&tm_k, 0, half, split * p.chunk, b * p.H_kv + kv);
+      tma_prefetch_l2_4d(&tm_v, 0, half, split * p.chunk, b * p.H_kv + kv);
+    }
+  }
   // inputs written by earlier grids are visible after this wait (coherent loads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int seqlen_in = __ldca(p.seqlens + b);

@@ -107,6 +107,17 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Prefetch of a tile into L2 (no shared memory, no completion to wait for).
+// Safe ahead of a grid-dependency wait: L2 is the point of coherence, so a later
+// write by the preceding grid still reaches every load that follows the wait.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int c0, int c1, int c2,
+                                                   int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // Tile load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA of a CTA pair (`bar` is a
 // shared::cluster address, e.g. from dsmem_addr).
