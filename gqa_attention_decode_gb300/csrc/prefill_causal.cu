@@ -65,13 +65,20 @@ struct Params {
   uint16_t *o;
   float *lse;
   int B, H_q, H_kv, G, T_q, S_kv, q_offset;
-  int n_qtiles, n_pairs, total_units;
+  int n_qtiles;
+  int n_hp;         // head pairs of a KV group that share a query tile: G / 2
+  int odd;          // G odd: the group's last head pairs two of its own query tiles
+  int total_units;
   float sl2;  // scale * log2(e)
   WaitCtl wait;
 };
 
+// Two slots of 128 query rows: slot i is query tile qt_i of head h_i.  Either
+// two heads of a KV group on one query tile, or (G odd) the group's last head
+// on query tiles qt and qt - 1, which read the same key tiles (the lower one
+// has its last key tile wholly in the future: masked, a tile of zeros).
 struct Unit {
-  int b, kv, qt, h0, h1, n_kv;
+  int b, kv, qt0, qt1, h0, h1, n_kv;
   bool second_valid;
 };
 
@@ -82,19 +89,39 @@ __device__ __forceinline__ int snake_unit(int k, int w, int P) {
   return k * P + ((k & 1) ? P - 1 - w : w);
 }
 
+// Units, longest first.  Query tiles are taken in ranks r = 0, 1, ... (tile
+// n_qtiles - 1 - r); rank r holds B * H_kv * n_hp head-pair units and, for even
+// r when G is odd, B * H_kv last-head units (tiles of ranks r and r + 1).
 __device__ __forceinline__ Unit unit_at(const Params &p, int u) {
   Unit w;
-  const int per_qt = p.B * p.H_kv * p.n_pairs;
-  w.qt = p.n_qtiles - 1 - u / per_qt;  // latest (longest) query tiles first
-  int r = u % per_qt;
-  const int pair = r % p.n_pairs;
-  r /= p.n_pairs;
-  w.kv = r % p.H_kv;
-  w.b = r / p.H_kv;
-  w.h0 = w.kv * p.G + 2 * pair;
-  w.second_valid = 2 * pair + 1 < p.G;
-  w.h1 = w.second_valid ? w.h0 + 1 : w.h0;
-  const int qe = min((w.qt + 1) * kBM, p.T_q);
+  const int bh = p.B * p.H_kv;
+  const int pn = bh * p.n_hp;                 // head-pair units per rank
+  const int two = 2 * pn + (p.odd ? bh : 0);  // units of ranks 2t and 2t + 1
+  const int t = u / two;
+  int idx = u % two, rank = 2 * t;
+  if (idx >= pn + (p.odd ? bh : 0)) {
+    idx -= pn + (p.odd ? bh : 0);
+    rank += 1;
+  }
+  w.qt0 = p.n_qtiles - 1 - rank;  // latest (longest) query tiles first
+  if (idx < pn) {                 // heads 2 hp and 2 hp + 1 of a group, one query tile
+    const int hp = idx % p.n_hp;
+    const int r = idx / p.n_hp;
+    w.kv = r % p.H_kv;
+    w.b = r / p.H_kv;
+    w.h0 = w.kv * p.G + 2 * hp;
+    w.h1 = w.h0 + 1;
+    w.qt1 = w.qt0;
+    w.second_valid = true;
+  } else {                        // the group's last head, query tiles qt0 and qt0 - 1
+    const int r = idx - pn;
+    w.kv = r % p.H_kv;
+    w.b = r / p.H_kv;
+    w.h0 = w.h1 = w.kv * p.G + p.G - 1;
+    w.second_valid = w.qt0 > 0;
+    w.qt1 = w.second_valid ? w.qt0 - 1 : w.qt0;
+  }
+  const int qe = min((w.qt0 + 1) * kBM, p.T_q);
   w.n_kv = (p.q_offset + qe - 1) / kBN + 1;
   return w;
 }
@@ -205,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dst = sbase + kOffQ + i * kTileBytes;
           mbar_arrive_expect_tx(q_full(i), kTileBytes);
           for (int half = 0; half < 2; ++half)
-            tma_load_4d(dst + half * kHalfBytes, &tm_q, q_full(i), 0, half, w.qt * kBM,
-                        w.b * p.H_q + h, pol_q);
+            tma_load_4d(dst + half * kHalfBytes, &tm_q, q_full(i), 0, half,
+                        (i == 0 ? w.qt0 : w.qt1) * kBM, w.b * p.H_q + h, pol_q);
         }
         for (int j = 0; ok && j < w.n_kv; ++j) {
           for (int which = 0; which < 2; ++which, ++ld) {
@@ -313,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = snake_unit(k, blockIdx.x, gridDim.x);
       if (u >= p.total_units) break;
       const Unit w = unit_at(p, u);
-      const int q0 = p.q_offset + w.qt * kBM;  // absolute position of row 0 of the tile
+      const int qt = i == 0 ? w.qt0 : w.qt1;
+      const int q0 = p.q_offset + qt * kBM;  // absolute position of row 0 of the tile
       const int qpos = q0 + row;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < w.n_kv; ++j, ++tile) {
@@ -460,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
       tc::fence_after_sync();
       const int h = i == 0 ? w.h0 : w.h1;
-      const int qrow = w.qt * kBM + row;
+      const int qrow = qt * kBM + row;
       const bool store = (i == 0 || w.second_valid) && qrow < p.T_q;
       const size_t orow = ((size_t)w.b * p.H_q + h) * p.T_q + qrow;
       uint32_t ov[kD];
@@ -535,8 +563,11 @@ cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
   p.S_kv = a.S_kv;
   p.q_offset = a.q_offset;
   p.n_qtiles = (a.T_q + kBM - 1) / kBM;
-  p.n_pairs = (p.G + 1) / 2;
-  const long long units = (long long)p.n_qtiles * a.B * a.H_kv * p.n_pairs;
+  p.n_hp = p.G / 2;
+  p.odd = p.G & 1;
+  const long long bh = (long long)a.B * a.H_kv;
+  const long long units =
+      (long long)p.n_qtiles * bh * p.n_hp + (p.odd ? bh * ((p.n_qtiles + 1) / 2) : 0);
   if (units > 0x7fffffffLL) return cudaErrorNotSupported;
   p.total_units = (int)units;
   p.sl2 = a.scale * 1.4426950408889634f;

@@ -53,6 +53,9 @@ def run(q, k, v, q_offset, scale):
     (1, 16, 2, 384, 384, 0),      # exact multiple of the tile
     (2, 8, 2, 300, 1000, 700),    # G = 4: one head quad per KV head, two sequences
     (1, 12, 1, 200, 200, 0),      # G = 12: three head quads
+    (1, 10, 2, 520, 600, 80),     # G = 5: the last head of a group over query tiles 4+3, 2+1, 0
+    (2, 7, 1, 384, 384, 0),       # G = 7, three query tiles: last head over tiles 2+1, then 0
+    (1, 3, 3, 257, 257, 0),       # G = 1 (MHA), query tiles 2+1, then 0 (ragged)
 ])
 def test_small_cases_full_compare(B, H_q, H_kv, T_q, S_kv, q_offset):
     q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=31, device=DEV)
