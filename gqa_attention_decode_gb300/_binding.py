@@ -391,11 +391,11 @@ def gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, d, q_offset,
                                                                       q_offset, num_sms))
 
 
-def gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, d, q_offset, num_pairs, ws_bytes):
-    """Host-only work plan of the CTA-pair prefill: (units, split units, pieces per unit)."""
+def gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, d, q_offset, num_sms, ws_bytes):
+    """Host-only prefill work plan on `num_sms` SMs: (units, split units, pieces per unit)."""
     u, su, ps = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     rc = load_library().gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, d, q_offset,
-                                                     num_pairs, ws_bytes, ctypes.byref(u),
+                                                     num_sms, ws_bytes, ctypes.byref(u),
                                                      ctypes.byref(su), ctypes.byref(ps))
     _check(rc, "gqa_attn_prefill_causal_plan")
     return u.value, su.value, ps.value

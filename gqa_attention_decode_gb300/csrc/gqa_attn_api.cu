@@ -459,23 +459,27 @@ GQA_API size_t gqa_attn_prefill_causal_workspace_size(int B, int H_q, int H_kv, 
   if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0 ||
       num_sms <= 0 || H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
     return 0;
-  if ((H_q / H_kv) % 4 != 0) return 0;  // one CTA per unit: never split
-  const long long units = (long long)((T_q + 127) / 128) * B * H_kv * (H_q / H_kv / 4);
-  const size_t bytes = gqa::prefill_pair_workspace_bound(units, num_sms);
+  const int G = H_q / H_kv;
+  // the CTA-pair kernel's units (G % 4 == 0), else the single-CTA kernel's
+  const size_t bytes =
+      G % 4 == 0
+          ? gqa::prefill_pair_workspace_bound((long long)((T_q + 127) / 128) * B * H_kv * (G / 4),
+                                              num_sms)
+          : gqa::prefill_workspace_bound(gqa::prefill_units(B, H_q, H_kv, T_q), num_sms);
   return (bytes + 255) / 256 * 256;
 }
 
 GQA_API int gqa_attn_prefill_causal_plan(int B, int H_q, int H_kv, int T_q, int S_kv, int d,
-                                         int q_offset, int num_pairs, size_t ws_bytes,
+                                         int q_offset, int num_sms, size_t ws_bytes,
                                          int *out_units, int *out_split_units,
                                          int *out_pieces_per_unit) {
   if (!out_units || !out_split_units || !out_pieces_per_unit) return GQA_ERR_INVALID_ARG;
   if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0 ||
-      num_pairs <= 0 || H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
+      num_sms < 2 || H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
     return GQA_ERR_INVALID_ARG;
   *out_units = *out_split_units = 0;
   *out_pieces_per_unit = 1;
-  if ((H_q / H_kv) % 4 != 0 || B == 0 || T_q == 0) return GQA_OK;
+  if (B == 0 || T_q == 0) return GQA_OK;
   gqa::PrefillLaunch a = {};
   a.B = B;
   a.H_q = H_q;
@@ -483,10 +487,12 @@ GQA_API int gqa_attn_prefill_causal_plan(int B, int H_q, int H_kv, int T_q, int 
   a.T_q = T_q;
   a.S_kv = S_kv;
   a.q_offset = q_offset;
-  a.max_pairs = num_pairs;
+  a.num_sms = num_sms;
+  a.max_pairs = num_sms / 2;  // one CTA per SM
   a.ws = ws_bytes > 0 ? reinterpret_cast<void *>(uintptr_t(256)) : nullptr;  // size decides
   a.ws_bytes = ws_bytes;
-  const gqa::PrefillPairPlan pl = gqa::prefill_pair_plan(a);
+  const gqa::PrefillPlan pl =
+      gqa::prefill_pair_eligible(a) ? gqa::prefill_pair_plan(a) : gqa::prefill_plan(a);
   *out_units = pl.units;
   *out_split_units = pl.units - pl.n_full;
   *out_pieces_per_unit = pl.split_s;
@@ -541,7 +547,9 @@ GQA_API int gqa_attn_prefill_causal_kernel_count(int B, int H_q, int H_kv, int T
   const gqa::PrefillLaunch a = prefill_launch_args(nullptr, nullptr, nullptr, B, H_q, H_kv, T_q,
                                                    S_kv, q_offset, 1.f, nullptr, nullptr, ws,
                                                    ws_bytes, st);
-  *out_kernels = gqa::prefill_pair_eligible(a) && gqa::prefill_pair_plan(a).pieces > 0 ? 2 : 1;
+  const gqa::PrefillPlan pl =
+      gqa::prefill_pair_eligible(a) ? gqa::prefill_pair_plan(a) : gqa::prefill_plan(a);
+  *out_kernels = pl.pieces > 0 ? 2 : 1;
   return GQA_OK;
 }
 

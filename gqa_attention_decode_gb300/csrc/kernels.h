@@ -77,24 +77,28 @@ struct PrefillLaunch {
   WaitCtl wait;
 };
 
-// CTA-pair kernel work plan (host only).
-struct PrefillPairPlan {
-  int units = 0;    // 128-row query tiles x head quads
+// Work plan of a prefill launch (host only): units of 128 query rows dealt in
+// rounds over the resident workers (CTAs or CTA pairs); the units of a partial
+// last round may be cut into key-range pieces merged afterwards.
+struct PrefillPlan {
+  int units = 0;    // work units
   int n_full = 0;   // units run whole
   int split_s = 1;  // pieces per split unit
   int pieces = 0;   // (units - n_full) * split_s
   int n_items = 0;  // n_full + pieces
-  int n_pairs = 0;  // clusters launched
+  int workers = 0;  // CTAs (or CTA pairs) launched
 };
-
 // Single-CTA kernel (any group size).
 cudaError_t prefill_prepare_device();
+PrefillPlan prefill_plan(const PrefillLaunch &a);
+size_t prefill_workspace_bound(long long units, int num_sms);
+long long prefill_units(int B, int H_q, int H_kv, int T_q);
 cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
                            PFN_cuTensorMapEncodeTiled_v12000 encode);
 // CTA-pair kernel (tcgen05 cta_group::2), for group sizes that are multiples of 4.
 cudaError_t prefill_pair_prepare_device(int *max_pairs);
 bool prefill_pair_eligible(const PrefillLaunch &a);
-PrefillPairPlan prefill_pair_plan(const PrefillLaunch &a);
+PrefillPlan prefill_pair_plan(const PrefillLaunch &a);
 // Workspace that lets every partial round split (at most one piece per pair).
 size_t prefill_pair_workspace_bound(long long units, int num_sms);
 cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,

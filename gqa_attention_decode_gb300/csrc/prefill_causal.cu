@@ -36,6 +36,7 @@
 
 #include "device_common.cuh"
 #include "kernels.h"
+#include "prefill_split.cuh"
 #include "tcgen05.cuh"
 
 namespace gqa {
@@ -68,7 +69,12 @@ struct Params {
   int n_qtiles;
   int n_hp;         // head pairs of a KV group that share a query tile: G / 2
   int odd;          // G odd: the group's last head pairs two of its own query tiles
-  int total_units;
+  // Items dealt to the CTAs: [0, n_full) whole units; the units after them
+  // cut into split_s key-range pieces (item n_full + t is piece t), whose
+  // partials go to ws_o / ws_ml and are combined by the merge kernel.
+  int n_items, n_full, split_s;
+  float *ws_o;   // [piece][2 slots][128 rows][128] fp32, O not yet divided by l
+  float *ws_ml;  // [piece][2 slots][128 rows][2] fp32: m (log2 units), l
   float sl2;  // scale * log2(e)
   WaitCtl wait;
 };
@@ -80,6 +86,8 @@ struct Params {
 struct Unit {
   int b, kv, qt0, qt1, h0, h1, n_kv;
   bool second_valid;
+  int kv_lo, kv_hi;  // key tiles of this item: [kv_lo, kv_hi)
+  int piece;         // -1: a whole unit, O and lse final; else its partial slot
 };
 
 // Unit of round k for worker w of P: units are sorted longest first and dealt
@@ -92,8 +100,15 @@ __device__ __forceinline__ int snake_unit(int k, int w, int P) {
 // Units, longest first.  Query tiles are taken in ranks r = 0, 1, ... (tile
 // n_qtiles - 1 - r); rank r holds B * H_kv * n_hp head-pair units and, for even
 // r when G is odd, B * H_kv last-head units (tiles of ranks r and r + 1).
-__device__ __forceinline__ Unit unit_at(const Params &p, int u) {
+__device__ __forceinline__ Unit unit_at(const Params &p, int item) {
   Unit w;
+  int u = item;
+  w.piece = -1;
+  if (item >= p.n_full) {
+    const int t = item - p.n_full;
+    u = p.n_full + t / p.split_s;
+    w.piece = t;
+  }
   const int bh = p.B * p.H_kv;
   const int pn = bh * p.n_hp;                 // head-pair units per rank
   const int two = 2 * pn + (p.odd ? bh : 0);  // units of ranks 2t and 2t + 1
@@ -123,7 +138,25 @@ __device__ __forceinline__ Unit unit_at(const Params &p, int u) {
   }
   const int qe = min((w.qt0 + 1) * kBM, p.T_q);
   w.n_kv = (p.q_offset + qe - 1) / kBN + 1;
+  w.kv_lo = 0;
+  w.kv_hi = w.n_kv;
+  if (w.piece >= 0) {
+    const int i = w.piece % p.split_s;
+    w.kv_lo = prefill_split::piece_start(i, p.split_s, w.n_kv);
+    w.kv_hi = prefill_split::piece_start(i + 1, p.split_s, w.n_kv);
+  }
   return w;
+}
+
+// Output row of slot hl of work item `item`, row `row` (false: not stored).
+__device__ __forceinline__ bool piece_out_row(const Params &p, int item, int hl, int row,
+                                              size_t *orow) {
+  const Unit w = unit_at(p, item);
+  if (hl == 1 && !w.second_valid) return false;
+  const int qrow = (hl == 0 ? w.qt0 : w.qt1) * kBM + row;
+  if (qrow >= p.T_q) return false;
+  *orow = ((size_t)w.b * p.H_q + (hl == 0 ? w.h0 : w.h1)) * p.T_q + qrow;
+  return true;
 }
 
 __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity, const WaitCtl &ctl,
@@ -224,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int k = 0; ok; ++k, ++it) {
         const int u = snake_unit(k, blockIdx.x, gridDim.x);
-        if (u >= p.total_units) break;
+        if (u >= p.n_items) break;
         const Unit w = unit_at(p, u);
         if (!wait_abortable(q_empty, (it & 1) ^ 1, p.wait, abort_flag)) { ok = false; break; }
         for (int i = 0; i < 2; ++i) {
@@ -235,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(dst + half * kHalfBytes, &tm_q, q_full(i), 0, half,
                         (i == 0 ? w.qt0 : w.qt1) * kBM, w.b * p.H_q + h, pol_q);
         }
-        for (int j = 0; ok && j < w.n_kv; ++j) {
+        for (int j = w.kv_lo; ok && j < w.kv_hi; ++j) {
           for (int which = 0; which < 2; ++which, ++ld) {
             const int s = ld % kStages;
             if (!wait_abortable(kv_empty(s), ((ld / kStages) & 1) ^ 1, p.wait, abort_flag)) {
@@ -268,9 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int k = 0; ok; ++k, ++it) {
         const int u = snake_unit(k, blockIdx.x, gridDim.x);
-        if (u >= p.total_units) break;
+        if (u >= p.n_items) break;
         const Unit w = unit_at(p, u);
-        const int n = w.n_kv;
+        const int n = w.kv_hi - w.kv_lo;
         for (int i = 0; ok && i < 2; ++i)
           if (!wait_abortable(q_full(i), it & 1, p.wait, abort_flag)) ok = false;
         tc::fence_after_sync();
@@ -338,13 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = 0; ok; ++k, ++it) {
       const int u = snake_unit(k, blockIdx.x, gridDim.x);
-      if (u >= p.total_units) break;
+      if (u >= p.n_items) break;
       const Unit w = unit_at(p, u);
       const int qt = i == 0 ? w.qt0 : w.qt1;
       const int q0 = p.q_offset + qt * kBM;  // absolute position of row 0 of the tile
       const int qpos = q0 + row;
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < w.n_kv; ++j, ++tile) {
+      for (int j = w.kv_lo; j < w.kv_hi; ++j, ++tile) {
         bool ready = wait_abortable(s_full(i), tile & 1, p.wait, abort_flag);
         if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
         tc::fence_after_sync();
@@ -428,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) prep(sv + 32 * c, c);
-        if (j == 0) {  // key 0 is visible to every row: finite
+        if (j == w.kv_lo) {  // its first key is visible to every row: finite
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int e = 0; e < kBN; e += 8)
@@ -453,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The reference max only moves when a score exceeds it by more than the
         // threshold; such a score alone makes the tile's sum exceed 2^threshold,
         // so the row max is computed only when a sum does (or is not finite).
-        if (j > 0 && __any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
+        if (j > w.kv_lo && __any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
           const float mt = row_max();  // S is still in tensor memory (P not yet written)
           if (__any_sync(0xffffffffu, mt > m_ref + kRescaleThreshold)) {
             const float m_new = fmaxf(m_ref, mt);
@@ -495,7 +528,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) tc::ld32(t_o + 32 * c, ov + 32 * c);
       tc::wait_ld();
-      if (store) {
+      if (store && w.piece >= 0) {
+        // a piece of a split unit: its partial (O not yet divided, m, l) for the merge
+        const size_t prow = prefill_split::partial_row(w.piece, 2, i, row);
+        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * kD);
+#pragma unroll
+        for (int v4 = 0; v4 < kD / 4; ++v4)
+          dst[v4] = make_float4(__uint_as_float(ov[4 * v4 + 0]), __uint_as_float(ov[4 * v4 + 1]),
+                                __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+        reinterpret_cast<float2 *>(p.ws_ml)[prow] = make_float2(m_ref, l);
+      } else if (store) {
         const float inv_l = 1.f / l;
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD);
 #pragma unroll
@@ -544,9 +586,32 @@ cudaError_t prefill_prepare_device() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, prefill::kSmemBytes);
 }
 
+long long prefill_units(int B, int H_q, int H_kv, int T_q) {
+  using namespace prefill;
+  const int G = H_q / H_kv;
+  const long long n_qtiles = (T_q + kBM - 1) / kBM;
+  const long long bh = (long long)B * H_kv;
+  return n_qtiles * bh * (G / 2) + ((G & 1) ? bh * ((n_qtiles + 1) / 2) : 0);
+}
+
+// Work plan: one CTA per SM; units longest first (the shortest are those of
+// query tile 0); with a workspace, the last round's units may be split.
+PrefillPlan prefill_plan(const PrefillLaunch &a) {
+  using namespace prefill;
+  const long long units = prefill_units(a.B, a.H_q, a.H_kv, a.T_q);
+  const int n_kv_min = (a.q_offset + (a.T_q < kBM ? a.T_q : kBM) - 1) / kBN + 1;
+  return prefill_split::make_plan(units, a.num_sms, n_kv_min, 2, a.ws, a.ws_bytes);
+}
+
+size_t prefill_workspace_bound(long long units, int num_sms) {
+  return prefill_split::workspace_bound(units, num_sms, 2);
+}
+
 cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
                            PFN_cuTensorMapEncodeTiled_v12000 encode) {
   using namespace prefill;
+  const PrefillPlan pl = prefill_plan(a);
+  if (pl.units <= 0) return cudaErrorNotSupported;
   CUtensorMap tm_q, tm_k, tm_v;
   if (make_map(&tm_q, a.q, a.T_q, a.B * a.H_q, encode) != CUDA_SUCCESS ||
       make_map(&tm_k, a.k, a.S_kv, a.B * a.H_kv, encode) != CUDA_SUCCESS ||
@@ -565,16 +630,18 @@ cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
   p.n_qtiles = (a.T_q + kBM - 1) / kBM;
   p.n_hp = p.G / 2;
   p.odd = p.G & 1;
-  const long long bh = (long long)a.B * a.H_kv;
-  const long long units =
-      (long long)p.n_qtiles * bh * p.n_hp + (p.odd ? bh * ((p.n_qtiles + 1) / 2) : 0);
-  if (units > 0x7fffffffLL) return cudaErrorNotSupported;
-  p.total_units = (int)units;
+  p.n_items = pl.n_items;
+  p.n_full = pl.n_full;
+  p.split_s = pl.split_s;
+  p.ws_o = pl.pieces > 0 ? static_cast<float *>(a.ws) : nullptr;
+  p.ws_ml = pl.pieces > 0 ? p.ws_o + (size_t)pl.pieces * 2 * kBM * kD : nullptr;
   p.sl2 = a.scale * 1.4426950408889634f;
   p.wait = a.wait;
-  const int grid = (int)(units < a.num_sms ? units : a.num_sms);
-  prefill_causal_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
-  return cudaGetLastError();
+  prefill_causal_kernel<<<pl.workers, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the pieces' merge, a programmatic dependent of the prefill kernel
+  return prefill_split::launch_merge<2>(p, pl, stream);
 }
 
 }  // namespace gqa

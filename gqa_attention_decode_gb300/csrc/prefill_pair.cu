@@ -36,6 +36,7 @@
 
 #include "device_common.cuh"
 #include "kernels.h"
+#include "prefill_split.cuh"
 #include "tcgen05.cuh"
 
 namespace gqa {
@@ -95,13 +96,6 @@ __device__ __forceinline__ int snake_unit(int k, int w, int P) {
   return k * P + ((k & 1) ? P - 1 - w : w);
 }
 
-// Key tile where piece i of s of an n-tile range starts.  With at least two
-// tiles per piece every piece but the first starts at or before the tile of
-// the unit's first query row, so its first tile has a visible key in every row.
-__host__ __device__ __forceinline__ int piece_start(int i, int s, int n) {
-  return (int)((long long)i * n / s);
-}
-
 __device__ __forceinline__ Unit unit_at(const Params &p, int item) {
   Unit w;
   int u = item;
@@ -124,8 +118,8 @@ __device__ __forceinline__ Unit unit_at(const Params &p, int item) {
   w.kv_hi = w.n_kv;
   if (w.piece >= 0) {
     const int i = w.piece % p.split_s;
-    w.kv_lo = piece_start(i, p.split_s, w.n_kv);
-    w.kv_hi = piece_start(i + 1, p.split_s, w.n_kv);
+    w.kv_lo = prefill_split::piece_start(i, p.split_s, w.n_kv);
+    w.kv_hi = prefill_split::piece_start(i + 1, p.split_s, w.n_kv);
   }
   return w;
 }
@@ -538,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::wait_ld();
       if (qrow < p.T_q && w.piece >= 0) {
         // a piece of a split unit: its partial (O not yet divided, m, l) for the merge
-        const size_t prow = ((size_t)w.piece * 4 + 2 * i + rank) * kBM + row;
+        const size_t prow = prefill_split::partial_row(w.piece, 4, 2 * i + rank, row);
         float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * kD);
 #pragma unroll
         for (int v4 = 0; v4 < kD / 4; ++v4)
@@ -575,63 +569,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge of a split unit's pieces (the log-sum-exp combination of partial
-// softmax states), one warp per (split unit, head, query row):
-//   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,
-//   O = sum_i 2^(m_i - M) O_i / L,  lse = M ln 2 + ln L.
-// Lane i < s reads piece i's (m, l); every lane owns 4 of the 128 columns.
-// Launched as a programmatic dependent of the pair kernel: the partials are
-// read through L2 after the grid-dependency wait.
-constexpr int kMergeThreads = 256;
-constexpr int kMaxPieces = 32;      // pieces per unit (one lane each in the merge)
-constexpr int kMinPieceTiles = 8;   // key tiles per piece at least
-constexpr size_t kPieceBytes = (size_t)4 * kBM * (kD + 2) * sizeof(float);
-
-__global__ void __launch_bounds__(kMergeThreads) prefill_pair_merge_kernel(const Params p) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
-  const int row = gw % kBM;
-  const int hl = (gw / kBM) % 4;  // head within the unit: 2 * slot + rank
-  const int su = gw / (4 * kBM);  // split unit
-  const int s = p.split_s;
-  if (su >= (p.n_items - p.n_full) / s) return;
-  const Unit w = unit_at(p, p.n_full + su * s);
+// Output row of head slot hl (2 * slot + rank) of work item `item`, row `row`.
+__device__ __forceinline__ bool piece_out_row(const Params &p, int item, int hl, int row,
+                                              size_t *orow) {
+  const Unit w = unit_at(p, item);
   const int qrow = w.qt * kBM + row;
-  if (qrow >= p.T_q) return;
-  const int h = head_of(p, w, hl & 1, hl >> 1);
-  const size_t orow = ((size_t)w.b * p.H_q + h) * p.T_q + qrow;
-  auto prow = [&](int i) { return ((size_t)(su * s + i) * 4 + hl) * kBM + row; };
-  float m = -INFINITY, l = 0.f;
-  if (lane < s) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml) + prow(lane));
-    m = ml.x;
-    l = ml.y;
-  }
-  float M = m;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  const float wgt = m > -INFINITY ? fast_exp2(m - M) : 0.f;
-  float L = wgt * l;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int i = 0; i < s; ++i) {
-    const float wi = __shfl_sync(0xffffffffu, wgt, i);
-    const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + prow(i) * kD) + lane);
-    acc.x = fmaf(wi, x.x, acc.x);
-    acc.y = fmaf(wi, x.y, acc.y);
-    acc.z = fmaf(wi, x.z, acc.z);
-    acc.w = fmaf(wi, x.w, acc.w);
-  }
-  const float inv_l = L > 0.f ? 1.f / L : 0.f;
-  uint2 pk;
-  pk.x = pack_bf16x2(acc.x * inv_l, acc.y * inv_l);
-  pk.y = pack_bf16x2(acc.z * inv_l, acc.w * inv_l);
-  reinterpret_cast<uint2 *>(p.o + orow * kD)[lane] = pk;
-  if (lane == 0) p.lse[orow] = L > 0.f ? M * 0.69314718055994531f + logf(L) : -INFINITY;
+  if (qrow >= p.T_q) return false;
+  *orow = ((size_t)w.b * p.H_q + head_of(p, w, hl & 1, hl >> 1)) * p.T_q + qrow;
+  return true;
 }
 
 // dims (innermost first): 64 columns, 2 column halves, rows, heads; box of
@@ -677,52 +622,27 @@ bool prefill_pair_eligible(const PrefillLaunch &a) {
   return a.H_kv > 0 && (a.H_q / a.H_kv) % 4 == 0 && a.max_pairs > 0;
 }
 
-// Work plan: units of one 128-row query tile of four heads; with a workspace,
-// the units of the last, partial round (all units when there are fewer than
-// pairs) are cut into pieces of contiguous key tiles so the round fills the
-// pairs.  Pieces per unit: pairs / such units, at most kMaxPieces, at least
-// kMinPieceTiles tiles each (the shortest unit is the one of query tile 0).
-PrefillPairPlan prefill_pair_plan(const PrefillLaunch &a) {
+// Work plan: units of one 128-row query tile of four heads over the resident
+// CTA pairs; with a workspace, the last round's units may be split by key range
+// (the shortest unit is the one of query tile 0).
+PrefillPlan prefill_pair_plan(const PrefillLaunch &a) {
   using namespace prefill_pair;
-  PrefillPairPlan pl;
   const int G = a.H_q / a.H_kv;
   const int n_qtiles = (a.T_q + kBM - 1) / kBM;
   const long long units = (long long)n_qtiles * a.B * a.H_kv * (G / 4);
-  if (units <= 0 || units > 0x7fffffffLL || a.max_pairs <= 0) return pl;
-  const int U = (int)units, P = a.max_pairs;
-  pl.units = U;
-  pl.n_full = U;
-  pl.split_s = 1;
-  const int r = U % P;  // units of the last round
-  if (a.ws != nullptr && r > 0) {
-    const int n_kv_min = (a.q_offset + (a.T_q < kBM ? a.T_q : kBM) - 1) / kBN + 1;
-    int sp = P / r;
-    if (sp > kMaxPieces) sp = kMaxPieces;
-    if (sp > n_kv_min / kMinPieceTiles) sp = n_kv_min / kMinPieceTiles;
-    if (sp >= 2 && (size_t)r * sp * kPieceBytes <= a.ws_bytes) {
-      pl.n_full = U - r;
-      pl.split_s = sp;
-    }
-  }
-  pl.pieces = (U - pl.n_full) * pl.split_s;
-  pl.n_items = pl.n_full + pl.pieces;
-  pl.n_pairs = pl.n_items < P ? pl.n_items : P;
-  return pl;
+  const int n_kv_min = (a.q_offset + (a.T_q < kBM ? a.T_q : kBM) - 1) / kBN + 1;
+  return prefill_split::make_plan(units, a.max_pairs, n_kv_min, 4, a.ws, a.ws_bytes);
 }
 
 size_t prefill_pair_workspace_bound(long long units, int num_sms) {
-  using namespace prefill_pair;
-  // never more pieces than pairs, nor than kMaxPieces per unit
-  const long long pairs = num_sms / 2, most = units * kMaxPieces;
-  const long long pieces = most < pairs ? most : pairs;
-  return pieces > 0 ? (size_t)pieces * kPieceBytes : 0;
+  return prefill_split::workspace_bound(units, num_sms / 2, 4);
 }
 
 cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
                                 PFN_cuTensorMapEncodeTiled_v12000 encode) {
   using namespace prefill_pair;
   if (!prefill_pair_eligible(a)) return cudaErrorNotSupported;
-  const PrefillPairPlan pl = prefill_pair_plan(a);
+  const PrefillPlan pl = prefill_pair_plan(a);
   if (pl.units <= 0) return cudaErrorNotSupported;
   CUtensorMap tm_q, tm_k, tm_v;
   if (make_map(&tm_q, a.q, a.T_q, a.B * a.H_q, kBM, encode) != CUDA_SUCCESS ||
@@ -742,7 +662,7 @@ cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
   p.n_qtiles = (a.T_q + kBM - 1) / kBM;
   p.n_quads = p.G / 4;
   p.n_items = pl.n_items;
-  p.n_pairs = pl.n_pairs;
+  p.n_pairs = pl.workers;
   p.n_full = pl.n_full;
   p.split_s = pl.split_s;
   p.ws_o = pl.pieces > 0 ? static_cast<float *>(a.ws) : nullptr;
@@ -762,19 +682,9 @@ cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tm_q, tm_k, tm_v, p);
-  if (e != cudaSuccess || pl.pieces == 0) return e;
+  if (e != cudaSuccess) return e;
   // the pieces' merge, a programmatic dependent of the pair kernel
-  const long long warps = (long long)(pl.pieces / pl.split_s) * 4 * kBM;
-  cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3((unsigned)((warps + kMergeThreads / 32 - 1) / (kMergeThreads / 32)), 1, 1);
-  mcfg.blockDim = dim3(kMergeThreads, 1, 1);
-  mcfg.stream = stream;
-  cudaLaunchAttribute mattr[1];
-  mattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  mattr[0].val.programmaticStreamSerializationAllowed = 1;
-  mcfg.attrs = mattr;
-  mcfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&mcfg, prefill_pair_merge_kernel, p);
+  return prefill_split::launch_merge<4>(p, pl, stream);
 }
 
 }  // namespace gqa

@@ -327,34 +327,34 @@ GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
 
 /*
  * Bytes of device workspace that let gqa_attn_prefill_causal_ws split key
- * ranges (host only, no CUDA call).  Work is dealt in rounds of units (a
- * 128-row query tile of four heads of a KV group) over the device's CTA
- * pairs; when the last round is partial -- or there are fewer units than
- * pairs, as for a short chunk after a long prefix -- its units are cut into
- * pieces of contiguous key tiles (at least 8 tiles each, at most one piece per
- * pair), each piece's partial softmax state (O before division, m, l) goes to
+ * ranges (host only, no CUDA call).  Work is dealt in rounds of units (128
+ * query rows of four heads of a KV group on a CTA pair when G is a multiple of
+ * 4, else of two 128-row slots on one CTA) over the device's resident workers;
+ * when the last round is partial -- or there are fewer units than workers, as
+ * for a short chunk after a long prefix -- its units are cut into pieces of
+ * contiguous key tiles (at least 8 tiles each, at most 32 per unit and one per
+ * worker), each piece's partial softmax state (O before division, m, l) goes to
  * the workspace and a log-sum-exp merge kernel combines them: the record's
  * split-and-reduce (sections 2.2 and 4) applied to prefill.  The bound is one
- * piece per pair, at most 32 per unit: min(32 * units, num_sms / 2) * 266240
- * bytes, rounded up to 256.
- * Returns 0 when nothing would split (G not a multiple of 4) or for invalid
- * arguments.
+ * piece per worker: min(32 * units, num_sms / 2) * 266240 bytes (CTA pairs)
+ * or min(32 * units, num_sms) * 133120 bytes (single CTAs), rounded up to 256.
+ * Returns 0 for invalid arguments.
  */
 GQA_API size_t gqa_attn_prefill_causal_workspace_size(int B, int H_q, int H_kv, int T_q,
                                                       int S_kv, int d, int q_offset,
                                                       int num_sms);
 
 /*
- * The CTA-pair prefill work plan for `num_pairs` resident pairs and `ws_bytes`
- * of workspace (host only, no CUDA call): writes the number of units, how
- * many of them (the last round's) are split, and the pieces per split unit
- * (1 if none).  Piece i of s of a unit with n key tiles covers tiles
+ * The prefill work plan on a device of `num_sms` SMs (one CTA per SM: num_sms / 2
+ * CTA pairs when G is a multiple of 4, else num_sms CTAs) with `ws_bytes` of
+ * workspace (host only, no CUDA call): writes the number of units, how many of
+ * them (the last round's) are split, and the pieces per split unit (1 if
+ * none).  Piece i of s of a unit with n key tiles covers tiles
  * [i*n/s, (i+1)*n/s).  Units are dealt longest first, so the split ones are
- * the shortest.  G not a multiple of 4 (one CTA per unit): 0 units, no split.
- * Returns GQA_OK or GQA_ERR_INVALID_ARG.
+ * the shortest.  Returns GQA_OK or GQA_ERR_INVALID_ARG.
  */
 GQA_API int gqa_attn_prefill_causal_plan(int B, int H_q, int H_kv, int T_q, int S_kv, int d,
-                                         int q_offset, int num_pairs, size_t ws_bytes,
+                                         int q_offset, int num_sms, size_t ws_bytes,
                                          int *out_units, int *out_split_units,
                                          int *out_pieces_per_unit);
 

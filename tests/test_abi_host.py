@@ -86,40 +86,47 @@ def test_workspace_size(lib):
     assert gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 0, 0) == 0  # bad num_sms
 
 
-PIECE_BYTES = 4 * 128 * 130 * 4   # per piece: 4 heads x 128 rows x (O[128], m, l) fp32
+PIECE_BYTES = 4 * 128 * 130 * 4   # per piece, CTA pairs: 4 heads x 128 rows x (O[128], m, l) fp32
+PIECE_BYTES_1 = 2 * 128 * 130 * 4  # per piece, one CTA: 2 slots x 128 rows
 
 
-@pytest.mark.parametrize("shape,pairs,expect", [
+@pytest.mark.parametrize("shape,sms,expect", [
     # chunked 32K (last 2K): 256 units on 76 pairs, the 28 of the fourth round cut in 2
-    ((1, 64, 8, 2048, 32768, 30720), 76, (256, 28, 2)),
+    ((1, 64, 8, 2048, 32768, 30720), 152, (256, 28, 2)),
     # 8K causal: the last round's units are 1-3 key tiles long, nothing to split
-    ((1, 64, 8, 8192, 8192, 0), 76, (1024, 0, 1)),
+    ((1, 64, 8, 8192, 8192, 0), 152, (1024, 0, 1)),
     # a 128-token chunk after 32K keys: 16 units, each cut in 4 (76 // 16)
-    ((1, 64, 8, 128, 32768, 32640), 76, (16, 16, 4)),
+    ((1, 64, 8, 128, 32768, 32640), 152, (16, 16, 4)),
     # two units of 32 tiles: at most 32 // 8 = 4 pieces each
-    ((1, 8, 2, 128, 4096, 3968), 76, (2, 2, 4)),
+    ((1, 8, 2, 128, 4096, 3968), 152, (2, 2, 4)),
     # units fill whole rounds: no split
-    ((1, 64, 8, 2048, 32768, 30720), 64, (256, 0, 1)),
+    ((1, 64, 8, 2048, 32768, 30720), 128, (256, 0, 1)),
     # one unit, 300 pairs: capped at 32 pieces
-    ((1, 4, 1, 100, 65536, 65436), 300, (1, 1, 32)),
-    # G not a multiple of 4 runs one CTA per unit: no plan
-    ((1, 6, 2, 2048, 32768, 30720), 76, (0, 0, 1)),
+    ((1, 4, 1, 100, 65536, 65436), 600, (1, 1, 32)),
+    # G = 3 (one CTA per unit): 16 query tiles x 2 KV heads head-pair units plus
+    # 8 x 2 last-head units over two query tiles = 48 units on 152 CTAs, cut in 3
+    ((1, 6, 2, 2048, 32768, 30720), 152, (48, 48, 3)),
+    # G = 2, 8K causal: 2048 units, nothing to split
+    ((1, 64, 32, 8192, 8192, 0), 152, (2048, 0, 1)),
+    # MHA, a 256-token chunk after 128K keys: 64 heads x 1 two-tile unit on 152 CTAs
+    ((1, 64, 64, 256, 131072, 130816), 152, (64, 64, 2)),
 ])
-def test_prefill_split_plan(lib, shape, pairs, expect):
+def test_prefill_split_plan(lib, shape, sms, expect):
     B, H_q, H_kv, T_q, S_kv, q_off = shape
-    got = gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, pairs, 1 << 30)
+    got = gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, sms, 1 << 30)
     assert got == expect
     units, split_units, s = got
+    piece = PIECE_BYTES if (H_q // H_kv) % 4 == 0 else PIECE_BYTES_1
     if split_units:
         # the workspace the plan needs is within the size query's bound
         bound = gqa.gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, 128, q_off,
-                                                           2 * pairs)
-        assert split_units * s * PIECE_BYTES <= bound
+                                                           sms)
+        assert split_units * s * piece <= bound
         # too small a workspace: no split, never an error
-        assert gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, pairs,
-                                                split_units * s * PIECE_BYTES - 1)[1] == 0
+        assert gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, sms,
+                                                split_units * s * piece - 1)[1] == 0
         # no workspace: no split
-        assert gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, pairs,
+        assert gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, sms,
                                                 0)[1] == 0
 
 
@@ -151,7 +158,11 @@ def test_prefill_workspace_size(lib):
                                                       152) == 64 * PIECE_BYTES
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 4, 1, 100, 4096, 128, 3996,
                                                       152) == 32 * PIECE_BYTES
-    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 6, 2, 128, 4096, 128, 3968, 152) == 0
+    # one CTA per unit (G = 3): 2 head-pair + 2 last-head units, 32 pieces each at most
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 6, 2, 128, 4096, 128, 3968,
+                                                      152) == 128 * PIECE_BYTES_1
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 6, 2, 2048, 32768, 128, 30720,
+                                                      152) == 152 * PIECE_BYTES_1
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 100, 128, 0, 152) == 0
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 256, 128, 0, 0) == 0
 

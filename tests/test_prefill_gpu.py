@@ -157,14 +157,19 @@ def test_running_max_paths(H_q, H_kv):
     compare(o, lse, o_ref, lse_ref, f"running max paths G={H_q // H_kv}")
 
 
-# Shapes whose last round of units is split by key range (76 CTA pairs on a
-# GB300): (B, H_q, H_kv, T_q, S_kv, q_offset).
+# Shapes whose last round of units is split by key range (76 CTA pairs or 152
+# CTAs on a GB300): (B, H_q, H_kv, T_q, S_kv, q_offset).
 SPLIT_CASES = [
     (1, 8, 2, 128, 4096, 3968),     # 2 units, 4 pieces each (fewer units than pairs)
     (1, 16, 2, 200, 3000, 2800),    # G = 8, 8 units, ragged second query tile
     (1, 8, 1, 300, 4300, 4000),     # 6 units, 4 pieces each, q_offset not tile aligned
     (1, 32, 8, 1280, 3328, 2048),   # 80 units: one full round, the 4 left cut in 2
     (2, 16, 2, 256, 2304, 2048),    # two sequences
+    # one CTA per unit (G not a multiple of 4)
+    (1, 6, 2, 128, 4096, 3968),     # G = 3: 4 units, 4 pieces each
+    (1, 4, 4, 300, 3000, 2700),     # MHA: last-head units over query tiles 2+1 and 0, cut in 2
+    (1, 10, 2, 256, 2560, 2304),    # G = 5
+    (2, 8, 4, 200, 2200, 2000),     # G = 2, two sequences, ragged second query tile
 ]
 
 
