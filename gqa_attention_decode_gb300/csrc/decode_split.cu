@@ -75,6 +75,7 @@ struct Params {
   int B, H_q, H_kv, G, S_max, num_splits, chunk;
   int T_q, n_cols, cgroups;  // new tokens per sequence, G * T_q, column groups of 4 warps
   float scale_log2;  // scale * log2(e)
+  int l2_prefetch_tiles;  // tiles of its chunk a CTA pulls into L2 before the dependency wait
   WaitCtl wait;
 };
 
@@ -133,11 +134,14 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   if (warp == n_consumers && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    // Dense cache: pull the first tiles of this split's key range into L2 while
-    // the preceding grid finishes (its length is not known yet, so the range is
-    // the split's whole chunk; keys past the sequence are masked later).
+    // Dense cache, one-wave grid: pull the first tiles of this split's key range
+    // into L2 while the preceding grid finishes (its length is not known yet,
+    // so the range is the split's whole chunk; keys past the sequence are
+    // masked later).  Only a grid that is resident all at once can overlap the
+    // preceding grid; in a larger one, splits past their sequence's end would
+    // only prefetch padding.
     if (!kPaged) {
-      const int tiles = min(GQA_DECODE_L2_PREFETCH_TILES, p.chunk / kTileKeys);
+      const int tiles = min(p.l2_prefetch_tiles, p.chunk / kTileKeys);
       for (int i = 0; i < tiles; ++i) {
         const int key0 = split * p.chunk + i * kTileKeys;
         for (int half = 0; half < 2; ++half) {
@@ -698,6 +702,7 @@ static decode::Params make_params(const DecodeLaunch &a) {
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
+  p.l2_prefetch_tiles = 0;
   p.wait = a.wait;
   return p;
 }
@@ -738,7 +743,9 @@ cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   if (a.S_max <= 0) return cudaSuccess;
   CUtensorMap tm_k, tm_v;
   if (!make_maps(a, encode, &tm_k, &tm_v)) return cudaErrorInvalidValue;
-  const Params p = make_params(a);
+  Params p = make_params(a);
+  const long long ctas = (long long)a.num_splits * a.H_kv * a.B;
+  if (ctas <= a.num_sms) p.l2_prefetch_tiles = GQA_DECODE_L2_PREFETCH_TILES;  // one wave
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_splits, a.H_kv, a.B);
   cfg.blockDim = dim3(kThreads);
@@ -748,7 +755,6 @@ cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const long long ctas = (long long)a.num_splits * a.H_kv * a.B;
   const bool paged = a.block_table != nullptr;
   if (p.n_cols > 8)  // multi-token decode: two n-tiles per warp, one CTA per SM
     return launch_variant<kOneWaveStages, 1, false, 2>(&cfg, tm_k, tm_v, p, paged);

@@ -63,6 +63,7 @@ struct Params {
   float *lse_part;
   int B, H_q, H_kv, G, T_q, S_max, num_splits, chunk;
   int page_size, max_pages, num_pages;
+  int l2_prefetch;  // one-wave grid on a dense cache: prefetch the first key tile
   float sl2;  // scale * log2(e)
   WaitCtl wait;
 };
@@ -125,10 +126,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Dense cache: the first key tile of this split's chunk is pulled into L2
-  // while the preceding grid finishes (L2 is the point of coherence, so this is
-  // safe ahead of the wait; the sequence length is not known yet).
-  if (p.block_table == nullptr && warp == kWarpTma && lane == 0 && p.chunk >= kBN) {
+  // Dense cache, one-wave grid: the first key tile of this split's chunk is
+  // pulled into L2 while the preceding grid finishes (L2 is the point of
+  // coherence, so this is safe ahead of the wait; the sequence length is not
+  // known yet).
+  if (p.l2_prefetch && warp == kWarpTma && lane == 0 && p.chunk >= kBN) {
     for (int half = 0; half < 2; ++half) {
       tma_prefetch_l2_4d(&tm_k, 0, half, split * p.chunk, b * p.H_kv + kv);
       tma_prefetch_l2_4d(&tm_v, 0, half, split * p.chunk, b * p.H_kv + kv);
@@ -533,6 +535,7 @@ cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
+  p.l2_prefetch = !paged && (long long)a.num_splits * a.H_kv * a.B <= a.num_sms;
   p.o_part = a.o_part;
   p.lse_part = a.lse_part;
   p.B = a.B;
