@@ -21,7 +21,7 @@
 //     longest-first (latest query tile first).
 //   * Warps 0-3 and 4-7: softmax for head 0 and head 1, one thread per query
 //     row, the whole 128-column S row held in registers.  Warp 8: TMA producer
-//     (Q tiles, then K_j, V_j through a 5-stage ring).  Warp 9: allocates the 512
+//     (Q tiles, then K_j, V_j through a 4-stage ring).  Warp 9: allocates the 512
 //     TMEM columns and issues every tcgen05.mma from one thread (M = N = 128,
 //     K = 16, bf16 in, fp32 accumulate).
 //   * TMEM: S0, S1 (128 columns each) and O0, O1 (128 columns each).  P is
@@ -45,7 +45,7 @@ namespace prefill {
 constexpr int kD = 128;
 constexpr int kBM = 128;                     // query rows per tile
 constexpr int kBN = 128;                     // keys per tile
-constexpr int kStages = 5;                   // K/V ring depth (each stage holds one K or V tile)
+constexpr int kStages = 4;                   // K/V ring depth (each stage holds one K or V tile)
 constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr int kThreads = 320;
 constexpr int kTileBytes = kBM * kD * 2;     // 32 KiB

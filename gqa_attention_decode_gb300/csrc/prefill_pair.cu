@@ -46,7 +46,7 @@ constexpr int kD = 128;
 constexpr int kBM = 128;                  // query rows per tile (per CTA)
 constexpr int kBN = 128;                  // keys per tile
 constexpr int kHalfKeys = kBN / 2;        // keys of a K tile held by one CTA
-constexpr int kStages = 9;                // ring of 16 KiB stages (a K half or a V half)
+constexpr int kStages = 6;                // ring of 16 KiB stages (a K half or a V half)
 constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr int kThreads = 320;
 constexpr int kQBytes = kBM * kD * 2;     // 32 KiB per slot
