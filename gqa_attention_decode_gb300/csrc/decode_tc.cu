@@ -330,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_s = [&]() {
 #pragma unroll
         for (int c = 0; c < 4; ++c) tc::ld32(t_s + 32 * c, sv + 32 * c);
-        tc::wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::wait_ld32(sv + 32 * c);  // one wait; ties each chunk
         if (!pos_scale) {
 #pragma unroll
           for (int e = 0; e < kBN; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * p.sl2);
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
             tc::ld32(t_o + 32 * c, r);
-            tc::wait_ld();
+            tc::wait_ld32(r);
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
             tc::st32(t_o + 32 * c, r);
@@ -455,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r0[32], r1[32];
           tc::ld32(t_o + 32 * c, r0);
           if (use1) tc::ld32(t_o + 128u + 32 * c, r1);
-          tc::wait_ld();
+          tc::wait_ld32(r0);         // waits for both loads; ties r0's registers to it
+          if (use1) tc::wait_ld32(r1);  // (already complete) ties r1's
           if (row < R) {
             const size_t orow = (size_t)(b * p.H_q + kv * p.G) * p.T_q + row;
             float4 *dst =

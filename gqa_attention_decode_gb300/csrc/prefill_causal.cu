@@ -456,9 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // common path: the whole row in registers (one load wait), before the exp turn
         uint32_t sv[kBN];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc::ld32(t_s + 32 * c, sv + 32 * c);
-        tc::wait_ld();
+tc::ld128_wait(t_s, sv);
 #pragma unroll
         for (int c = 0; c < 4; ++c) prep(sv + 32 * c, c);
         if (j == w.kv_lo) {  // its first key is visible to every row: finite
@@ -508,8 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mbar_arrive(tok(1 - i));  // the exp unit is free: the other warpgroup may start
-        tc::st32(t_s, pk);
-        tc::st32(t_s + 32, pk + 32);
+        tc::st64(t_s, pk);
         tc::wait_st();
         l += tsum;
         tc::fence_before_sync();
@@ -525,9 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool store = (i == 0 || w.second_valid) && qrow < p.T_q;
       const size_t orow = ((size_t)w.b * p.H_q + h) * p.T_q + qrow;
       uint32_t ov[kD];
-#pragma unroll
-      for (int c = 0; c < kD / 32; ++c) tc::ld32(t_o + 32 * c, ov + 32 * c);
-      tc::wait_ld();
+tc::ld128_wait(t_o, ov);
       if (store && w.piece >= 0) {
         // a piece of a split unit: its partial (O not yet divided, m, l) for the merge
         const size_t prow = prefill_split::partial_row(w.piece, 2, i, row);

@@ -445,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sv[kBN];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tc::ld32(t_s + 32 * c, sv + 32 * c);
-        tc::wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::wait_ld32(sv + 32 * c);  // one wait; ties each chunk
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (!pos_scale) {
@@ -529,7 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ov[kD];
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) tc::ld32(t_o + 32 * c, ov + 32 * c);
-      tc::wait_ld();
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) tc::wait_ld32(ov + 32 * c);
       if (qrow < p.T_q && w.piece >= 0) {
         // a piece of a split unit: its partial (O not yet divided, m, l) for the merge
         const size_t prow = prefill_split::partial_row(w.piece, 4, 2 * i + rank, row);
