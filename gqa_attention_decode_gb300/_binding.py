@@ -66,6 +66,8 @@ _SIGNATURES = {
     "gqa_attn_prefill_causal_from_host": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int,
                                                    _c_int, _c_int, _c_int, _c_int, _c_float,
                                                    _vp, _vp, _vp, _c_size, _vp]),
+    "gqa_attn_merge_states": (_c_int, [_vp, _vp, _c_int, ctypes.c_longlong, _c_int, _vp, _vp,
+                                       _vp]),
     "gqa_attn_device_status": (_c_int, [_vp, _ip]),
     "gqa_attn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
 }
@@ -448,6 +450,35 @@ def gqa_attn_prefill_causal(q, k, v, scale, q_offset=0, o=None, lse=None, worksp
                                             ws_ptr, workspace.numel(),
                                             _stream_handle(stream, dev))
     _check(rc, "gqa_attn_prefill_causal_ws")
+    return o, lse
+
+
+def gqa_attn_merge_states(o_parts, lse_parts, o=None, lse=None, stream=None):
+    """Combine attention states over disjoint key shards.  o_parts [P, ..., d] bf16,
+    lse_parts [P, ...] fp32 (natural log), the shards stacked on the first axis.
+    Returns (o [..., d] bf16, lse [...] fp32)."""
+    lib = load_library()
+    if not isinstance(o_parts, torch.Tensor) or not isinstance(lse_parts, torch.Tensor):
+        raise TypeError("o_parts and lse_parts must be torch.Tensors")
+    if o_parts.dtype != torch.bfloat16 or lse_parts.dtype != torch.float32:
+        raise TypeError("o_parts must be bfloat16 and lse_parts float32")
+    if not o_parts.is_cuda or lse_parts.device != o_parts.device:
+        raise ValueError("o_parts and lse_parts must be CUDA tensors on one device")
+    if o_parts.dim() < 2 or tuple(o_parts.shape[:-1]) != tuple(lse_parts.shape):
+        raise ValueError("o_parts must be [P, ..., d] and lse_parts [P, ...]")
+    if not o_parts.is_contiguous() or not lse_parts.is_contiguous():
+        raise ValueError("o_parts and lse_parts must be contiguous")
+    dev = o_parts.device
+    P, d = o_parts.shape[0], o_parts.shape[-1]
+    rows = lse_parts[0].numel() if P > 0 else 0
+    if o is None:
+        o = torch.empty(o_parts.shape[1:], dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_merge_states(_ptr(o_parts), _ptr(lse_parts), P, rows, d, _ptr(o),
+                                       _ptr(lse), _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_merge_states")
     return o, lse
 
 

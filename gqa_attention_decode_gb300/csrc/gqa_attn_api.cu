@@ -553,6 +553,24 @@ GQA_API int gqa_attn_prefill_causal_kernel_count(int B, int H_q, int H_kv, int T
   return GQA_OK;
 }
 
+GQA_API int gqa_attn_merge_states(const gqa_bf16_t *o_parts, const float *lse_parts,
+                                  int n_parts, long long rows, int d, gqa_bf16_t *o, float *lse,
+                                  gqa_stream_t stream) {
+  if (n_parts < 1 || rows < 0 || d <= 0) return GQA_ERR_INVALID_ARG;
+  if (rows == 0) return GQA_OK;
+  if (!o_parts || !lse_parts || !o || !lse) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o) || !aligned16(lse))
+    return GQA_ERR_INVALID_ARG;
+  if (d != 128) return GQA_ERR_UNSUPPORTED;
+  if (rows > 0x7fffffffLL * 8 || (long long)n_parts * rows > (1LL << 40))
+    return GQA_ERR_UNSUPPORTED;
+  DeviceState *st = nullptr;
+  int rc = device_state(&st);
+  if (rc != GQA_OK) return rc;
+  return to_status(gqa::merge_states_launch(o_parts, lse_parts, n_parts, rows, o, lse,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 // ---- host-buffer variants ------------------------------------------------------
 
 namespace {

@@ -104,6 +104,11 @@ size_t prefill_pair_workspace_bound(long long units, int num_sms);
 cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
                                 PFN_cuTensorMapEncodeTiled_v12000 encode);
 
+// ---- combination of attention states over key shards ---------------------------
+// o_parts [n_parts][rows][128] bf16, lse_parts [n_parts][rows] fp32 (natural log).
+cudaError_t merge_states_launch(const uint16_t *o_parts, const float *lse_parts, int n_parts,
+                                long long rows, uint16_t *o, float *lse, cudaStream_t stream);
+
 // ---- diagnostics --------------------------------------------------------------
 cudaError_t selftest_bounded_wait_launch(WaitCtl wait, cudaStream_t stream);
 

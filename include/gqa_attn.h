@@ -385,6 +385,35 @@ GQA_API int gqa_attn_prefill_causal_kernel_count(int B, int H_q, int H_kv, int T
                                                  int *out_kernels);
 
 /* ------------------------------------------------------------------------- */
+/* Combination of attention states over key shards                            */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Combines attention states computed over disjoint key shards (record:
+ * section 4 "Reduction", the associative log-sum-exp merge, here of
+ * finalised states).  For each row r and shards i = 0 .. n_parts-1:
+ *     lse[r] = ln sum_i exp(lse_parts[i][r])
+ *     o[r]   = sum_i exp(lse_parts[i][r] - lse[r]) * o_parts[i][r]
+ * A shard with lse = -inf (no visible key) contributes nothing; a row with
+ * -inf in every shard gets O = 0, lse = -inf.  The shard states are outputs
+ * of this library's calls over key shards, e.g. decode over a shared prefix
+ * and over each sequence's own suffix, or the KV shards of a
+ * sequence-parallel decode gathered from several GPUs (section 4's reduce
+ * across ranks; the gather itself is the caller's).
+ *
+ *   o_parts    device [n_parts, rows, d] bf16 (each shard's normalised O).
+ *   lse_parts  device [n_parts, rows] fp32 (natural log, scaled scores).
+ *   n_parts    >= 1; rows >= 0 (rows == 0 launches nothing); d must be 128.
+ *   o          device [rows, d] bf16 output; lse device [rows] fp32 output.
+ * One kernel on `stream`, launched as a programmatic dependent.  The result
+ * differs from one call over all keys by the rounding of the bf16 shard
+ * outputs (at most about 2^-9 relative per element of O).
+ */
+GQA_API int gqa_attn_merge_states(const gqa_bf16_t *o_parts, const float *lse_parts,
+                                  int n_parts, long long rows, int d, gqa_bf16_t *o, float *lse,
+                                  gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Host-buffer variants (whole-call end-to-end path)                           */
 /* ------------------------------------------------------------------------- */
 

@@ -22,5 +22,6 @@ from .attention import (  # noqa: F401
     partial_triplet,
     merge_triplets,
     finalize_triplet,
+    merge_states,
     online_softmax_tiles,
 )

@@ -246,6 +246,31 @@ def finalize_triplet(t):
     return out, lse
 
 
+def merge_states(o_parts, lse_parts):
+    """Combine finalised attention states of disjoint key shards.
+
+    The record's section 4 reduction applied to normalised partials: a shard's
+    (O_i, lse_i) is its (m, l, O) triplet after ``finalize_triplet``, so with
+    lse = ln sum_i exp(lse_i) the combined output is
+    O = sum_i exp(lse_i - lse) O_i.  o_parts [P, R, d], lse_parts [P, R]; a
+    shard with lse_i = -inf (no visible key) contributes nothing; a row whose
+    shards are all empty gives O = 0, lse = -inf.
+    """
+    o_parts = _f64(o_parts)
+    lse_parts = _f64(lse_parts)
+    m = lse_parts.max(axis=0)
+    ok = np.isfinite(m)
+    m_safe = np.where(ok, m, 0.0)
+    w = np.where(np.isfinite(lse_parts), np.exp(np.where(np.isfinite(lse_parts), lse_parts, 0.0)
+                                                 - m_safe[None, :]), 0.0)
+    total = w.sum(axis=0)
+    out = np.zeros(o_parts.shape[1:])
+    out[ok] = (w[:, ok, None] * o_parts[:, ok]).sum(axis=0) / total[ok, None]
+    lse = np.full(m.shape, NEG_INF)
+    lse[ok] = m[ok] + np.log(total[ok])
+    return out, lse
+
+
 def online_softmax_tiles(q_rows, k, v, scale, n_visible, tile):
     """The per-tile online-softmax loop of section 3, in float64.
 

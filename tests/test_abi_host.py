@@ -278,6 +278,19 @@ def test_paged_multi_rejections(lib):
     assert call(64, 8, 16, 256, B=0) == gqa.GQA_OK
 
 
+def test_merge_states_rejects_before_any_cuda_call(lib):
+    v = ctypes.c_void_p
+    p = 1 << 20
+    call = lambda o_parts=p, lse_parts=p, n=2, rows=10, d=128, o=p, lse=p: \
+        lib.gqa_attn_merge_states(v(o_parts), v(lse_parts), n, rows, d, v(o), v(lse), v(0))
+    assert call(n=0) == gqa.GQA_ERR_INVALID_ARG
+    assert call(rows=-1) == gqa.GQA_ERR_INVALID_ARG
+    assert call(o=0) == gqa.GQA_ERR_INVALID_ARG
+    assert call(lse_parts=p + 4) == gqa.GQA_ERR_INVALID_ARG    # misaligned
+    assert call(d=64) == gqa.GQA_ERR_UNSUPPORTED
+    assert call(rows=0) == gqa.GQA_OK                          # nothing to do
+
+
 def test_multi_token_rejections(lib):
     v = ctypes.c_void_p
     p = 1 << 20

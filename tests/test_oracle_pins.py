@@ -256,6 +256,44 @@ def test_split_merge_equals_unsplit(seed):
         np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_merge_states_of_shards_equals_unsplit(seed):
+    """Attention over disjoint key shards, each finalised to (O_i, lse_i), then
+    combined by merge_states, equals attention over all keys (the record's
+    section 4 associativity); empty shards (lse = -inf) change nothing."""
+    r = np.random.default_rng(100 + seed)
+    R, N, d = 5, 41, 8
+    q, k, v = r.standard_normal((R, d)), r.standard_normal((N, d)), r.standard_normal((N, d))
+    scale = 0.35
+    ref_o, ref_lse = A.attend_rows(q, k, v, scale, np.full(R, N))
+    cuts = np.sort(r.integers(0, N + 1, size=4))
+    bounds = [0, *cuts.tolist(), N]
+    o_p, l_p = [], []
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        o_i, l_i = A.finalize_triplet(A.partial_triplet(q, k, v, scale, lo, hi))
+        o_p.append(o_i)
+        l_p.append(l_i)
+    o, lse = A.merge_states(np.stack(o_p), np.stack(l_p))
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_merge_states_closed_forms():
+    """Two states with equal lse average their outputs and add ln 2; a single
+    state is returned unchanged; all-empty rows give (0, -inf)."""
+    o = np.array([[[1.0, -2.0]], [[3.0, 4.0]]])
+    lse = np.array([[0.5], [0.5]])
+    out, l = A.merge_states(o, lse)
+    np.testing.assert_allclose(out, [[2.0, 1.0]], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(l, [0.5 + np.log(2.0)], rtol=0, atol=1e-15)
+    out, l = A.merge_states(o[:1], lse[:1])
+    np.testing.assert_array_equal(out, o[0])
+    np.testing.assert_array_equal(l, lse[0])
+    out, l = A.merge_states(o, np.full((2, 1), -np.inf))
+    np.testing.assert_array_equal(out, [[0.0, 0.0]])
+    assert l[0] == -np.inf
+
+
 @pytest.mark.parametrize("tile", [1, 3, 7, 64])
 def test_online_softmax_tiles_equal_definition(tile):
     r = np.random.default_rng(tile)
