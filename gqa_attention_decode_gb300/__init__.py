@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     GQA_ERR_CUDA,
     GQA_ERR_WORKSPACE,
     GQA_ERR_TIMEOUT,
+    GQA_ERR_OUT_OF_BOUNDS,
     lib_path,
     load_library,
     gqa_status_string,
@@ -40,4 +41,6 @@ from ._binding import (  # noqa: F401
     gqa_attn_prefill_causal_from_host,
     gqa_attn_device_status,
     gqa_attn_selftest_bounded_wait,
+    gqa_attn_bounds_checked,
+    gqa_attn_selftest_bounds,
 )

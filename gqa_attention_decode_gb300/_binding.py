@@ -18,6 +18,7 @@ GQA_ERR_UNSUPPORTED = 2
 GQA_ERR_CUDA = 3
 GQA_ERR_WORKSPACE = 4
 GQA_ERR_TIMEOUT = 5
+GQA_ERR_OUT_OF_BOUNDS = 6
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libgqa_attn.so"
@@ -70,6 +71,8 @@ _SIGNATURES = {
                                        _vp]),
     "gqa_attn_device_status": (_c_int, [_vp, _ip]),
     "gqa_attn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
+    "gqa_attn_bounds_checked": (_c_int, []),
+    "gqa_attn_selftest_bounds": (_c_int, [_vp]),
 }
 
 
@@ -553,6 +556,20 @@ def gqa_attn_device_status(stream=None, device=None) -> int:
                                                      ctypes.byref(out)),
                "gqa_attn_device_status")
     return out.value
+
+
+def gqa_attn_bounds_checked() -> bool:
+    """Whether the loaded library is a bounds-checked build (libgqa_attn_debug.so)."""
+    return bool(load_library().gqa_attn_bounds_checked())
+
+
+def gqa_attn_selftest_bounds(stream=None, device=None) -> None:
+    """Bounds-checked builds: one store past its range, recorded as
+    GQA_ERR_OUT_OF_BOUNDS in the device status (raises GQAError elsewhere)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(load_library().gqa_attn_selftest_bounds(_stream_handle(stream, dev)),
+               "gqa_attn_selftest_bounds")
 
 
 def gqa_attn_selftest_bounded_wait(timeout_us: int, stream=None, device=None) -> None:

@@ -22,6 +22,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libgqa_attn.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+# The bounds-checked build: every kernel checks the index of each global store
+# against its extent and records violations in the status word.
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libgqa_attn_debug.so")
+DEBUG_FLAGS = ["-DGQA_DEBUG_BOUNDS"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH_FLAGS + [
@@ -44,7 +48,7 @@ def sources() -> list[str]:
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _stamp(nvcc: str) -> str:
+def _stamp(nvcc: str, extra: list[str]) -> str:
     h = hashlib.sha256()
     for d in (CSRC, INCLUDE):
         for f in sorted(os.listdir(d)):
@@ -52,26 +56,30 @@ def _stamp(nvcc: str) -> str:
                 h.update(f.encode())
                 with open(os.path.join(d, f), "rb") as fh:
                     h.update(fh.read())
-    h.update(" ".join(NVCC_FLAGS + LINK_FLAGS).encode())
+    h.update(" ".join(NVCC_FLAGS + extra + LINK_FLAGS).encode())
     h.update(subprocess.run([nvcc, "--version"], capture_output=True, text=True).stdout.encode())
     h.update(os.uname().machine.encode())
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library if needed; returns its path."""
+def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False) -> str:
+    """Compile and link the library if needed; returns its path.  debug_bounds:
+    the bounds-checked build (libgqa_attn_debug.so, objects apart)."""
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    stamp = _stamp(nvcc)
-    stamp_file = os.path.join(BUILD_DIR, "libgqa_attn.stamp")
-    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp_file):
+    extra = DEBUG_FLAGS if debug_bounds else []
+    lib_path = DEBUG_LIB_PATH if debug_bounds else LIB_PATH
+    build_dir = os.path.join(BUILD_DIR, "debug") if debug_bounds else BUILD_DIR
+    os.makedirs(build_dir, exist_ok=True)
+    stamp = _stamp(nvcc, extra)
+    stamp_file = os.path.join(build_dir, "libgqa_attn.stamp")
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
-                return LIB_PATH
+                return lib_path
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src).replace(".cu", ".o"))
-        cmd = [nvcc, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(build_dir, os.path.basename(src).replace(".cu", ".o"))
+        cmd = [nvcc, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -84,15 +92,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     srcs = sources()
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     r = subprocess.run([nvcc, *LINK_FLAGS, *objs, "-o", tmp], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug_bounds="--debug-bounds" in sys.argv))

@@ -435,7 +435,9 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     col_row[n] = row;
     if (kFused) {
       cta_lse[n] = lse_s;
-    } else if (row >= 0) {
+    } else if (row >= 0 &&
+               store_ok((size_t)row * p.num_splits + split,
+                        (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) {
       p.lse_part[(size_t)row * p.num_splits + split] = lse_s;
     }
   }
@@ -458,7 +460,8 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     }
     if (kFused) {
       reinterpret_cast<float4 *>(cta_o + n * kD)[d4] = acc;
-    } else {
+    } else if (store_ok((size_t)row * p.num_splits + split,
+                        (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) {
       reinterpret_cast<float4 *>(p.o_part + ((size_t)row * p.num_splits + split) * kD)[d4] = acc;
     }
   }
@@ -485,6 +488,7 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
         const int gh = n / p.T_q, tq = n % p.T_q;
         const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + gh) * p.T_q + tq;
         const __nv_bfloat16 r = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+        if (!store_ok(row, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) continue;
         p.o[row * kD + dd] = *reinterpret_cast<const uint16_t *>(&r);
         if (dd == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
       }

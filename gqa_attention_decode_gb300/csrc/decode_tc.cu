@@ -446,11 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = L > 0.f ? 1.f / L : 0.f;
         const float c0 = w0 * inv, c1 = w1 * inv;  // 0 for a slot with no visible key
         const bool use1 = n_slot[1] > 0;            // warp-uniform
-        if (row < R) {
-          const size_t orow = (size_t)(b * p.H_q + kv * p.G) * p.T_q + row;
+        // rows past G * T_q belong to other heads' queries: computed, never stored
+        const size_t orow = (size_t)(b * p.H_q + kv * p.G) * p.T_q + row;
+        const bool store = row < R && store_ok(orow * p.num_splits + split,
+                                               (size_t)p.B * p.H_q * p.T_q * p.num_splits,
+                                               p.wait.status);
+        if (store)
           p.lse_part[orow * p.num_splits + split] =
               L > 0.f ? mx * 0.69314718055994531f + logf(L) : -INFINITY;
-        }
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t r0[32], r1[32];
@@ -458,8 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (use1) tc::ld32(t_o + 128u + 32 * c, r1);
           tc::wait_ld32(r0);         // waits for both loads; ties r0's registers to it
           if (use1) tc::wait_ld32(r1);  // (already complete) ties r1's
-          if (row < R) {
-            const size_t orow = (size_t)(b * p.H_q + kv * p.G) * p.T_q + row;
+          if (store) {
             float4 *dst =
                 reinterpret_cast<float4 *>(p.o_part + (orow * p.num_splits + split) * kD) + 8 * c;
             // both slots' O are finite (every slot with a tile wrote its O, and V

@@ -12,6 +12,24 @@ namespace gqa {
 // Status word values (mirrors gqa_status_t).
 constexpr int kStatusInvalidArg = 1;  // a device-side input out of range (clamped)
 constexpr int kStatusTimeout = 5;
+constexpr int kStatusOutOfBounds = 6;  // debug builds: a store index past its extent
+
+// Guard of a global store: whether element `idx` lies inside the `extent`
+// elements the kernel derives from its own arguments.  Debug builds
+// (GQA_DEBUG_BOUNDS) record a violation in the status word and skip the store;
+// release builds compile the check away.
+__device__ __forceinline__ bool store_ok(size_t idx, size_t extent, int *status) {
+#ifdef GQA_DEBUG_BOUNDS
+  if (idx < extent) return true;
+  atomicExch(status, kStatusOutOfBounds);
+  return false;
+#else
+  (void)idx;
+  (void)extent;
+  (void)status;
+  return true;
+#endif
+}
 
 // Bounded-wait control passed to every kernel: where to record a timeout and
 // how long a single wait may take.

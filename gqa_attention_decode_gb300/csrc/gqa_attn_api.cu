@@ -1,6 +1,6 @@
 // gqa_attn_api.cu -- the extern "C" boundary: argument checks, the decode split
 // planner, per-device set-up, host-buffer staging and diagnostics.  Every
-// numerical step runs in the kernels of decode_split.cu and prefill_causal.cu.
+// numerical step runs in the library's kernels (the other files of csrc/).
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
@@ -202,6 +202,12 @@ __global__ void selftest_wait_kernel(gqa::WaitCtl wait) {
   __syncthreads();
 }
 
+// One store of index `extent` into an `extent`-element range: past its end by
+// one, so a bounds-checked build records GQA_ERR_OUT_OF_BOUNDS and skips it.
+__global__ void selftest_bounds_kernel(float *sink, int *status) {
+  if (threadIdx.x == 0 && gqa::store_ok(1, 1, status)) sink[0] = 1.f;
+}
+
 }  // namespace
 
 namespace gqa {
@@ -221,6 +227,8 @@ GQA_API const char *gqa_status_string(int status) {
     case GQA_ERR_CUDA: return "GQA_ERR_CUDA: CUDA call failed";
     case GQA_ERR_WORKSPACE: return "GQA_ERR_WORKSPACE: workspace too small";
     case GQA_ERR_TIMEOUT: return "GQA_ERR_TIMEOUT: bounded device wait ran out";
+    case GQA_ERR_OUT_OF_BOUNDS:
+      return "GQA_ERR_OUT_OF_BOUNDS: a kernel store index past its extent (bounds-checked build)";
     default: return "unknown gqa status";
   }
 }
@@ -721,6 +729,30 @@ GQA_API int gqa_attn_selftest_bounded_wait(int timeout_us, gqa_stream_t stream) 
   w.status = st->status;
   w.timeout_ns = (uint64_t)timeout_us * 1000ull;
   return to_status(gqa::selftest_bounded_wait_launch(w, static_cast<cudaStream_t>(stream)));
+}
+
+GQA_API int gqa_attn_bounds_checked(void) {
+#ifdef GQA_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+GQA_API int gqa_attn_selftest_bounds(gqa_stream_t stream) {
+#ifndef GQA_DEBUG_BOUNDS
+  (void)stream;
+  return GQA_ERR_UNSUPPORTED;  // release builds carry no store checks
+#else
+  DeviceState *st = nullptr;
+  int rc = device_state(&st);
+  if (rc != GQA_OK) return rc;
+  // the store is skipped, so the sink is never written: the status word's own
+  // address serves (a valid device pointer)
+  selftest_bounds_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<float *>(st->status), st->status);
+  return to_status(cudaGetLastError());
+#endif
 }
 
 }  // extern "C"

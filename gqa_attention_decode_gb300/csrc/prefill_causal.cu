@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // common path: the whole row in registers (one load wait), before the exp turn
         uint32_t sv[kBN];
-tc::ld128_wait(t_s, sv);
+        tc::ld128_wait(t_s, sv);
 #pragma unroll
         for (int c = 0; c < 4; ++c) prep(sv + 32 * c, c);
         if (j == w.kv_lo) {  // its first key is visible to every row: finite
@@ -522,17 +522,19 @@ tc::ld128_wait(t_s, sv);
       const bool store = (i == 0 || w.second_valid) && qrow < p.T_q;
       const size_t orow = ((size_t)w.b * p.H_q + h) * p.T_q + qrow;
       uint32_t ov[kD];
-tc::ld128_wait(t_o, ov);
+      tc::ld128_wait(t_o, ov);
       if (store && w.piece >= 0) {
         // a piece of a split unit: its partial (O not yet divided, m, l) for the merge
         const size_t prow = prefill_split::partial_row(w.piece, 2, i, row);
-        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * kD);
+        if (store_ok(prow, (size_t)(p.n_items - p.n_full) * 2 * kBM, p.wait.status)) {
+          float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * kD);
 #pragma unroll
-        for (int v4 = 0; v4 < kD / 4; ++v4)
-          dst[v4] = make_float4(__uint_as_float(ov[4 * v4 + 0]), __uint_as_float(ov[4 * v4 + 1]),
-                                __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
-        reinterpret_cast<float2 *>(p.ws_ml)[prow] = make_float2(m_ref, l);
-      } else if (store) {
+          for (int v4 = 0; v4 < kD / 4; ++v4)
+            dst[v4] = make_float4(__uint_as_float(ov[4 * v4 + 0]), __uint_as_float(ov[4 * v4 + 1]),
+                                  __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+          reinterpret_cast<float2 *>(p.ws_ml)[prow] = make_float2(m_ref, l);
+        }
+      } else if (store && store_ok(orow, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) {
         const float inv_l = 1.f / l;
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD);
 #pragma unroll

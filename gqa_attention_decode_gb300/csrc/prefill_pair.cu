@@ -535,13 +535,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qrow < p.T_q && w.piece >= 0) {
         // a piece of a split unit: its partial (O not yet divided, m, l) for the merge
         const size_t prow = prefill_split::partial_row(w.piece, 4, 2 * i + rank, row);
-        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * kD);
+        if (store_ok(prow, (size_t)(p.n_items - p.n_full) * 4 * kBM, p.wait.status)) {
+          float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * kD);
 #pragma unroll
-        for (int v4 = 0; v4 < kD / 4; ++v4)
-          dst[v4] = make_float4(__uint_as_float(ov[4 * v4 + 0]), __uint_as_float(ov[4 * v4 + 1]),
-                                __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
-        reinterpret_cast<float2 *>(p.ws_ml)[prow] = make_float2(m_ref, l);
-      } else if (qrow < p.T_q) {
+          for (int v4 = 0; v4 < kD / 4; ++v4)
+            dst[v4] = make_float4(__uint_as_float(ov[4 * v4 + 0]), __uint_as_float(ov[4 * v4 + 1]),
+                                  __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+          reinterpret_cast<float2 *>(p.ws_ml)[prow] = make_float2(m_ref, l);
+        }
+      } else if (qrow < p.T_q && store_ok(orow, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) {
         const float inv_l = 1.f / l;
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD);
 #pragma unroll

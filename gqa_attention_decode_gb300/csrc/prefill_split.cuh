@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const P p) {
   if (su >= (p.n_items - p.n_full) / s) return;
   size_t orow;
   if (!piece_out_row(p, p.n_full + su * s, hl, row, &orow)) return;
+  if (!store_ok(orow, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) return;
   float m = -INFINITY, l = 0.f;
   if (lane < s) {
     const float2 ml =

@@ -73,7 +73,9 @@ typedef enum {
   GQA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d != 128, G > 8)  */
   GQA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed                 */
   GQA_ERR_WORKSPACE = 4,   /* workspace smaller than the size function reports */
-  GQA_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out               */
+  GQA_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out               */
+  GQA_ERR_OUT_OF_BOUNDS = 6 /* bounds-checked builds: a kernel store index past
+                              its extent (the store is skipped)                 */
 } gqa_status_t;
 
 /* Human-readable name of a status code; never NULL, static storage. */
@@ -474,6 +476,20 @@ GQA_API int gqa_attn_device_status(gqa_stream_t stream, int *out_status);
  * word read by gqa_attn_device_status, and returns; nothing traps or hangs.
  */
 GQA_API int gqa_attn_selftest_bounded_wait(int timeout_us, gqa_stream_t stream);
+
+/*
+ * Bounds-checked builds (libgqa_attn_debug.so, compiled with GQA_DEBUG_BOUNDS)
+ * check, in every kernel, the index of each global store against the extent
+ * the kernel derives from its arguments; a store past it is skipped and
+ * GQA_ERR_OUT_OF_BOUNDS is recorded in the status word read by
+ * gqa_attn_device_status.  A stand-in for a memory checker: slower, same
+ * results.  gqa_attn_bounds_checked returns 1 in such a build, else 0.
+ * gqa_attn_selftest_bounds launches one store one element past its range, which
+ * a bounds-checked build records (and skips); release builds return
+ * GQA_ERR_UNSUPPORTED and launch nothing.
+ */
+GQA_API int gqa_attn_bounds_checked(void);
+GQA_API int gqa_attn_selftest_bounds(gqa_stream_t stream);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -278,6 +278,14 @@ def test_paged_multi_rejections(lib):
     assert call(64, 8, 16, 256, B=0) == gqa.GQA_OK
 
 
+def test_release_build_carries_no_bounds_checks(lib):
+    """The release library compiles the store checks away; its bounds self-test
+    refuses before any CUDA call (the bounds-checked build is libgqa_attn_debug.so)."""
+    assert gqa.gqa_attn_bounds_checked() is False
+    assert lib.gqa_attn_selftest_bounds(ctypes.c_void_p(0)) == gqa.GQA_ERR_UNSUPPORTED
+    assert "OUT_OF_BOUNDS" in gqa.gqa_status_string(gqa.GQA_ERR_OUT_OF_BOUNDS)
+
+
 def test_merge_states_rejects_before_any_cuda_call(lib):
     v = ctypes.c_void_p
     p = 1 << 20

@@ -1,0 +1,98 @@
+"""Every kernel path under the bounds-checked build (libgqa_attn_debug.so).
+
+That build checks, in every kernel, the index of each global store against the
+extent the kernel derives from its arguments and records a violation as
+GQA_ERR_OUT_OF_BOUNDS in the device status word (the store is skipped): a
+stand-in for a memory checker.  The calls below reach the warp-MMA and
+tcgen05 decode kernels (dense and paged, one and many tokens, the
+single-kernel cluster merge and split + merge), both causal prefill kernels
+with and without the key-range split, and the merge of shard states; none may
+record a violation, and sampled results must match the oracle.  The library
+is loaded in a child process (one library per process).
+"""
+import os
+import subprocess
+import sys
+import textwrap
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SCRIPT = textwrap.dedent("""
+    import math, sys
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import numpy as np, torch
+    import gqa_synth, oracle
+    import gqa_attention_decode_gb300 as gqa
+    from parity import compare
+
+    gqa.load_library()
+    assert gqa.gqa_attn_bounds_checked(), "not the bounds-checked build"
+    dev = torch.device("cuda", 0)
+    np64 = lambda t: t.detach().float().cpu().numpy().astype(np.float64)
+
+    def ok(what):
+        st = gqa.gqa_attn_device_status()
+        assert st == gqa.GQA_OK, (what, st)
+
+    # decode: cluster-merged single kernel, split + merge, T_q = 4, T_q = 16 (tcgen05)
+    for (B, H_q, H_kv, S, T_q, splits) in [(1, 8, 1, 256, 1, 4), (2, 64, 8, 4096, 1, 0),
+                                            (2, 64, 8, 4096, 4, 0), (1, 64, 8, 4096, 16, 0),
+                                            (3, 32, 2, 2048, 1, 40)]:
+        q = gqa_synth.bf16_normal((B, H_q, T_q, 128), 1, dev)
+        _, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S, 128, 2, dev,
+                                              [S] + [S // 3] * (B - 1))
+        o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(dev), 0.088, splits)
+        torch.cuda.synchronize()
+        ok(("decode", B, H_q, H_kv, S, T_q, splits))
+        o_ref, l_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 0.088)
+        compare(o, lse, o_ref, l_ref, "debug decode")
+        # the same cache, paged (256-key pages in pool order)
+        mp = S // 256
+        kp = k.view(B, H_kv, mp, 256, 128).permute(0, 2, 1, 3, 4).reshape(B * mp, H_kv, 256, 128).contiguous()
+        vp = v.view(B, H_kv, mp, 256, 128).permute(0, 2, 1, 3, 4).reshape(B * mp, H_kv, 256, 128).contiguous()
+        table = torch.arange(B * mp, dtype=torch.int32, device=dev).view(B, mp)
+        o2, l2 = gqa.gqa_attn_decode_paged_multi(q, kp, vp, table, sl.to(dev), 0.088, splits)
+        torch.cuda.synchronize()
+        ok(("paged decode", B, H_q, H_kv, S, T_q, splits))
+        assert torch.equal(o2, o) and torch.equal(l2, lse)
+
+    # prefill: CTA pairs (G = 8, 4) and one CTA per unit (G = 3, 1), whole and split
+    for (H_q, H_kv, T, S) in [(16, 2, 300, 300), (8, 2, 128, 4096), (6, 2, 200, 200),
+                              (6, 2, 128, 4096), (4, 4, 256, 2304), (16, 2, 200, 3000)]:
+        qo = S - T
+        q, k, v = gqa_synth.prefill_inputs(1, H_q, H_kv, T, S, 128, seed=3, device=dev)
+        o, lse = gqa.gqa_attn_prefill_causal(q, k, v, 0.088, qo)
+        torch.cuda.synchronize()
+        ok(("prefill", H_q, H_kv, T, S))
+        o_ref, l_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), qo, 0.088)
+        compare(o, lse, o_ref, l_ref, "debug prefill")
+
+    # merge of shard states
+    parts = torch.randn((3, 1000, 128), device=dev).to(torch.bfloat16)
+    lses = torch.randn((3, 1000), device=dev)
+    gqa.gqa_attn_merge_states(parts, lses)
+    torch.cuda.synchronize()
+    ok("merge states")
+
+    # the check itself: one store one element past its range is recorded
+    gqa.gqa_attn_selftest_bounds()
+    assert gqa.gqa_attn_device_status() == gqa.GQA_ERR_OUT_OF_BOUNDS
+    assert gqa.gqa_attn_device_status() == gqa.GQA_OK     # read and cleared
+    print("debug-bounds ok")
+""")
+
+
+def test_every_path_under_the_bounds_checked_build():
+    sys.path.insert(0, ROOT)
+    from gqa_attention_decode_gb300 import build
+    lib = build.build(debug_bounds=True)
+    env = dict(os.environ, GQA_ATTN_LIB=lib)
+    r = subprocess.run([sys.executable, "-c", f"import os\nROOT = {ROOT!r}\n" + SCRIPT],
+                       env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert "debug-bounds ok" in r.stdout
