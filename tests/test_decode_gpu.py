@@ -238,3 +238,33 @@ def test_one_million_keys_sampled():
         del kk, vv
     compare(torch.stack([o[0, h] for h in picks]), torch.stack([lse[0, h] for h in picks]),
             ref_o, ref_lse, "2^20 keys")
+
+
+def test_l2_prefetch_sees_the_preceding_grids_writes():
+    """A one-wave decode prefetches its first K/V tiles into L2 before its
+    grid-dependency wait, while the preceding grid may still be writing.  Here
+    the preceding grid (a merge of shard states, which lets its dependents
+    launch at its start) writes the very K cache the decode reads, over a
+    buffer that held NaN: the decode must see the new keys."""
+    H_q, H_kv, S, d = 64, 8, 8192, 128
+    # 19 splits x 8 KV heads = one wave of split CTAs (the prefetching path), then the merge
+    assert gqa.gqa_attn_decode_kernel_count(1, H_q, H_kv, S, d, 0, DEV) == 2
+    g = torch.Generator(device="cpu").manual_seed(77)
+    parts = torch.randn((1, H_kv * S, d), generator=g).to(torch.bfloat16).to(DEV)
+    lse_parts = torch.zeros((1, H_kv * S), dtype=torch.float32, device=DEV)
+    q, _, v, sl = gqa_synth.decode_inputs(1, H_q, H_kv, S, d, seed=78, device=DEV)
+    k_buf = torch.full((H_kv * S, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse_out = torch.empty((H_kv * S,), dtype=torch.float32, device=DEV)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        k_buf.fill_(float("nan"))
+        # merge of a single shard: writes parts[0] into k_buf (the identity)
+        gqa.gqa_attn_merge_states(parts, lse_parts, k_buf, lse_out)
+        o, lse = gqa.gqa_attn_decode(q, k_buf.view(1, H_kv, S, d), v, sl.to(DEV),
+                                     1 / math.sqrt(d))
+        torch.cuda.synchronize()
+        assert torch.equal(k_buf, parts[0])
+        assert torch.isfinite(o.float()).all()
+    o_ref, lse_ref = oracle.decode(np64(q), np64(parts[0].view(1, H_kv, S, d)), np64(v),
+                                   sl.numpy(), 1 / math.sqrt(d))
+    compare(o, lse, o_ref, lse_ref, "decode after a grid writing its K cache")
