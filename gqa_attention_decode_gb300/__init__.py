@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     gqa_attn_decode_noalloc,
     GQA_NOALLOC_SCRATCH_BYTES,
     gqa_attn_prefill_causal,
+    gqa_attn_prefill_causal_paged,
     gqa_attn_merge_states,
     gqa_attn_prefill_causal_workspace_size,
     gqa_attn_prefill_causal_kernel_count,

@@ -58,6 +58,8 @@ _SIGNATURES = {
                                             _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp,
                                             _c_size, _vp]),
     "gqa_attn_prefill_causal_kernel_count": (_c_int, [_c_int] * 7 + [_c_size, _ip]),
+    "gqa_attn_prefill_causal_paged": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 10 +
+                                      [_c_float, _vp, _vp, _vp, _c_size, _vp]),
     "gqa_attn_prefill_causal_plan": (_c_int, [_c_int] * 8 + [_c_size, _ip, _ip, _ip]),
     "gqa_attn_decode_from_host_arena_size": (_c_size, [_c_int] * 7),
     "gqa_attn_decode_from_host": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
@@ -482,6 +484,43 @@ def gqa_attn_merge_states(o_parts, lse_parts, o=None, lse=None, stream=None):
         rc = lib.gqa_attn_merge_states(_ptr(o_parts), _ptr(lse_parts), P, rows, d, _ptr(o),
                                        _ptr(lse), _stream_handle(stream, dev))
     _check(rc, "gqa_attn_merge_states")
+    return o, lse
+
+
+def gqa_attn_prefill_causal_paged(q, k_pages, v_pages, block_table, S_kv, scale, q_offset=0,
+                                  o=None, lse=None, workspace=None, stream=None):
+    """Causal prefill over a paged cache.  q [B,H_q,T_q,d]; k_pages, v_pages
+    [num_pages,H_kv,page_size,d] bf16; block_table [B, max_pages_per_seq] int32;
+    every sequence has S_kv keys.  Row i of q is at absolute position q_offset + i."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    _need(k_pages, "k_pages", torch.bfloat16, 4, dev)
+    _need(v_pages, "v_pages", torch.bfloat16, 4, dev)
+    _need(block_table, "block_table", torch.int32, 2, dev)
+    B, H_q, T_q, d = q.shape
+    num_pages, H_kv, page_size, _ = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or k_pages.shape[3] != d:
+        raise ValueError("k_pages/v_pages must be [num_pages, H_kv, page_size, d]")
+    if block_table.shape[0] != B:
+        raise ValueError("block_table needs B rows")
+    if o is None:
+        o = torch.empty((B, H_q, T_q, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=dev)
+    if workspace is None:
+        nbytes = gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, d,
+                                                        int(q_offset), _num_sms(dev))
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, 1, dev)
+    ws_ptr = _ptr(workspace) if workspace.numel() > 0 else None
+    with torch.cuda.device(dev):
+        rc = lib.gqa_attn_prefill_causal_paged(
+            _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), B, H_q, H_kv, T_q,
+            int(S_kv), num_pages, page_size, block_table.shape[1], d, int(q_offset),
+            float(scale), _ptr(o), _ptr(lse), ws_ptr, workspace.numel(),
+            _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_prefill_causal_paged")
     return o, lse
 
 

@@ -528,6 +528,35 @@ GQA_API int gqa_attn_prefill_causal_ws(const gqa_bf16_t *q, const gqa_bf16_t *k,
   return to_status(e);
 }
 
+GQA_API int gqa_attn_prefill_causal_paged(
+    const gqa_bf16_t *q, const gqa_bf16_t *k_pages, const gqa_bf16_t *v_pages,
+    const int32_t *block_table, int B, int H_q, int H_kv, int T_q, int S_kv, int num_pages,
+    int page_size, int max_pages_per_seq, int d, int q_offset, float scale, gqa_bf16_t *o,
+    float *lse, void *workspace, size_t ws_bytes, gqa_stream_t stream) {
+  int rc = check_prefill_args(q, k_pages, v_pages, B, H_q, H_kv, T_q, S_kv, d, q_offset, scale,
+                              o, lse);
+  if (rc != GQA_OK || B == 0 || T_q == 0) return rc;
+  if (page_size <= 0 || num_pages < 0 || max_pages_per_seq < 0) return GQA_ERR_INVALID_ARG;
+  if ((long long)max_pages_per_seq * page_size < S_kv) return GQA_ERR_INVALID_ARG;
+  if (num_pages == 0 || !block_table || !aligned16(block_table)) return GQA_ERR_INVALID_ARG;
+  if (page_size % 128 != 0) return GQA_ERR_UNSUPPORTED;  // a key tile must not straddle pages
+  if ((long long)num_pages * H_kv >= 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  if ((ws_bytes > 0 && !workspace) || (workspace && !aligned16(workspace)))
+    return GQA_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  if ((rc = device_state(&st)) != GQA_OK) return rc;
+  gqa::PrefillLaunch a = prefill_launch_args(q, k_pages, v_pages, B, H_q, H_kv, T_q, S_kv,
+                                             q_offset, scale, o, lse, workspace, ws_bytes, st);
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages_per_seq;
+  a.num_pages = num_pages;
+  // paged K/V: one CTA per unit for every group size
+  cudaError_t e = gqa::prefill_launch(a, static_cast<cudaStream_t>(stream), g_encode);
+  if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+  return to_status(e);
+}
+
 GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
                                     const gqa_bf16_t *v, int B, int H_q, int H_kv, int T_q,
                                     int S_kv, int d, int q_offset, float scale, gqa_bf16_t *o,

@@ -74,6 +74,10 @@ struct PrefillLaunch {
   int max_pairs;  // CTA-pair kernel: clusters of two resident at once (0: not available)
   void *ws;         // optional scratch for key-split pieces (nullptr: no split)
   size_t ws_bytes;
+  // paged K/V (single-CTA kernel only): [num_pages, H_kv, page_size, d] pages,
+  // block table [B, max_pages]; nullptr: dense K/V
+  const int32_t *block_table;
+  int page_size, max_pages, num_pages;
   WaitCtl wait;
 };
 

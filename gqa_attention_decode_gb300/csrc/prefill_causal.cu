@@ -79,6 +79,18 @@ struct Params {
   WaitCtl wait;
 };
 
+// Paged K/V ([num_pages, H_kv, page_size, d], page_size a multiple of 128): keys
+// [i*page_size, (i+1)*page_size) of sequence b are in page block_table[b *
+// max_pages + i].  Empty for the dense kernel, whose parameters (and register
+// allocation) it leaves untouched.
+template <bool kPaged>
+struct PageArgs {
+  const int32_t *block_table;
+  int page_size, max_pages, num_pages;
+};
+template <>
+struct PageArgs<false> {};
+
 // Two slots of 128 query rows: slot i is query tile qt_i of head h_i.  Either
 // two heads of a KV group on one query tile, or (G odd) the group's last head
 // on query tiles qt and qt - 1, which read the same key tiles (the lower one
@@ -195,10 +207,14 @@ __device__ __forceinline__ constexpr uint32_t mnmajor_step(int kk) { return kk *
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
+// kPaged: K/V in pages through pg.block_table (a separate instantiation, so the
+// dense kernel carries none of the page handling)
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                          const __grid_constant__ CUtensorMap tm_v, const Params p,
+                          const PageArgs<kPaged> pg) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -278,9 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = sbase + kOffStage + s * kTileBytes;
             mbar_arrive_expect_tx(kv_full(s), kTileBytes);
             const CUtensorMap *map = which == 0 ? &tm_k : &tm_v;
+            int c2 = j * kBN, c3 = w.b * p.H_kv + w.kv;  // the tile's first key row and block
+            if constexpr (kPaged) {
+              // a 128-key tile lies in one page (page sizes are multiples of 128); a
+              // page id outside the pool reads zeros (a block past the tensor map)
+              // and is reported through the status word
+              const int page = j * kBN / pg.page_size;
+              const int page_id = __ldca(pg.block_table + (size_t)w.b * pg.max_pages + page);
+              const bool bad = page_id < 0 || page_id >= pg.num_pages;
+              if (bad) atomicExch(p.wait.status, kStatusInvalidArg);
+              c2 = j * kBN - page * pg.page_size;
+              c3 = bad ? pg.num_pages * p.H_kv : page_id * p.H_kv + w.kv;
+            }
             for (int half = 0; half < 2; ++half)
-              tma_load_4d(dst + half * kHalfBytes, map, kv_full(s), 0, half, j * kBN,
-                          w.b * p.H_kv + w.kv, pol_kv);
+              tma_load_4d(dst + half * kHalfBytes, map, kv_full(s), 0, half, c2, c3, pol_kv);
           }
         }
       }
@@ -507,6 +534,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive(tok(1 - i));  // the exp unit is free: the other warpgroup may start
         tc::st64(t_s, pk);
+        if constexpr (kPaged) if (i == 0 && (j + 1) * kBN > p.S_kv) {
+          // Paged K/V: the rows of this tile past the sequence come from the page's
+          // unused slots (any bits, NaN included), and P V multiplies them by zero:
+          // clear them in the V stage (load 2 * tile + 1) before P V reads it.  Slot
+          // 0's P V is the first to read the stage and waits for this signal.
+          const int ldv = 2 * tile + 1;
+          const bool landed = wait_abortable(kv_full(ldv % kStages), (ldv / kStages) & 1, p.wait,
+                                             abort_flag);
+          if (landed) {
+            uint8_t *vt = smem + kOffStage + (ldv % kStages) * kTileBytes;
+            const int first = p.S_kv - j * kBN;  // first row past the sequence
+            for (int idx = threadIdx.x; idx < (kBN - first) * 16; idx += 128) {
+              const int r = first + idx / 16, c = idx % 16;  // 16 chunks of 16 B per row
+              *reinterpret_cast<uint4 *>(vt + (c >> 3) * kHalfBytes + r * 128 + (c & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // the tensor core reads these rows
+          }
+        }
         tc::wait_st();
         l += tsum;
         tc::fence_before_sync();
@@ -579,7 +625,11 @@ CUresult make_map(CUtensorMap *map, const uint16_t *base, int rows, int heads,
 }  // namespace prefill
 
 cudaError_t prefill_prepare_device() {
-  return cudaFuncSetAttribute(prefill::prefill_causal_kernel,
+  cudaError_t e = cudaFuncSetAttribute(prefill::prefill_causal_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       prefill::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill::prefill_causal_kernel<true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, prefill::kSmemBytes);
 }
 
@@ -609,10 +659,16 @@ cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
   using namespace prefill;
   const PrefillPlan pl = prefill_plan(a);
   if (pl.units <= 0) return cudaErrorNotSupported;
+  const bool paged = a.block_table != nullptr;
+  if (paged && (a.page_size <= 0 || a.page_size % kBN != 0)) return cudaErrorInvalidValue;
+  // K/V blocks of rows: one per (sequence, KV head) of S_kv keys, or one per
+  // (page, KV head) of page_size keys
+  const int kv_rows = paged ? a.page_size : a.S_kv;
+  const int kv_blocks = paged ? a.num_pages * a.H_kv : a.B * a.H_kv;
   CUtensorMap tm_q, tm_k, tm_v;
   if (make_map(&tm_q, a.q, a.T_q, a.B * a.H_q, encode) != CUDA_SUCCESS ||
-      make_map(&tm_k, a.k, a.S_kv, a.B * a.H_kv, encode) != CUDA_SUCCESS ||
-      make_map(&tm_v, a.v, a.S_kv, a.B * a.H_kv, encode) != CUDA_SUCCESS)
+      make_map(&tm_k, a.k, kv_rows, kv_blocks, encode) != CUDA_SUCCESS ||
+      make_map(&tm_v, a.v, kv_rows, kv_blocks, encode) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   Params p;
   p.o = a.o;
@@ -634,7 +690,14 @@ cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
   p.ws_ml = pl.pieces > 0 ? p.ws_o + (size_t)pl.pieces * 2 * kBM * kD : nullptr;
   p.sl2 = a.scale * 1.4426950408889634f;
   p.wait = a.wait;
-  prefill_causal_kernel<<<pl.workers, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+  if (paged) {
+    const PageArgs<true> pg{a.block_table, a.page_size, a.max_pages, a.num_pages};
+    prefill_causal_kernel<true>
+        <<<pl.workers, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p, pg);
+  } else {
+    prefill_causal_kernel<false>
+        <<<pl.workers, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p, PageArgs<false>{});
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the pieces' merge, a programmatic dependent of the prefill kernel

@@ -623,7 +623,8 @@ cudaError_t prefill_pair_prepare_device(int *max_pairs) {
 }
 
 bool prefill_pair_eligible(const PrefillLaunch &a) {
-  return a.H_kv > 0 && (a.H_q / a.H_kv) % 4 == 0 && a.max_pairs > 0;
+  // dense K/V only (a paged cache runs on the single-CTA kernel)
+  return a.H_kv > 0 && (a.H_q / a.H_kv) % 4 == 0 && a.max_pairs > 0 && a.block_table == nullptr;
 }
 
 // Work plan: units of one 128-row query tile of four heads over the resident

@@ -378,6 +378,33 @@ GQA_API int gqa_attn_prefill_causal_ws(const gqa_bf16_t *q, const gqa_bf16_t *k,
                                        gqa_stream_t stream);
 
 /*
+ * Causal prefill over a paged KV cache (block table): the chunked prefill of a
+ * serving engine, whose prefix (and, once appended, the chunk's own keys) live
+ * in the same pages as decode reads (see gqa_attn_decode_paged).
+ *
+ *   k_pages, v_pages   device [num_pages, H_kv, page_size, d] bf16; read only.
+ *   block_table        device [B, max_pages_per_seq] int32: keys
+ *                      [i*page_size, (i+1)*page_size) of sequence b are in page
+ *                      block_table[b*max_pages_per_seq + i]; entries past key
+ *                      S_kv - 1 are never read.  An entry outside
+ *                      [0, num_pages) reads zeros and is reported as
+ *                      GQA_ERR_INVALID_ARG by gqa_attn_device_status.
+ *   S_kv               keys of every sequence (<= max_pages_per_seq * page_size);
+ *                      rows of the last page past it may hold any bits (they
+ *                      are cleared before use).
+ *   page_size          a positive multiple of 128 (else GQA_ERR_UNSUPPORTED).
+ *   num_pages * H_kv   below 2^31.
+ * Everything else is that of gqa_attn_prefill_causal_ws (the workspace size of
+ * gqa_attn_prefill_causal_workspace_size serves).  Runs the one-CTA-per-unit
+ * kernel for every group size.
+ */
+GQA_API int gqa_attn_prefill_causal_paged(
+    const gqa_bf16_t *q, const gqa_bf16_t *k_pages, const gqa_bf16_t *v_pages,
+    const int32_t *block_table, int B, int H_q, int H_kv, int T_q, int S_kv, int num_pages,
+    int page_size, int max_pages_per_seq, int d, int q_offset, float scale, gqa_bf16_t *o,
+    float *lse, void *workspace, size_t ws_bytes, gqa_stream_t stream);
+
+/*
  * Kernels one gqa_attn_prefill_causal_ws call with `ws_bytes` of workspace
  * launches on the current device: 1, 2 (split + merge), 0 for an empty
  * problem.  Initialises the library's per-device state (a CUDA call).

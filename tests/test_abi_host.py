@@ -286,6 +286,21 @@ def test_release_build_carries_no_bounds_checks(lib):
     assert "OUT_OF_BOUNDS" in gqa.gqa_status_string(gqa.GQA_ERR_OUT_OF_BOUNDS)
 
 
+def test_paged_prefill_rejects_before_any_cuda_call(lib):
+    v = ctypes.c_void_p
+    p = 1 << 20
+    def call(table=p, S_kv=1024, num_pages=8, page_size=256, max_pages=4, d=128, B=1):
+        return lib.gqa_attn_prefill_causal_paged(v(p), v(p), v(p), v(table), B, 8, 2, 128, S_kv,
+                                                 num_pages, page_size, max_pages, d, S_kv - 128,
+                                                 0.088, v(p), v(p), v(0), 0, v(0))
+    assert call(table=0) == gqa.GQA_ERR_INVALID_ARG
+    assert call(S_kv=2048) == gqa.GQA_ERR_INVALID_ARG            # past max_pages * page_size
+    assert call(num_pages=0) == gqa.GQA_ERR_INVALID_ARG
+    assert call(page_size=64, max_pages=16) == gqa.GQA_ERR_UNSUPPORTED  # tiles straddle pages
+    assert call(d=64) == gqa.GQA_ERR_UNSUPPORTED
+    assert call(B=0) == gqa.GQA_OK
+
+
 def test_merge_states_rejects_before_any_cuda_call(lib):
     v = ctypes.c_void_p
     p = 1 << 20

@@ -72,6 +72,21 @@ SCRIPT = textwrap.dedent("""
         o_ref, l_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), qo, 0.088)
         compare(o, lse, o_ref, l_ref, "debug prefill")
 
+    # prefill over a paged cache (pool in order, 256-key pages, a ragged last page)
+    q, k, v = gqa_synth.prefill_inputs(1, 6, 2, 200, 1000, 128, seed=4, device=dev)
+    kp = torch.zeros((4, 2, 256, 128), dtype=k.dtype, device=dev)
+    vp = torch.zeros_like(kp)
+    for i in range(4):
+        n = min(256, 1000 - 256 * i)
+        kp[i, :, :n] = k[0, :, 256 * i:256 * i + n]
+        vp[i, :, :n] = v[0, :, 256 * i:256 * i + n]
+    table = torch.arange(4, dtype=torch.int32, device=dev).view(1, 4)
+    o, lse = gqa.gqa_attn_prefill_causal_paged(q, kp, vp, table, 1000, 0.088, 800)
+    torch.cuda.synchronize()
+    ok("paged prefill")
+    o_ref, l_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), 800, 0.088)
+    compare(o, lse, o_ref, l_ref, "debug paged prefill")
+
     # merge of shard states
     parts = torch.randn((3, 1000, 128), device=dev).to(torch.bfloat16)
     lses = torch.randn((3, 1000), device=dev)
