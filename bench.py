@@ -654,7 +654,7 @@ def run_all_configs(device):
                      if len(kvs) * kv_bytes > 2 * l2_bytes else
                      "L2 resident (latency-bound)")})
 
-    def prefill_line(name):
+    def prefill_line(name, page_size=0):
         w = gqa_synth.WORKLOADS[name]
         q, k, v = gqa_synth.workload_prefill_inputs(w, device)
         o = torch.empty_like(q)
@@ -664,11 +664,27 @@ def run_all_configs(device):
         ws = torch.empty(nb, dtype=torch.uint8, device=device)
         kernels = gqa.gqa_attn_prefill_causal_kernel_count(w.B, w.H_q, w.H_kv, w.T_q, w.S_kv,
                                                            w.d, w.q_offset, nb, device)
-        fn = lambda: gqa.gqa_attn_prefill_causal(q, k, v, w.scale, w.q_offset, o, lse, ws)
+        kernel = prefill_kernel_name(w.G)
+        if page_size:   # the same K/V in a pool of pages (in order), read through a block table
+            mp = -(-w.S_kv // page_size)
+            kp = torch.zeros((w.B * mp, w.H_kv, page_size, w.d), dtype=k.dtype, device=device)
+            vp = torch.zeros_like(kp)
+            for b in range(w.B):
+                for i in range(mp):
+                    n = min(page_size, w.S_kv - i * page_size)
+                    kp[b * mp + i, :, :n] = k[b, :, i * page_size:i * page_size + n]
+                    vp[b * mp + i, :, :n] = v[b, :, i * page_size:i * page_size + n]
+            table = torch.arange(w.B * mp, dtype=torch.int32, device=device).view(w.B, mp)
+            fn = lambda: gqa.gqa_attn_prefill_causal_paged(q, kp, vp, table, w.S_kv, w.scale,
+                                                           w.q_offset, o, lse, ws)
+            name = f"{name} paged({page_size})"
+            kernel = "prefill_causal_kernel"
+        else:
+            fn = lambda: gqa.gqa_attn_prefill_causal(q, k, v, w.scale, w.q_offset, o, lse, ws)
         us = time_graph(fn, 1, 10)
         tf = prefill_flops(w) / us / 1e6
         emit({"workload": name, "us_per_call": us, "value": tf, "unit": "TFLOP/s",
-              "bound": "tensor", "kernel": prefill_kernel_name(w.G), "kernels_per_call": kernels,
+              "bound": "tensor", "kernel": kernel, "kernels_per_call": kernels,
               "peak": peaks["bf16_tflops"], "frac": tf / peaks["bf16_tflops"],
               "frac_of_sustained": tf / peaks["bf16_tflops_sustained"],
               "flops_per_call": prefill_flops(w)})
@@ -682,6 +698,7 @@ def run_all_configs(device):
     decode_line("llama70b_decode_32k", T_q=16)
     decode_line("llama70b_decode_32k", page_size=256)
     decode_line("llama70b_decode_32k", T_q=16, page_size=256)
+    prefill_line("chunked_prefill_32k", page_size=256)
 
 
 def main():
