@@ -134,20 +134,29 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   if (warp == n_consumers && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    // Dense cache, one-wave grid: pull the first tiles of this split's key range
-    // into L2 while the preceding grid finishes (its length is not known yet,
-    // so the range is the split's whole chunk; keys past the sequence are
-    // masked later).  Only a grid that is resident all at once can overlap the
+    // One-wave grid: pull the first tiles of this split's key range into L2
+    // while the preceding grid finishes (its length is not known yet, so the
+    // range is the split's whole chunk; keys past the sequence are masked
+    // later).  Only a grid that is resident all at once can overlap the
     // preceding grid; in a larger one, splits past their sequence's end would
-    // only prefetch padding.
-    if (!kPaged) {
-      const int tiles = min(p.l2_prefetch_tiles, p.chunk / kTileKeys);
-      for (int i = 0; i < tiles; ++i) {
-        const int key0 = split * p.chunk + i * kTileKeys;
-        for (int half = 0; half < 2; ++half) {
-          tma_prefetch_l2_4d(&tm_k, 0, half, key0, b * p.H_kv + kv);
-          tma_prefetch_l2_4d(&tm_v, 0, half, key0, b * p.H_kv + kv);
-        }
+    // only prefetch padding.  A paged cache's table is read here ahead of the
+    // wait as a hint only (relaxed loads, ids outside the pool skipped): the
+    // loads that matter read it again after the wait.
+    const int tiles = min(p.l2_prefetch_tiles, p.chunk / kTileKeys);
+    for (int i = 0; i < tiles; ++i) {
+      const int key0 = split * p.chunk + i * kTileKeys;
+      int c2 = key0, c3 = b * p.H_kv + kv;
+      if (kPaged) {
+        const int page = key0 / p.page_size;
+        if (page >= p.max_pages) break;
+        const int page_id = ld_relaxed_s32(p.block_table + (size_t)b * p.max_pages + page);
+        if (page_id < 0 || page_id >= p.num_pages) continue;
+        c2 = key0 - page * p.page_size;
+        c3 = page_id * p.H_kv + kv;
+      }
+      for (int half = 0; half < 2; ++half) {
+        tma_prefetch_l2_4d(&tm_k, 0, half, c2, c3);
+        tma_prefetch_l2_4d(&tm_v, 0, half, c2, c3);
       }
     }
   }

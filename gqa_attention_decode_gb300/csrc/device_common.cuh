@@ -125,6 +125,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// A relaxed (morally strong) load of a value another grid may be writing:
+// either the old or the new value, for use as a hint only.
+__device__ __forceinline__ int ld_relaxed_s32(const int32_t *p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Prefetch of a tile into L2 (no shared memory, no completion to wait for).
 // Safe ahead of a grid-dependency wait: L2 is the point of coherence, so a later
 // write by the preceding grid still reaches every load that follows the wait.
