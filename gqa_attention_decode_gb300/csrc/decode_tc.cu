@@ -63,7 +63,7 @@ struct Params {
   float *lse_part;
   int B, H_q, H_kv, G, T_q, S_max, num_splits, chunk;
   int page_size, max_pages, num_pages;
-  int l2_prefetch;  // one-wave grid on a dense cache: prefetch the first key tile
+  int l2_prefetch;  // one-wave grid: prefetch the first key tile before the wait
   float sl2;  // scale * log2(e)
   WaitCtl wait;
 };
@@ -126,14 +126,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Dense cache, one-wave grid: the first key tile of this split's chunk is
-  // pulled into L2 while the preceding grid finishes (L2 is the point of
-  // coherence, so this is safe ahead of the wait; the sequence length is not
-  // known yet).
+  // One-wave grid: the first key tile of this split's chunk is pulled into L2
+  // while the preceding grid finishes (L2 is the point of coherence, so this is
+  // safe ahead of the wait; the sequence length is not known yet).  A paged
+  // cache's block-table entry is read here as a hint only: a preceding grid
+  // may still write it, and the loads after the wait read it again, so a stale
+  // entry costs one wasted L2 fill; an id outside the pool is skipped.
   if (p.l2_prefetch && warp == kWarpTma && lane == 0 && p.chunk >= kBN) {
-    for (int half = 0; half < 2; ++half) {
-      tma_prefetch_l2_4d(&tm_k, 0, half, split * p.chunk, b * p.H_kv + kv);
-      tma_prefetch_l2_4d(&tm_v, 0, half, split * p.chunk, b * p.H_kv + kv);
+    const int key0 = split * p.chunk;
+    int c2 = key0, c3 = b * p.H_kv + kv;
+    bool go = true;
+    if (p.block_table != nullptr) {
+      const int page = key0 / p.page_size;
+      const int page_id =
+          page < p.max_pages ? ld_relaxed_s32(p.block_table + (size_t)b * p.max_pages + page) : -1;
+      go = page_id >= 0 && page_id < p.num_pages;
+      c2 = key0 - page * p.page_size;
+      c3 = page_id * p.H_kv + kv;
+    }
+    for (int half = 0; go && half < 2; ++half) {
+      tma_prefetch_l2_4d(&tm_k, 0, half, c2, c3);
+      tma_prefetch_l2_4d(&tm_v, 0, half, c2, c3);
     }
   }
   // inputs written by earlier grids are visible after this wait (coherent loads)
@@ -539,7 +552,7 @@ cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
-  p.l2_prefetch = !paged && (long long)a.num_splits * a.H_kv * a.B <= a.num_sms;
+  p.l2_prefetch = (long long)a.num_splits * a.H_kv * a.B <= a.num_sms;
   p.o_part = a.o_part;
   p.lse_part = a.lse_part;
   p.B = a.B;

@@ -202,3 +202,54 @@ def test_page_id_outside_pool_is_reported_tensor_core_path():
     v1 = torch.stack([torch.cat([vp[int(p)] for p in tcpu[1]], dim=1)])
     o_ref, lse_ref = oracle.decode_multi(np64(q[1:]), np64(k1), np64(v1), sl.numpy()[1:], 0.1)
     compare(o[1:], l[1:], o_ref, lse_ref, "sequence with valid pages (tensor cores)")
+
+
+def test_l2_prefetch_reads_the_block_table_the_preceding_grid_writes():
+    """A one-wave decode reads the block-table entries of its first tiles before
+    its grid-dependency wait (an L2 prefetch hint) while the preceding grid may
+    still be writing the table.  Here the preceding grid (a merge of shard
+    states, which lets its dependents launch at its start) writes the table
+    over one that points at NaN pages: the decode must read the new table.
+    The table's int32 ids are written as the bf16 halves of one merge row
+    (ids 128..191: every half is a normal bf16 or +0, copied exactly)."""
+    B, H_q, H_kv, S, d, ps = 2, 64, 8, 8192, 128, 256
+    splits, _ = gqa.gqa_attn_decode_plan(B, H_kv, S, torch.cuda.get_device_properties(0)
+                                         .multi_processor_count)
+    assert splits * H_kv * B <= torch.cuda.get_device_properties(0).multi_processor_count
+    q, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S, d, seed=79, device=DEV)
+    q16 = gqa_synth.bf16_normal((B, H_q, 16, d), 80, DEV)
+    mp = S // ps
+    perm = torch.randperm(B * mp, generator=torch.Generator().manual_seed(81))
+    true_table = (128 + perm).to(torch.int32).view(B, mp)
+    kp = torch.full((128 + B * mp, H_kv, ps, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    vp = torch.full_like(kp, float("nan"))
+    for b in range(B):
+        for i in range(mp):
+            kp[int(true_table[b, i])] = k[b, :, i * ps:(i + 1) * ps]
+            vp[int(true_table[b, i])] = v[b, :, i * ps:(i + 1) * ps]
+    parts = true_table.to(DEV).view(torch.bfloat16).reshape(1, 1, d)
+    assert parts.shape[-1] == d
+    lse_parts = torch.zeros((1, 1), dtype=torch.float32, device=DEV)
+    table = torch.empty((B, mp), dtype=torch.int32, device=DEV)
+    stale = torch.arange(B * mp, dtype=torch.int32, device=DEV).view(B, mp)   # NaN pages
+    lse_out = torch.empty((1,), dtype=torch.float32, device=DEV)
+    sl_d = sl.to(DEV)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for qq in (q, q16):
+            table.copy_(stale)
+            gqa.gqa_attn_merge_states(parts, lse_parts, table.view(torch.bfloat16).view(1, d),
+                                      lse_out)
+            if qq.dim() == 3:
+                o, lse = gqa.gqa_attn_decode_paged(qq, kp, vp, table, sl_d, 1 / math.sqrt(d))
+            else:
+                o16, lse16 = gqa.gqa_attn_decode_paged_multi(qq, kp, vp, table, sl_d,
+                                                             1 / math.sqrt(d))
+            torch.cuda.synchronize()
+            assert torch.equal(table.cpu(), true_table)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(o16.float()).all()
+    o_ref, lse_ref = oracle.decode(np64(q), np64(k), np64(v), sl.numpy(), 1 / math.sqrt(d))
+    compare(o, lse, o_ref, lse_ref, "paged decode after a grid writing its block table")
+    o_ref, lse_ref = oracle.decode_multi(np64(q16), np64(k), np64(v), sl.numpy(),
+                                         1 / math.sqrt(d))
+    compare(o16, lse16, o_ref, lse_ref, "paged 16-token decode after a grid writing its table")
