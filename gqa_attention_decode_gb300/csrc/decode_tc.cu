@@ -126,6 +126,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
   // One-wave grid: the first key tile of this split's chunk is pulled into L2
   // while the preceding grid finishes (L2 is the point of coherence, so this is
   // safe ahead of the wait; the sequence length is not known yet).  A paged
@@ -149,23 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_l2_4d(&tm_v, 0, half, c2, c3);
     }
   }
-  // inputs written by earlier grids are visible after this wait (coherent loads)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int seqlen_in = __ldca(p.seqlens + b);
-  // out-of-range lengths are clamped and reported through the status word
-  if ((seqlen_in < 0 || seqlen_in > p.S_max) && threadIdx.x == 0 && split == 0)
-    atomicExch(p.wait.status, kStatusInvalidArg);
-  const int seqlen = min(max(seqlen_in, 0), p.S_max);
-  const int key_begin = split * p.chunk;
-  const int key_end = min(key_begin + p.chunk, seqlen);
-  if (key_begin >= key_end) return;  // empty split: the merge never reads it
-  const int n_tiles = (key_end - key_begin + kBN - 1) / kBN;
-  const int n_slot[2] = {(n_tiles + 1) / 2, n_tiles / 2};  // slot s: tiles j with j % 2 == s
-  const int R = p.G * p.T_q;                                 // rows that are stored
-  // the last tile may run past the sequence: its V rows there (cache rows that
-  // may hold any bits) are cleared before P V reads them
-  const int tail_keys = key_begin + n_tiles * kBN - seqlen;  // > 0: rows to clear
-
+  // Barriers and tensor memory are set up before the grid-dependency wait: none
+  // of it reads another grid's output.
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(kv_full(s), 1);
@@ -192,6 +182,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // inputs written by earlier grids are visible after this wait (coherent loads)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int seqlen_in = __ldca(p.seqlens + b);
+  // out-of-range lengths are clamped and reported through the status word
+  if ((seqlen_in < 0 || seqlen_in > p.S_max) && threadIdx.x == 0 && split == 0)
+    atomicExch(p.wait.status, kStatusInvalidArg);
+  const int seqlen = min(max(seqlen_in, 0), p.S_max);
+  const int key_begin = split * p.chunk;
+  const int key_end = min(key_begin + p.chunk, seqlen);
+  if (key_begin >= key_end) {  // empty split: the merge never reads it (CTA-uniform)
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpMma) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(tmem, kTmemCols);
+    }
+    return;
+  }
+  const int n_tiles = (key_end - key_begin + kBN - 1) / kBN;
+  const int n_slot[2] = {(n_tiles + 1) / 2, n_tiles / 2};  // slot s: tiles j with j % 2 == s
+  const int R = p.G * p.T_q;                                 // rows that are stored
+  // the last tile may run past the sequence: its V rows there (cache rows that
+  // may hold any bits) are cleared before P V reads them
+  const int tail_keys = key_begin + n_tiles * kBN - seqlen;  // > 0: rows to clear
 
   if (warp == kWarpTma) {
     // ------------------------- TMA producer -------------------------
@@ -202,9 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       const int q_row0 = (b * p.H_q + kv * p.G) * p.T_q;  // first (head, token) row of the group
       mbar_arrive_expect_tx(q_full, kTileBytes);
       for (int half = 0; half < 2; ++half)
@@ -461,12 +472,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool use1 = n_slot[1] > 0;            // warp-uniform
         // rows past G * T_q belong to other heads' queries: computed, never stored
         const size_t orow = (size_t)(b * p.H_q + kv * p.G) * p.T_q + row;
-        const bool store = row < R && store_ok(orow * p.num_splits + split,
-                                               (size_t)p.B * p.H_q * p.T_q * p.num_splits,
-                                               p.wait.status);
-        if (store)
+        const size_t n_part_rows = (size_t)p.B * p.H_q * p.T_q * p.num_splits;
+        if (row < R && store_ok(orow * p.num_splits + split, n_part_rows, p.wait.status))
           p.lse_part[orow * p.num_splits + split] =
               L > 0.f ? mx * 0.69314718055994531f + logf(L) : -INFINITY;
+        // The combined rows go through shared memory so that the global stores
+        // are whole 512-byte rows: a thread holds one row, and storing it
+        // directly would make every warp store touch 32 rows.  The ring is idle
+        // here (both slots' last P V completed, so every copy has landed and
+        // every MMA that read a stage is done).  Each warp stages its 32 rows,
+        // 16-byte chunk ch of row i at chunk slot ch ^ i (conflict-free both ways).
+        uint8_t *stage = smem + kOffStage + wq * (32 * kD * 4);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t r0[32], r1[32];
@@ -474,27 +490,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (use1) tc::ld32(t_o + 128u + 32 * c, r1);
           tc::wait_ld32(r0);         // waits for both loads; ties r0's registers to it
           if (use1) tc::wait_ld32(r1);  // (already complete) ties r1's
-          if (store) {
-            float4 *dst =
-                reinterpret_cast<float4 *>(p.o_part + (orow * p.num_splits + split) * kD) + 8 * c;
-            // both slots' O are finite (every slot with a tile wrote its O, and V
-            // rows past the sequence were cleared); a slot with no tile is skipped
+          // both slots' O are finite (every slot with a tile wrote its O, and V
+          // rows past the sequence were cleared); a slot with no tile is skipped
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float4 v;
-              v.x = c0 * __uint_as_float(r0[4 * e + 0]);
-              v.y = c0 * __uint_as_float(r0[4 * e + 1]);
-              v.z = c0 * __uint_as_float(r0[4 * e + 2]);
-              v.w = c0 * __uint_as_float(r0[4 * e + 3]);
-              if (use1) {
-                v.x = fmaf(c1, __uint_as_float(r1[4 * e + 0]), v.x);
-                v.y = fmaf(c1, __uint_as_float(r1[4 * e + 1]), v.y);
-                v.z = fmaf(c1, __uint_as_float(r1[4 * e + 2]), v.z);
-                v.w = fmaf(c1, __uint_as_float(r1[4 * e + 3]), v.w);
-              }
-              dst[e] = v;
+          for (int e = 0; e < 8; ++e) {
+            float4 v;
+            v.x = c0 * __uint_as_float(r0[4 * e + 0]);
+            v.y = c0 * __uint_as_float(r0[4 * e + 1]);
+            v.z = c0 * __uint_as_float(r0[4 * e + 2]);
+            v.w = c0 * __uint_as_float(r0[4 * e + 3]);
+            if (use1) {
+              v.x = fmaf(c1, __uint_as_float(r1[4 * e + 0]), v.x);
+              v.y = fmaf(c1, __uint_as_float(r1[4 * e + 1]), v.y);
+              v.z = fmaf(c1, __uint_as_float(r1[4 * e + 2]), v.z);
+              v.w = fmaf(c1, __uint_as_float(r1[4 * e + 3]), v.w);
             }
+            *reinterpret_cast<float4 *>(stage + lane * (kD * 4) + (((8 * c + e) ^ lane) & 31) * 16) =
+                v;
           }
+        }
+        __syncwarp();
+        // row i of the warp: lane l stores its 16-byte chunk l
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+          const int r = 32 * wq + i;
+          const size_t prow = ((size_t)(b * p.H_q + kv * p.G) * p.T_q + r) * p.num_splits + split;
+          if (r < R && store_ok(prow, n_part_rows, p.wait.status))
+            reinterpret_cast<float4 *>(p.o_part + prow * kD)[lane] =
+                *reinterpret_cast<const float4 *>(stage + i * (kD * 4) + ((lane ^ i) & 31) * 16);
         }
       }
     }
