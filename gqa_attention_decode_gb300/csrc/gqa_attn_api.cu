@@ -551,8 +551,11 @@ GQA_API int gqa_attn_prefill_causal_paged(
   a.page_size = page_size;
   a.max_pages = max_pages_per_seq;
   a.num_pages = num_pages;
-  // paged K/V: one CTA per unit for every group size
-  cudaError_t e = gqa::prefill_launch(a, static_cast<cudaStream_t>(stream), g_encode);
+  // paged K/V: the CTA-pair kernel when the group size is a multiple of 4 and
+  // S_kv a multiple of 128; one CTA per unit otherwise
+  cudaError_t e = gqa::prefill_pair_eligible(a)
+                      ? gqa::prefill_pair_launch(a, static_cast<cudaStream_t>(stream), g_encode)
+                      : gqa::prefill_launch(a, static_cast<cudaStream_t>(stream), g_encode);
   if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
   return to_status(e);
 }

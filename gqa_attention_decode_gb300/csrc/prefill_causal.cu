@@ -79,17 +79,7 @@ struct Params {
   WaitCtl wait;
 };
 
-// Paged K/V ([num_pages, H_kv, page_size, d], page_size a multiple of 128): keys
-// [i*page_size, (i+1)*page_size) of sequence b are in page block_table[b *
-// max_pages + i].  Empty for the dense kernel, whose parameters (and register
-// allocation) it leaves untouched.
-template <bool kPaged>
-struct PageArgs {
-  const int32_t *block_table;
-  int page_size, max_pages, num_pages;
-};
-template <>
-struct PageArgs<false> {};
+using prefill_split::PageArgs;
 
 // Two slots of 128 query rows: slot i is query tile qt_i of head h_i.  Either
 // two heads of a KV group on one query tile, or (G odd) the group's last head

@@ -171,10 +171,18 @@ __device__ __forceinline__ uint64_t desc_v_base(uint32_t tile) {
 }
 __device__ __forceinline__ constexpr uint32_t v_step(int kk) { return kk * 2048; }
 
+using prefill_split::PageArgs;
+
+// kPaged: K/V in pages through pg.block_table (a separate instantiation; the
+// dense kernel's parameters are unchanged).  Used only when S_kv is a multiple
+// of 128, so every key tile the pair loads holds keys of the sequence and no
+// row of a page's unused tail is ever multiplied.
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                        const __grid_constant__ CUtensorMap tm_v, const Params p,
+                        const PageArgs<kPaged> pg) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -258,12 +266,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t full = dsmem_addr(kv_full(s), 0);
             if (leader) mbar_arrive_expect_tx(kv_full(s), 2 * kStageBytes);
             const uint32_t dst = sbase + kOffStage + s * kStageBytes;
+            int key0 = j * kBN, blk = kv_row;  // the tile's first key row and block
+            if constexpr (kPaged) {
+              // a 128-key tile lies in one page (page sizes are multiples of 128); a
+              // page id outside the pool reads zeros (a block past the tensor map)
+              // and is reported through the status word
+              const int page = j * kBN / pg.page_size;
+              const int page_id = __ldca(pg.block_table + (size_t)w.b * pg.max_pages + page);
+              const bool bad = page_id < 0 || page_id >= pg.num_pages;
+              if (bad) atomicExch(p.wait.status, kStatusInvalidArg);
+              key0 = j * kBN - page * pg.page_size;
+              blk = bad ? pg.num_pages * p.H_kv : page_id * p.H_kv + w.kv;
+            }
             if (which == 0) {  // K: keys j*128 + 64*rank .. +63, all of d
               for (int half = 0; half < 2; ++half)
                 tma_load_4d_pair(dst + half * kKHalfColBytes, &tm_k, full, 0, half,
-                                 j * kBN + kHalfKeys * rank, kv_row, pol_kv);
+                                 key0 + kHalfKeys * rank, blk, pol_kv);
             } else {  // V: keys j*128 .. +127, d 64*rank .. +63
-              tma_load_4d_pair(dst, &tm_v, full, 0, rank, j * kBN, kv_row, pol_kv);
+              tma_load_4d_pair(dst, &tm_v, full, 0, rank, key0, blk, pol_kv);
             }
           }
         }
@@ -601,8 +621,11 @@ CUresult make_map(CUtensorMap *map, const uint16_t *base, int rows, int heads, i
 cudaError_t prefill_pair_prepare_device(int *max_pairs) {
   using namespace prefill_pair;
   *max_pairs = 0;
-  cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel,
+  cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_pair_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // clusters of two the device runs at once (each CTA takes a whole SM)
   cudaLaunchConfig_t cfg = {};
@@ -617,14 +640,19 @@ cudaError_t prefill_pair_prepare_device(int *max_pairs) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel, &cfg) == cudaSuccess) *max_pairs = n;
+  if (cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel<false>, &cfg) == cudaSuccess)
+    *max_pairs = n;
   cudaGetLastError();  // a refused query only disables the pair kernel
   return cudaSuccess;
 }
 
 bool prefill_pair_eligible(const PrefillLaunch &a) {
-  // dense K/V only (a paged cache runs on the single-CTA kernel)
-  return a.H_kv > 0 && (a.H_q / a.H_kv) % 4 == 0 && a.max_pairs > 0 && a.block_table == nullptr;
+  // a paged cache only when every key tile is whole (S_kv a multiple of 128);
+  // otherwise it runs on the single-CTA kernel, which clears the V rows of a
+  // page's unused tail before P V reads them
+  return a.H_kv > 0 && (a.H_q / a.H_kv) % 4 == 0 && a.max_pairs > 0 &&
+         (a.block_table == nullptr ||
+          (a.S_kv % prefill_pair::kBN == 0 && a.page_size > 0 && a.page_size % prefill_pair::kBN == 0));
 }
 
 // Work plan: units of one 128-row query tile of four heads over the resident
@@ -649,10 +677,15 @@ cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
   if (!prefill_pair_eligible(a)) return cudaErrorNotSupported;
   const PrefillPlan pl = prefill_pair_plan(a);
   if (pl.units <= 0) return cudaErrorNotSupported;
+  // K/V blocks of rows: one per (sequence, KV head) of S_kv keys, or one per
+  // (page, KV head) of page_size keys
+  const bool paged = a.block_table != nullptr;
+  const int kv_rows = paged ? a.page_size : a.S_kv;
+  const int kv_blocks = paged ? a.num_pages * a.H_kv : a.B * a.H_kv;
   CUtensorMap tm_q, tm_k, tm_v;
   if (make_map(&tm_q, a.q, a.T_q, a.B * a.H_q, kBM, encode) != CUDA_SUCCESS ||
-      make_map(&tm_k, a.k, a.S_kv, a.B * a.H_kv, kHalfKeys, encode) != CUDA_SUCCESS ||
-      make_map(&tm_v, a.v, a.S_kv, a.B * a.H_kv, kBN, encode) != CUDA_SUCCESS)
+      make_map(&tm_k, a.k, kv_rows, kv_blocks, kHalfKeys, encode) != CUDA_SUCCESS ||
+      make_map(&tm_v, a.v, kv_rows, kv_blocks, kBN, encode) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   Params p;
   p.o = a.o;
@@ -686,7 +719,12 @@ cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tm_q, tm_k, tm_v, p);
+  cudaError_t e =
+      paged ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<true>, tm_q, tm_k, tm_v, p,
+                                 PageArgs<true>{a.block_table, a.page_size, a.max_pages,
+                                                a.num_pages})
+            : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<false>, tm_q, tm_k, tm_v, p,
+                                 PageArgs<false>{});
   if (e != cudaSuccess) return e;
   // the pieces' merge, a programmatic dependent of the pair kernel
   return prefill_split::launch_merge<4>(p, pl, stream);

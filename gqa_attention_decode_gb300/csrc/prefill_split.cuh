@@ -44,6 +44,18 @@ __host__ __device__ __forceinline__ int piece_start(int i, int s, int n) {
   return (int)((long long)i * n / s);
 }
 
+// Paged K/V ([num_pages, H_kv, page_size, d], page_size a multiple of 128): keys
+// [i*page_size, (i+1)*page_size) of sequence b are in page block_table[b *
+// max_pages + i].  Empty for a dense kernel, whose parameters (and register
+// allocation) it leaves untouched.
+template <bool kPaged>
+struct PageArgs {
+  const int32_t *block_table;
+  int page_size, max_pages, num_pages;
+};
+template <>
+struct PageArgs<false> {};
+
 using Plan = PrefillPlan;
 // `units` units on `workers` resident workers; `n_kv_min` key tiles of the
 // shortest unit; a workspace of `ws_bytes` (none if `ws` is null).  The

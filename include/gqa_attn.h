@@ -395,8 +395,10 @@ GQA_API int gqa_attn_prefill_causal_ws(const gqa_bf16_t *q, const gqa_bf16_t *k,
  *   page_size          a positive multiple of 128 (else GQA_ERR_UNSUPPORTED).
  *   num_pages * H_kv   below 2^31.
  * Everything else is that of gqa_attn_prefill_causal_ws (the workspace size of
- * gqa_attn_prefill_causal_workspace_size serves).  Runs the one-CTA-per-unit
- * kernel for every group size.
+ * gqa_attn_prefill_causal_workspace_size serves).  Runs the CTA-pair kernel
+ * when G is a multiple of 4 and S_kv a multiple of 128 (the results then equal
+ * gqa_attn_prefill_causal_ws's on the same keys bit for bit), the
+ * one-CTA-per-unit kernel otherwise.
  */
 GQA_API int gqa_attn_prefill_causal_paged(
     const gqa_bf16_t *q, const gqa_bf16_t *k_pages, const gqa_bf16_t *v_pages,

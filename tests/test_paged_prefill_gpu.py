@@ -2,9 +2,10 @@
 
 The pages are a shuffled pool built from a dense cache; unused pages and the
 rows of each sequence's last page past S_kv hold NaN, which must never reach a
-result.  For group sizes that run one CTA per unit on a dense cache too, the
-paged call must equal the dense call bit for bit; every case is compared with
-the oracle.
+result.  Where the paged and the dense call run the same kernel (group sizes
+that run one CTA per unit on a dense cache too, and the CTA-pair kernel when
+S_kv is a multiple of 128), the paged call must equal the dense call bit for
+bit; every case is compared with the oracle.
 """
 import math
 
@@ -60,7 +61,9 @@ def to_pages(k, v, page_size, extra_pages, seed):
     (1, 4, 2, 300, 300, 0, 128),       # G = 2, square causal, ragged last page
     (2, 6, 2, 200, 1000, 800, 256),    # G = 3, a chunk after a prefix, two sequences
     (1, 4, 4, 128, 4000, 3872, 512),   # MHA, a short chunk after a long prefix (key split)
-    (1, 16, 2, 257, 700, 443, 128),    # G = 8 (one CTA per unit when paged)
+    (1, 16, 2, 257, 700, 443, 128),    # G = 8, S_kv not a multiple of 128: one CTA per unit
+    (2, 16, 2, 300, 1024, 724, 256),   # G = 8, whole key tiles: CTA pairs
+    (1, 64, 8, 256, 4096, 3840, 512),  # the 70B layer's groups, a chunk after a long prefix
     (1, 8, 1, 1, 1, 0, 128),           # one query, one key
 ])
 def test_paged_prefill_against_oracle(B, H_q, H_kv, T_q, S_kv, q_offset, page_size):
@@ -72,7 +75,7 @@ def test_paged_prefill_against_oracle(B, H_q, H_kv, T_q, S_kv, q_offset, page_si
     assert torch.isfinite(o.float()).all()
     o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), q_offset, scale)
     compare(o, lse, o_ref, lse_ref, f"paged prefill {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
-    if (H_q // H_kv) % 4 != 0:   # the dense call runs the same kernel: identical results
+    if (H_q // H_kv) % 4 != 0 or S_kv % 128 == 0:   # the dense call runs the same kernel
         o_d, l_d = gqa.gqa_attn_prefill_causal(q, k, v, scale, q_offset)
         torch.cuda.synchronize()
         assert torch.equal(o, o_d) and torch.equal(lse, l_d)

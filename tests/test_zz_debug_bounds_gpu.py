@@ -87,6 +87,17 @@ SCRIPT = textwrap.dedent("""
     o_ref, l_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), 800, 0.088)
     compare(o, lse, o_ref, l_ref, "debug paged prefill")
 
+    # the same on CTA pairs (G = 8, whole key tiles)
+    q, k, v = gqa_synth.prefill_inputs(1, 16, 2, 300, 1024, 128, seed=5, device=dev)
+    kp = k[0].view(2, 4, 256, 128).permute(1, 0, 2, 3).contiguous()
+    vp = v[0].view(2, 4, 256, 128).permute(1, 0, 2, 3).contiguous()
+    table = torch.arange(4, dtype=torch.int32, device=dev).view(1, 4)
+    o, lse = gqa.gqa_attn_prefill_causal_paged(q, kp, vp, table, 1024, 0.088, 724)
+    torch.cuda.synchronize()
+    ok("paged prefill, CTA pairs")
+    o_ref, l_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), 724, 0.088)
+    compare(o, lse, o_ref, l_ref, "debug paged prefill, CTA pairs")
+
     # merge of shard states
     parts = torch.randn((3, 1000, 128), device=dev).to(torch.bfloat16)
     lses = torch.randn((3, 1000), device=dev)
