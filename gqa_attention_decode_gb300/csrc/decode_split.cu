@@ -73,6 +73,7 @@ struct Params {
   const int32_t *block_table;  // paged variant: [B, max_pages]
   int page_size, max_pages, num_pages;
   int B, H_q, H_kv, G, S_max, num_splits, chunk;
+  int num_sms;  // SMs the host plan counted on (the device-side chunk rule)
   int T_q, n_cols, cgroups;  // new tokens per sequence, G * T_q, column groups of 4 warps
   float scale_log2;  // scale * log2(e)
   int l2_prefetch_tiles;  // tiles of its chunk a CTA pulls into L2 before the dependency wait
@@ -165,12 +166,15 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int seqlen_in = __ldca(p.seqlens + b);
+  const int seqlen = min(max(seqlen_in, 0), p.S_max);
+  // the chunk for the batch's actual lengths (the host's chunk when they are S_max)
+  const int chunk = device_chunk(p.seqlens, p.B, seqlen, p.S_max, p.chunk, p.num_splits, p.H_kv,
+                                 p.num_sms, kTileKeys);
   // out-of-range lengths are clamped and reported through the status word
   if ((seqlen_in < 0 || seqlen_in > p.S_max) && threadIdx.x == 0 && split == 0)
     atomicExch(p.wait.status, kStatusInvalidArg);
-  const int seqlen = min(max(seqlen_in, 0), p.S_max);
-  const int key_begin = split * p.chunk;
-  const int key_end = min(key_begin + p.chunk, seqlen);
+  const int key_begin = split * chunk;
+  const int key_end = min(key_begin + chunk, seqlen);
   if (!kFused && key_begin >= key_end) return;  // empty split: the merge never reads it
   // (a fused CTA with no keys still takes part in the cluster merge)
   const int n_tiles = max(0, (key_end - key_begin + kTileKeys - 1) / kTileKeys);
@@ -525,7 +529,8 @@ constexpr int kMergeRound = 4;
 __global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
                         const int32_t *__restrict__ seqlens, uint16_t *__restrict__ o,
-                        float *__restrict__ lse, int S_max, int num_splits, int chunk) {
+                        float *__restrict__ lse, int S_max, int num_splits, int chunk, int H_kv,
+                        int num_sms, int tile) {
   __shared__ float4 red_o[kMergeGroups][32];
   __shared__ float red_w[kMergeGroups];
   __shared__ float red_m[kMergeGroups];
@@ -535,7 +540,11 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int h = blockIdx.x, b = blockIdx.y;  // h: (query head, new token) row of sequence b
   const int t = threadIdx.x, grp = t >> 5, lane = t & 31;
   const int seqlen = min(max(__ldcg(seqlens + b), 0), S_max);
-  const int ns = min((seqlen + chunk - 1) / chunk, num_splits);
+  // the splits that hold keys of this row: the chunk the split kernel derived
+  // from the same lengths
+  const int dchunk = device_chunk(seqlens, gridDim.y, seqlen, S_max, chunk, num_splits, H_kv,
+                                  num_sms, tile);
+  const int ns = min((seqlen + dchunk - 1) / dchunk, num_splits);
   const size_t row = (size_t)b * gridDim.x + h;
   const float *lp = lse_part + row * num_splits;
   const float4 *op = reinterpret_cast<const float4 *>(o_part + row * num_splits * kD) + lane;
@@ -707,6 +716,7 @@ static decode::Params make_params(const DecodeLaunch &a) {
   p.S_max = a.S_max;
   p.num_splits = a.num_splits;
   p.chunk = a.chunk;
+  p.num_sms = a.num_sms;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.T_q = a.T_q > 0 ? a.T_q : 1;
   p.n_cols = p.G * p.T_q;
@@ -790,7 +800,8 @@ cudaError_t decode_merge_launch(const DecodeLaunch &a, cudaStream_t stream) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_merge_kernel, (const float *)a.o_part,
                             (const float *)a.lse_part, a.seqlens, a.o, a.lse, a.S_max,
-                            a.num_splits, a.chunk > 0 ? a.chunk : 1);
+                            a.num_splits, a.chunk > 0 ? a.chunk : 1, a.H_kv, a.num_sms,
+                            a.chunk_tile > 0 ? a.chunk_tile : kTileKeys);
 }
 
 }  // namespace gqa

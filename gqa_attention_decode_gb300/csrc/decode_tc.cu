@@ -63,6 +63,7 @@ struct Params {
   float *lse_part;
   int B, H_q, H_kv, G, T_q, S_max, num_splits, chunk;
   int page_size, max_pages, num_pages;
+  int num_sms;  // SMs the host plan counted on (the device-side chunk rule)
   int l2_prefetch;  // one-wave grid: prefetch the first key tile before the wait
   float sl2;  // scale * log2(e)
   WaitCtl wait;
@@ -185,12 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // inputs written by earlier grids are visible after this wait (coherent loads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int seqlen_in = __ldca(p.seqlens + b);
+  const int seqlen = min(max(seqlen_in, 0), p.S_max);
+  // the chunk for the batch's actual lengths (the host's chunk when they are S_max)
+  const int chunk = device_chunk(p.seqlens, p.B, seqlen, p.S_max, p.chunk, p.num_splits, p.H_kv,
+                                 p.num_sms, kBN);
   // out-of-range lengths are clamped and reported through the status word
   if ((seqlen_in < 0 || seqlen_in > p.S_max) && threadIdx.x == 0 && split == 0)
     atomicExch(p.wait.status, kStatusInvalidArg);
-  const int seqlen = min(max(seqlen_in, 0), p.S_max);
-  const int key_begin = split * p.chunk;
-  const int key_end = min(key_begin + p.chunk, seqlen);
+  const int key_begin = split * chunk;
+  const int key_end = min(key_begin + chunk, seqlen);
   if (key_begin >= key_end) {  // empty split: the merge never reads it (CTA-uniform)
     tc::fence_before_sync();
     __syncthreads();
@@ -586,6 +590,7 @@ cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   p.S_max = a.S_max;
   p.num_splits = a.num_splits;
   p.chunk = a.chunk;
+  p.num_sms = a.num_sms;
   p.sl2 = a.scale * 1.4426950408889634f;
   p.wait = a.wait;
   cudaLaunchConfig_t cfg = {};

@@ -144,6 +144,59 @@ __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int c
                : "memory");
 }
 
+// ceil(n / d) for n < 2^20, d >= 1: the approximate hardware reciprocal (a few
+// ulp) puts n * (1/d) within one of n / d, and one integer correction each way
+// makes the quotient exact (checked against exact division with the
+// reciprocal perturbed by up to 4 ulp either way).
+__device__ __forceinline__ unsigned ceil_div_small(unsigned n, unsigned d) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__uint2float_rn(d)));
+  unsigned q = __float2uint_rz(__uint2float_rn(n) * r);
+  if (q * d > n) --q;
+  else if ((q + 1) * d <= n) ++q;  // q = floor(n / d)
+  return q + (q * d != n ? 1u : 0u);
+}
+
+// Keys per split for the sequence lengths found on the device (the decode's
+// split planner, second half).  The host plan sized `chunk` (keys, a multiple
+// of `tile`) for S_max, the only length it knows.  When the sequences are
+// shorter, their key tiles (T over the batch, per KV head) are spread so that
+// about one chunk per SM results: ceil(T * H_kv / num_sms) tiles, never more
+// than the host's chunk and never so few that the longest sequence needs more
+// than `splits` chunks.  With every sequence at S_max this is the host's chunk
+// (or a little less).  `seqlen` is this CTA's clamped length, which is the
+// whole batch when B = 1 (no further load).  The split kernels and the merge
+// call it with the same arguments and get the same value.  Warp-collective:
+// all 32 lanes of the warp call it.
+__device__ __forceinline__ int device_chunk(const int32_t *seqlens, int B, int seqlen, int S_max,
+                                            int chunk, int splits, int H_kv, int num_sms,
+                                            int tile) {
+  // one sequence that fills its cache: the host's chunk (the rule gives it, or
+  // a little less), with nothing on the kernel's start-up path
+  if (B == 1 && seqlen >= S_max) return chunk;
+  unsigned t_sum, t_max;
+  if (B == 1) {
+    t_sum = t_max = (unsigned)(seqlen + tile - 1) / tile;
+  } else {
+    t_sum = 0;
+    t_max = 0;
+    for (int i = threadIdx.x & 31; i < B; i += 32) {
+      const unsigned t = (unsigned)(min(max(__ldca(seqlens + i), 0), S_max) + tile - 1) / tile;
+      t_sum += t;
+      t_max = max(t_max, t);
+    }
+    t_sum = __reduce_add_sync(0xffffffffu, t_sum);
+    t_max = __reduce_max_sync(0xffffffffu, t_max);
+  }
+  const unsigned chunk_tiles = (unsigned)(chunk / tile);
+  // totals of 2^20 tiles or more are far above any cap: the host's chunk
+  const unsigned work = t_sum < (1u << 20) / (unsigned)H_kv ? t_sum * (unsigned)H_kv : 1u << 20;
+  unsigned c = work >= (1u << 20) ? chunk_tiles : ceil_div_small(work, (unsigned)num_sms);
+  c = min(c, chunk_tiles);
+  c = max(c, t_max < (1u << 20) ? ceil_div_small(t_max, (unsigned)splits) : chunk_tiles);
+  return (int)max(c, 1u) * tile;
+}
+
 // Tile load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA of a CTA pair (`bar` is a
 // shared::cluster address, e.g. from dsmem_addr).

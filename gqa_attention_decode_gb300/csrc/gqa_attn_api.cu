@@ -298,6 +298,7 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   a.lse = lse;
   a.o_part = static_cast<float *>(const_cast<void *>(workspace));
   a.lse_part = a.o_part + (size_t)B * H_q * T_q * splits * d;
+  a.chunk_tile = tensor_cores ? gqa::kDecodeTcTileKeys : gqa::kDecodeTileKeys;
   a.num_sms = st->num_sms;
   a.fused_clusters = st->fused_clusters;
   a.wait.status = st->status;

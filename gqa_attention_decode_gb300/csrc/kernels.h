@@ -19,6 +19,7 @@ struct DecodeLaunch {
   int num_pages, page_size, max_pages;  // paged layout (S_max = max_pages * page_size)
   const int32_t *seqlens;   // [B]
   int B, H_q, H_kv, S_max, num_splits, chunk;
+  int chunk_tile;   // keys a chunk is a multiple of: 64 (split kernel) or 128 (tcgen05 kernel)
   int T_q;          // new tokens per sequence (1: plain decode); G * T_q <= kDecodeMaxCols
   float scale;
   uint16_t *o;      // [B, H_q, T_q, d]

@@ -90,11 +90,18 @@ GQA_API int gqa_attn_abi_version(void);
 
 /*
  * Split plan for decode (host only, no CUDA call).  The KV sequence of every
- * (batch, KV head) is cut into contiguous chunks of `chunk` keys; split s owns
- * keys [s*chunk, min((s+1)*chunk, seqlen)) -- the contiguous-block placement of
- * the record's section 2.1 ("KV cache allocation"), rank r owning
- * [r*B, (r+1)*B).  A split whose range is empty does no work and is skipped by
- * the merge.
+ * (batch, KV head) is cut into contiguous chunks; split s owns keys
+ * [s*c, min((s+1)*c, seqlen)) -- the contiguous-block placement of the
+ * record's section 2.1 ("KV cache allocation"), rank r owning [r*B, (r+1)*B).
+ * The plan fixes the grid (out_num_splits) and the largest chunk (out_chunk),
+ * sized for S_max, the only length the host knows.  On the device each call
+ * takes c from the sequence lengths it finds there: with T key tiles of
+ * 64 keys (128 on the tensor-core path) over the batch, c is
+ * ceil(T * H_kv / num_sms) tiles, at most out_chunk and at least what lets
+ * the longest sequence fit in out_num_splits chunks; a single sequence that
+ * fills its cache uses out_chunk.  Short sequences in a long cache are thereby
+ * spread over the SMs rather than over the first few splits.  A split whose
+ * range is empty does no work and is skipped by the merge.
  *
  *   B, H_kv, S_max  batch, KV heads, capacity of the KV cache in keys (>= 0)
  *   num_sms         streaming multiprocessors of the target device (> 0)
@@ -103,7 +110,7 @@ GQA_API int gqa_attn_abi_version(void);
  *                   > 0: use this many splits (clamped to the number of 64-key
  *                   tiles in S_max).
  *   out_num_splits  written: splits per sequence (grid width), >= 1 if S_max > 0
- *   out_chunk       written: keys per split, a multiple of 64
+ *   out_chunk       written: keys per split at most, a multiple of 64
  * Returns GQA_OK or GQA_ERR_INVALID_ARG (negative sizes, num_sms <= 0, null
  * outputs).
  */

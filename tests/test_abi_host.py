@@ -325,9 +325,12 @@ def test_multi_token_rejections(lib):
     assert call(1, 64, 8, 2, d=64) == gqa.GQA_ERR_UNSUPPORTED
     assert call(65535, 65536, 8192, 1) == gqa.GQA_ERR_UNSUPPORTED  # > 2^31 output rows
     assert call(0, 64, 8, 2) == gqa.GQA_OK
+    # workspace: per (row, split) O[128] and lse in fp32, rounded up to 256 bytes
+    ws_bytes = lambda rows, splits: (rows * splits * 129 * 4 + 255) // 256 * 256
+    assert gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 152) == ws_bytes(64, 19)
     assert gqa.gqa_attn_decode_multi_workspace_size(1, 64, 8, 4, 32768, 128, 152) == \
-        4 * gqa.gqa_attn_decode_workspace_size(1, 64, 8, 32768, 128, 152)
+        ws_bytes(64 * 4, 19)
     # more than 32 rows per KV head: tensor-core split kernel, chunks of whole
     # 128-key tiles (1728 keys -> 1792, still 19 splits for 32K keys)
     assert gqa.gqa_attn_decode_multi_workspace_size(1, 64, 8, 16, 32768, 128, 152) == \
-        (64 * 16 * 19 * 129 * 4 + 255) // 256 * 256
+        ws_bytes(64 * 16, 19)

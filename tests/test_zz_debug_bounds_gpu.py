@@ -61,6 +61,17 @@ SCRIPT = textwrap.dedent("""
         ok(("paged decode", B, H_q, H_kv, S, T_q, splits))
         assert torch.equal(o2, o) and torch.equal(l2, lse)
 
+    # short sequences in a long cache (the device-side chunk), T_q = 1 and 16
+    for T_q in (1, 16):
+        q = gqa_synth.bf16_normal((2, 64, T_q, 128), 6, dev)
+        _, k, v, sl = gqa_synth.decode_inputs(2, 64, 8, 32768, 128, 7, dev, [3000, 17])
+        o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(dev), 0.088)
+        torch.cuda.synchronize()
+        ok(("short in long cache", T_q))
+        o_ref, l_ref = oracle.decode_multi(np64(q), np64(k[:, :, :3000]), np64(v[:, :, :3000]),
+                                           sl.numpy(), 0.088)
+        compare(o, lse, o_ref, l_ref, "debug short in long cache")
+
     # prefill: CTA pairs (G = 8, 4) and one CTA per unit (G = 3, 1), whole and split
     for (H_q, H_kv, T, S) in [(16, 2, 300, 300), (8, 2, 128, 4096), (6, 2, 200, 200),
                               (6, 2, 128, 4096), (4, 4, 256, 2304), (16, 2, 200, 3000)]:
