@@ -9,6 +9,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import gqa_attention_decode_gb300 as gqa
@@ -334,3 +335,32 @@ def test_multi_token_rejections(lib):
     # 128-key tiles (1728 keys -> 1792, still 19 splits for 32K keys)
     assert gqa.gqa_attn_decode_multi_workspace_size(1, 64, 8, 16, 32768, 128, 152) == \
         ws_bytes(64 * 16, 19)
+
+
+def test_device_chunk_ceil_division_is_exact():
+    """The device-side split planner divides with the approximate hardware
+    reciprocal, then corrects the quotient once each way with integer compares
+    (ceil_div_small in csrc/device_common.cuh).  The same steps in float32 here,
+    with the reciprocal anywhere within 4 ulp of 1/d, must give ceil(n / d)
+    exactly for every n < 2^20 it is used on."""
+    rng = np.random.default_rng(11)
+
+    def ceil_div(n, d, r):
+        q = np.floor((n.astype(np.float32) * np.float32(r)).astype(np.float32)).astype(np.uint64)
+        dd = np.uint64(d)
+        q = np.where(q * dd > n, q - 1, np.where((q + 1) * dd <= n, q + 1, q))
+        return q + (q * dd != n)
+
+    for d in list(range(1, 160)) + [255, 1000, 4096, 65535, (1 << 20) - 1]:
+        n = np.concatenate([np.arange(0, 4096, dtype=np.uint64),
+                            rng.integers(0, 1 << 20, 20000).astype(np.uint64),
+                            np.array([(1 << 20) - 1, d - 1, d, d + 1, 2 * d], dtype=np.uint64)])
+        n = n[n < (1 << 20)]
+        exact = (n + np.uint64(d - 1)) // np.uint64(d)
+        r = np.float32(1) / np.float32(d)
+        lo = hi = r
+        for _ in range(5):
+            assert np.array_equal(ceil_div(n, d, lo), exact), (d, lo)
+            assert np.array_equal(ceil_div(n, d, hi), exact), (d, hi)
+            lo = np.nextafter(lo, np.float32(0))
+            hi = np.nextafter(hi, np.float32(np.inf))
