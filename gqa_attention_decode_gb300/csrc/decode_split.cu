@@ -168,8 +168,8 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   const int seqlen_in = __ldca(p.seqlens + b);
   const int seqlen = min(max(seqlen_in, 0), p.S_max);
   // the chunk for the batch's actual lengths (the host's chunk when they are S_max)
-  const int chunk = device_chunk(p.seqlens, p.B, seqlen, p.S_max, p.chunk, p.num_splits, p.H_kv,
-                                 p.num_sms, kTileKeys);
+  const int chunk =
+      device_chunk(seqlen, p.B, p.S_max, p.chunk, p.num_splits, p.H_kv, p.num_sms, kTileKeys);
   // out-of-range lengths are clamped and reported through the status word
   if ((seqlen_in < 0 || seqlen_in > p.S_max) && threadIdx.x == 0 && split == 0)
     atomicExch(p.wait.status, kStatusInvalidArg);
@@ -542,8 +542,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int seqlen = min(max(__ldcg(seqlens + b), 0), S_max);
   // the splits that hold keys of this row: the chunk the split kernel derived
   // from the same lengths
-  const int dchunk = device_chunk(seqlens, gridDim.y, seqlen, S_max, chunk, num_splits, H_kv,
-                                  num_sms, tile);
+  const int dchunk = device_chunk(seqlen, gridDim.y, S_max, chunk, num_splits, H_kv, num_sms, tile);
   const int ns = min((seqlen + dchunk - 1) / dchunk, num_splits);
   const size_t row = (size_t)b * gridDim.x + h;
   const float *lp = lse_part + row * num_splits;

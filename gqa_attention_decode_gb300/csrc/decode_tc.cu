@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int seqlen_in = __ldca(p.seqlens + b);
   const int seqlen = min(max(seqlen_in, 0), p.S_max);
   // the chunk for the batch's actual lengths (the host's chunk when they are S_max)
-  const int chunk = device_chunk(p.seqlens, p.B, seqlen, p.S_max, p.chunk, p.num_splits, p.H_kv,
-                                 p.num_sms, kBN);
+  const int chunk =
+      device_chunk(seqlen, p.B, p.S_max, p.chunk, p.num_splits, p.H_kv, p.num_sms, kBN);
   // out-of-range lengths are clamped and reported through the status word
   if ((seqlen_in < 0 || seqlen_in > p.S_max) && threadIdx.x == 0 && split == 0)
     atomicExch(p.wait.status, kStatusInvalidArg);

@@ -157,43 +157,26 @@ __device__ __forceinline__ unsigned ceil_div_small(unsigned n, unsigned d) {
   return q + (q * d != n ? 1u : 0u);
 }
 
-// Keys per split for the sequence lengths found on the device (the decode's
-// split planner, second half).  The host plan sized `chunk` (keys, a multiple
-// of `tile`) for S_max, the only length it knows.  When the sequences are
-// shorter, their key tiles (T over the batch, per KV head) are spread so that
-// about one chunk per SM results: ceil(T * H_kv / num_sms) tiles, never more
-// than the host's chunk and never so few that the longest sequence needs more
-// than `splits` chunks.  With every sequence at S_max this is the host's chunk
-// (or a little less).  `seqlen` is this CTA's clamped length, which is the
-// whole batch when B = 1 (no further load).  The split kernels and the merge
-// call it with the same arguments and get the same value.  Warp-collective:
-// all 32 lanes of the warp call it.
-__device__ __forceinline__ int device_chunk(const int32_t *seqlens, int B, int seqlen, int S_max,
-                                            int chunk, int splits, int H_kv, int num_sms,
-                                            int tile) {
-  // one sequence that fills its cache: the host's chunk (the rule gives it, or
-  // a little less), with nothing on the kernel's start-up path
-  if (B == 1 && seqlen >= S_max) return chunk;
-  unsigned t_sum, t_max;
-  if (B == 1) {
-    t_sum = t_max = (unsigned)(seqlen + tile - 1) / tile;
-  } else {
-    t_sum = 0;
-    t_max = 0;
-    for (int i = threadIdx.x & 31; i < B; i += 32) {
-      const unsigned t = (unsigned)(min(max(__ldca(seqlens + i), 0), S_max) + tile - 1) / tile;
-      t_sum += t;
-      t_max = max(t_max, t);
-    }
-    t_sum = __reduce_add_sync(0xffffffffu, t_sum);
-    t_max = __reduce_max_sync(0xffffffffu, t_max);
-  }
+// Keys per split for a sequence of `seqlen` keys (the decode's split planner,
+// second half).  The host plan sized `chunk` (keys, a multiple of `tile`) for
+// S_max, the only length it knows; the length itself lives on the device.  A
+// shorter sequence is spread as if the batch held B like it: its key tiles t
+// times B * H_kv, over the SMs, give ceil(t * B * H_kv / num_sms) tiles per
+// chunk, never more than the host's chunk and never so few that the sequence
+// needs more than `splits` chunks.  A sequence at S_max keeps the host's
+// chunk.  The split kernels and the merge call it with the same arguments and
+// get the same value.
+__device__ __forceinline__ int device_chunk(int seqlen, int B, int S_max, int chunk, int splits,
+                                            int H_kv, int num_sms, int tile) {
+  if (seqlen >= S_max) return chunk;
+  const unsigned t = (unsigned)(seqlen + tile - 1) / tile;
   const unsigned chunk_tiles = (unsigned)(chunk / tile);
   // totals of 2^20 tiles or more are far above any cap: the host's chunk
-  const unsigned work = t_sum < (1u << 20) / (unsigned)H_kv ? t_sum * (unsigned)H_kv : 1u << 20;
-  unsigned c = work >= (1u << 20) ? chunk_tiles : ceil_div_small(work, (unsigned)num_sms);
+  const unsigned long long work = (unsigned long long)t * (unsigned)H_kv * (unsigned)B;
+  unsigned c = work >= (1u << 20) ? chunk_tiles : ceil_div_small((unsigned)work, (unsigned)num_sms);
   c = min(c, chunk_tiles);
-  c = max(c, t_max < (1u << 20) ? ceil_div_small(t_max, (unsigned)splits) : chunk_tiles);
+  // at least what fits the sequence into the splits (the host's chunk always does)
+  c = max(c, t < (1u << 20) ? ceil_div_small(t, (unsigned)splits) : chunk_tiles);
   return (int)max(c, 1u) * tile;
 }
 

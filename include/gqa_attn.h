@@ -95,13 +95,13 @@ GQA_API int gqa_attn_abi_version(void);
  * record's section 2.1 ("KV cache allocation"), rank r owning [r*B, (r+1)*B).
  * The plan fixes the grid (out_num_splits) and the largest chunk (out_chunk),
  * sized for S_max, the only length the host knows.  On the device each call
- * takes c from the sequence lengths it finds there: with T key tiles of
- * 64 keys (128 on the tensor-core path) over the batch, c is
- * ceil(T * H_kv / num_sms) tiles, at most out_chunk and at least what lets
- * the longest sequence fit in out_num_splits chunks; a single sequence that
- * fills its cache uses out_chunk.  Short sequences in a long cache are thereby
- * spread over the SMs rather than over the first few splits.  A split whose
- * range is empty does no work and is skipped by the merge.
+ * takes c per sequence from the length it finds there: with t key tiles of
+ * 64 keys (128 on the tensor-core path), c is ceil(t * B * H_kv / num_sms)
+ * tiles, at most out_chunk and at least what fits the sequence into
+ * out_num_splits chunks; a sequence that fills its cache uses out_chunk.
+ * Short sequences in a long cache are thereby spread over the SMs rather than
+ * over the first few splits.  A split whose range is empty does no work and
+ * is skipped by the merge.
  *
  *   B, H_kv, S_max  batch, KV heads, capacity of the KV cache in keys (>= 0)
  *   num_sms         streaming multiprocessors of the target device (> 0)
