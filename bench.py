@@ -611,9 +611,12 @@ def run_all_configs(device):
         d["peak_source"] = peak_src
         print(json.dumps(d), flush=True)
 
-    def decode_line(name, T_q=1, page_size=0):
+    def decode_line(name, T_q=1, page_size=0, cache_keys=0):
         w = gqa_synth.WORKLOADS[name]
         q, k, v, sl = gqa_synth.workload_decode_inputs(w, device)
+        if cache_keys:  # the same sequences inside a longer (over-allocated) cache
+            q, k, v, sl = gqa_synth.decode_inputs(w.B, w.H_q, w.H_kv, cache_keys, w.d, w.seed,
+                                                  device, sl.tolist())
         if T_q > 1:
             q = gqa_synth.bf16_normal((w.B, w.H_q, T_q, w.d), w.seed, device)
         nbytes = decode_bytes(w, sl.tolist())
@@ -645,7 +648,9 @@ def run_all_configs(device):
             fn = lambda: [gqa.gqa_attn_decode(q, kc, vc, sld, w.scale, ns) for kc, vc in kvs]
         us = time_graph(fn, len(kvs), 20)
         gbs = nbytes / us / 1e3
-        label = name + (f" T_q={T_q}" if T_q > 1 else "") + (f" paged({page_size})" if page_size else "")
+        label = (name + (f" T_q={T_q}" if T_q > 1 else "") +
+                 (f" paged({page_size})" if page_size else "") +
+                 (f" in a {cache_keys >> 10}K-key cache" if cache_keys else ""))
         emit({"workload": label, "us_per_call": us, "value": gbs, "unit": "GB/s",
               "bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
               "bytes_per_call": nbytes, "kv_copies": len(kvs),
@@ -678,7 +683,8 @@ def run_all_configs(device):
             fn = lambda: gqa.gqa_attn_prefill_causal_paged(q, kp, vp, table, w.S_kv, w.scale,
                                                            w.q_offset, o, lse, ws)
             name = f"{name} paged({page_size})"
-            kernel = "prefill_causal_kernel"
+            # CTA pairs read pages only when every key tile is whole
+            kernel = kernel if w.S_kv % 128 == 0 else "prefill_causal_kernel"
         else:
             fn = lambda: gqa.gqa_attn_prefill_causal(q, k, v, w.scale, w.q_offset, o, lse, ws)
         us = time_graph(fn, 1, 10)
@@ -699,6 +705,7 @@ def run_all_configs(device):
     decode_line("llama70b_decode_32k", page_size=256)
     decode_line("llama70b_decode_32k", T_q=16, page_size=256)
     prefill_line("chunked_prefill_32k", page_size=256)
+    decode_line("llama70b_decode_32k", cache_keys=131072)
 
 
 def main():

@@ -118,7 +118,13 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
   uint64_t *empty_bar = full_bar + kStages;
 
-  const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  // grid (H_kv, B, splits): the first splits of every (sequence, KV head) come
+  // first in launch order, so a multi-wave grid puts the CTAs that hold keys on
+  // distinct SMs before any empty one; the cluster-merged grid is (splits, H_kv,
+  // B), a cluster along x
+  const int split = kFused ? blockIdx.x : blockIdx.z;
+  const int kv = kFused ? blockIdx.y : blockIdx.x;
+  const int b = kFused ? blockIdx.z : blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_consumers = kConsumerWarps * p.cgroups;  // warps before the producer
   __shared__ int failed;
@@ -769,7 +775,7 @@ cudaError_t decode_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   const long long ctas = (long long)a.num_splits * a.H_kv * a.B;
   if (ctas <= a.num_sms) p.l2_prefetch_tiles = GQA_DECODE_L2_PREFETCH_TILES;  // one wave
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_splits, a.H_kv, a.B);
+  cfg.gridDim = dim3(a.H_kv, a.B, a.num_splits);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

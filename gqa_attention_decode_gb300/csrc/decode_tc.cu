@@ -125,7 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *red_m = reinterpret_cast<float *>(smem + kOffRed);
   float *red_l = red_m + kRows;
 
-  const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  // grid (H_kv, B, splits): the first splits of every (sequence, KV head) come
+  // first in launch order (CTAs that hold keys before empty ones)
+  const int split = blockIdx.z, kv = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == kWarpTma && lane == 0) {
     tma_prefetch_desc(&tm_q);
@@ -594,7 +596,7 @@ cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   p.sl2 = a.scale * 1.4426950408889634f;
   p.wait = a.wait;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_splits, a.H_kv, a.B);
+  cfg.gridDim = dim3(a.H_kv, a.B, a.num_splits);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;

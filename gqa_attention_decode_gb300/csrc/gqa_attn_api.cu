@@ -21,6 +21,10 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxChunkTiles = 32;          // multi-wave plans: at most 2048 keys per split
 constexpr int kMaxChunkTilesOneWave = 32;   // single-wave plans: at most 2048 keys per split
 constexpr int kDecodeCtasPerSm = 2;
+constexpr int kMaxSplits = 65535;        // grid z limit
+// single-wave plans with this many splits per (sequence, KV head) or more
+// spread even one long sequence over the GPU: no cap on their chunks
+constexpr int kMinOneWaveSplits = 16;
 
 struct DeviceState {
   bool ready = false;
@@ -78,8 +82,10 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 
 // Plan: chunks of whole 64-key tiles.  Automatic:
 //  * if one CTA per SM can cover every (batch, KV head) with chunks of at most
-//    kMaxChunkTilesOneWave tiles, use exactly that single wave (no tail, the
-//    fixed per-CTA cost paid once, a deep ring per CTA);
+//    kMaxChunkTilesOneWave tiles, or with at least kMinOneWaveSplits splits
+//    each, use exactly that single wave (no tail, the fixed per-CTA cost paid
+//    once, a deep ring per CTA; the kernels shorten the chunks on the device
+//    for sequences shorter than S_max);
 //  * otherwise chunks of at most kMaxChunkTiles tiles so that two waves' worth
 //    of CTAs per SM keep ragged batches balanced.
 // Splits per (sequence, KV head) of a single-wave plan: one CTA per SM.
@@ -100,7 +106,8 @@ int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_split
   if (num_splits > 0) {
     chunk_tiles = ceil_div(tiles, num_splits < tiles ? num_splits : tiles);
   } else if (units <= num_sms &&
-             ceil_div(tiles, one_wave_splits(units, num_sms)) <= kMaxChunkTilesOneWave) {
+             (ceil_div(tiles, one_wave_splits(units, num_sms)) <= kMaxChunkTilesOneWave ||
+              one_wave_splits(units, num_sms) >= kMinOneWaveSplits)) {
     chunk_tiles = ceil_div(tiles, one_wave_splits(units, num_sms));
   } else {
     const long long want = (long long)num_sms * kDecodeCtasPerSm;
@@ -109,6 +116,8 @@ int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_split
     if (chunk_tiles > kMaxChunkTiles) chunk_tiles = kMaxChunkTiles;
     if (chunk_tiles < 1) chunk_tiles = 1;
   }
+  // splits run along the grid's z dimension: at most 65535 (longer chunks beyond)
+  if (ceil_div(tiles, chunk_tiles) > kMaxSplits) chunk_tiles = ceil_div(tiles, kMaxSplits);
   *out_splits = ceil_div(tiles, chunk_tiles);
   *out_chunk = chunk_tiles * tile;
   return GQA_OK;

@@ -54,8 +54,12 @@ def test_abi_version_and_status_strings(lib):
 @pytest.mark.parametrize("B,H_kv,S_max,sms,req,expect", [
     # one 32K sequence, 8 KV heads, 152 SMs: one wave of 19 splits x 8 heads
     (1, 8, 32768, 152, 0, (19, 1728)),
-    # 128K keys: chunks capped at 2048 keys, several waves of 2 CTAs/SM
-    (1, 8, 131072, 152, 0, (64, 2048)),
+    # 128K keys, one sequence: still one wave of 19 splits (at least 16 per KV
+    # head spread it over the GPU), chunks of 108 tiles
+    (1, 8, 131072, 152, 0, (19, 6912)),
+    # two sequences of 64K keys: 9 splits each, chunks capped at 2048 keys,
+    # several waves of 2 CTAs/SM
+    (2, 8, 65536, 152, 0, (32, 2048)),
     # tiny decode with 4 requested splits of one 64-key tile each
     (1, 1, 256, 152, 4, (4, 64)),
     # ragged batch: chunks capped at 2048 keys

@@ -215,17 +215,21 @@ def test_out_of_range_seqlens_are_clamped_and_reported():
 
 def test_one_million_keys_sampled():
     """One sequence of 2^20 - 37 keys in a 2^20-key cache (Llama3-70B heads): each
-    of K and V is 2 GiB, so element offsets pass 2^31, and the plan cuts the keys
-    into hundreds of splits that the merge combines.  Sampled heads of the first
-    and the last KV head against the oracle."""
+    of K and V is 2 GiB, so element offsets pass 2^31.  Run on the automatic plan
+    (one wave: 19 splits of ~55K keys) and on 512 requested splits that the merge
+    combines.  Sampled heads of the first and the last KV head against the
+    oracle."""
     B, H_q, H_kv, S = 1, 64, 8, 1 << 20
     n = S - 37
     q, k, v, sl = gqa_synth.decode_inputs(B, H_q, H_kv, S, 128, seed=71, device=DEV,
                                           seqlens=[n])
-    splits, chunk = gqa.gqa_attn_decode_plan(B, H_kv, S, torch.cuda.get_device_properties(0)
-                                             .multi_processor_count, 0)
-    assert splits * chunk >= S and splits >= 256
-    o, lse = run_decode(q, k, v, sl, 1 / math.sqrt(128))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    splits, chunk = gqa.gqa_attn_decode_plan(B, H_kv, S, sms, 0)
+    assert splits * chunk >= S and splits * H_kv <= sms
+    splits, chunk = gqa.gqa_attn_decode_plan(B, H_kv, S, sms, 512)
+    assert splits == 512 and splits * chunk >= S
+    runs = [run_decode(q, k, v, sl, 1 / math.sqrt(128)),
+            run_decode(q, k, v, sl, 1 / math.sqrt(128), num_splits=512)]
     picks = [0, 5, 56, 63]                      # KV heads 0 and 7
     ref_o = np.zeros((len(picks), 128))
     ref_lse = np.zeros(len(picks))
@@ -236,8 +240,9 @@ def test_one_million_keys_sampled():
                 ro, rl = oracle.attend_rows(np64(q[0, h])[None], kk, vv, 1 / math.sqrt(128), [n])
                 ref_o[i], ref_lse[i] = ro[0], rl[0]
         del kk, vv
-    compare(torch.stack([o[0, h] for h in picks]), torch.stack([lse[0, h] for h in picks]),
-            ref_o, ref_lse, "2^20 keys")
+    for (o, lse), what in zip(runs, ("one wave", "512 splits")):
+        compare(torch.stack([o[0, h] for h in picks]), torch.stack([lse[0, h] for h in picks]),
+                ref_o, ref_lse, f"2^20 keys, {what}")
 
 
 def test_l2_prefetch_sees_the_preceding_grids_writes():
