@@ -7,11 +7,14 @@ One step = split-KV decode of one token through the attention of all 80
 Llama3-70B layers over a 32K-token cache (B=1, H_q=64, H_kv=8, d=128), each
 layer with its own 128 MiB K/V cache (10 GiB in all, so no call finds its K/V
 in the 126 MB L2), followed by one causal prefill of an 8K prompt (same layer
-shape).  The headline `value` is the
-decode's HBM throughput in GB/s per gqa_attn_decode call (algorithmic bytes:
-every valid K and V row read once, 2*B*H_kv*S*d*2 bytes); the prefill's
-TFLOP/s (4*H_q*d*sum_i(visible keys of row i)) is reported in the `prefill`
-object.
+shape), one decode of the ragged batch of 16 sequences in a 128K-key cache
+(8 GiB of K/V) and one chunked prefill (the last 2K tokens of a 32K prompt).
+The headline `value` is the decode's HBM throughput in GB/s per
+gqa_attn_decode call on the 32K layer (algorithmic bytes: every valid K and
+V row read once, 2*B*H_kv*S*d*2 bytes); the prefill's TFLOP/s
+(4*H_q*d*sum_i(visible keys of row i)) is reported in the `prefill` object,
+the ragged batch and the chunked prefill in `ragged_decode` and
+`chunked_prefill`, each with its roofline.
 
 `--impl reference` times the fp64 CPU oracle (the correctness reference, the
 only "reference implementation" this method has) on the same workload, one
@@ -40,6 +43,8 @@ sys.path.insert(0, ROOT)
 METRIC = "GQA decode HBM GB/s (% of peak); causal prefill TFLOP/s (% of BF16 peak)"
 DECODE_WORKLOAD = "llama70b_decode_32k"
 PREFILL_WORKLOAD = "causal_prefill_8k"
+RAGGED_WORKLOAD = "ragged_decode_b16"
+CHUNKED_WORKLOAD = "chunked_prefill_32k"
 LAYERS = 80         # decode calls per step: one per Llama3-70B layer, each its own K/V cache
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -66,8 +71,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--parts", default="decode,prefill",
-                    help="comma list of decode,prefill (both by default)")
+    ap.add_argument("--parts", default="decode,prefill,ragged,chunked",
+                    help="comma list of decode,prefill,ragged,chunked (all by default)")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="decode calls per step, each on its own K/V copy")
     ap.add_argument("--no-e2e", action="store_true")
@@ -342,6 +347,27 @@ def run_ours(args, rank, world, device):
             dtype=torch.uint8, device=device)
     flops_prefill = prefill_flops(wp)
 
+    # ---- the largest workloads: ragged batch of 16, chunked 32K prefill ----
+    wr = gqa_synth.WORKLOADS[RAGGED_WORKLOAD]
+    if "ragged" in parts:
+        rq, rk, rv, rsl_cpu = gqa_synth.workload_decode_inputs(wr, device)
+        rsl = rsl_cpu.to(device)
+        rws = torch.empty(gqa.gqa_attn_decode_workspace_size(wr.B, wr.H_q, wr.H_kv, wr.S_max,
+                                                             wr.d, sms, wr.num_splits),
+                          dtype=torch.uint8, device=device)
+        ro = torch.empty((wr.B, wr.H_q, wr.d), dtype=torch.bfloat16, device=device)
+        rlse = torch.empty((wr.B, wr.H_q), dtype=torch.float32, device=device)
+        bytes_ragged = decode_bytes(wr, rsl_cpu.tolist())
+    wc = gqa_synth.WORKLOADS[CHUNKED_WORKLOAD]
+    if "chunked" in parts:
+        cq, ck, cv = gqa_synth.workload_prefill_inputs(wc, device)
+        co = torch.empty_like(cq)
+        clse = torch.empty((wc.B, wc.H_q, wc.T_q), dtype=torch.float32, device=device)
+        cws = torch.empty(gqa.gqa_attn_prefill_causal_workspace_size(
+            wc.B, wc.H_q, wc.H_kv, wc.T_q, wc.S_kv, wc.d, wc.q_offset, sms),
+            dtype=torch.uint8, device=device)
+    flops_chunked = prefill_flops(wc)
+
     # kernels one gqa_attn_decode call launches: 1 (cluster-merged single kernel)
     # or 2 (split + merge); with 2, a split-only graph times the dominant kernel
     call_kernels = gqa.gqa_attn_decode_kernel_count(wd.B, wd.H_q, wd.H_kv, wd.S_max, wd.d,
@@ -352,6 +378,12 @@ def run_ours(args, rank, world, device):
     if "prefill" in parts:
         launches_per_step += gqa.gqa_attn_prefill_causal_kernel_count(
             wp.B, wp.H_q, wp.H_kv, wp.T_q, wp.S_kv, wp.d, wp.q_offset, pws.numel(), device)
+    if "ragged" in parts:
+        launches_per_step += gqa.gqa_attn_decode_kernel_count(wr.B, wr.H_q, wr.H_kv, wr.S_max,
+                                                              wr.d, wr.num_splits, device)
+    if "chunked" in parts:
+        launches_per_step += gqa.gqa_attn_prefill_causal_kernel_count(
+            wc.B, wc.H_q, wc.H_kv, wc.T_q, wc.S_kv, wc.d, wc.q_offset, cws.numel(), device)
 
     # The calls of a step are captured once into CUDA graphs; the timed loop
     # replays the graphs with timing events between them, so host overhead
@@ -367,6 +399,12 @@ def run_ours(args, rank, world, device):
     def call_prefill():
         gqa.gqa_attn_prefill_causal(pq, pk, pv, wp.scale, wp.q_offset, po, plse, pws)
 
+    def call_ragged():
+        gqa.gqa_attn_decode(rq, rk, rv, rsl, wr.scale, wr.num_splits, ro, rlse, rws)
+
+    def call_chunked():
+        gqa.gqa_attn_prefill_causal(cq, ck, cv, wc.scale, wc.q_offset, co, clse, cws)
+
     calls = {}
     if "decode" in parts:
         calls["decode"] = call_decode_layers
@@ -374,6 +412,10 @@ def run_ours(args, rank, world, device):
             calls["split"] = call_split_layers
     if "prefill" in parts:
         calls["prefill"] = call_prefill
+    if "ragged" in parts:
+        calls["ragged"] = call_ragged
+    if "chunked" in parts:
+        calls["chunked"] = call_chunked
     for _ in range(max(args.warmup, 3)):          # eager warm-up (also per-device set-up)
         for fn in calls.values():
             fn()
@@ -404,8 +446,16 @@ def run_ours(args, rank, world, device):
             ev[4].record(stream)
             graphs["prefill"].replay()
             ev[5].record(stream)
+        if "ragged" in parts:
+            ev[6].record(stream)
+            graphs["ragged"].replay()
+            ev[7].record(stream)
+        if "chunked" in parts:
+            ev[8].record(stream)
+            graphs["chunked"].replay()
+            ev[9].record(stream)
 
-    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(10)]
     gpu_id = f"GPU-{torch.cuda.get_device_properties(device).uuid}"
     sampler = ClockSampler(gpu_id)
     time.sleep(0.3)
@@ -439,13 +489,19 @@ def run_ours(args, rank, world, device):
                     if "split" in graphs else decode_ms)
     if "prefill" in parts:
         prefill_ms = sum(e[4].elapsed_time(e[5]) for e in events)
+    ragged_ms = chunked_ms = 0.0
+    if "ragged" in parts:
+        ragged_ms = sum(e[6].elapsed_time(e[7]) for e in events)
+    if "chunked" in parts:
+        chunked_ms = sum(e[8].elapsed_time(e[9]) for e in events)
     # max over ranks of every time
-    times = torch.tensor([region_ms, decode_ms, split_ms, prefill_ms], dtype=torch.float64)
+    times = torch.tensor([region_ms, decode_ms, split_ms, prefill_ms, ragged_ms, chunked_ms],
+                         dtype=torch.float64)
     if world > 1:
         t = times.to(device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         times = t.cpu()
-    region_ms, decode_ms, split_ms, prefill_ms = times.tolist()
+    region_ms, decode_ms, split_ms, prefill_ms, ragged_ms, chunked_ms = times.tolist()
     K = args.steps
     result = {
         "metric": METRIC, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -454,7 +510,10 @@ def run_ours(args, rank, world, device):
         "config": {"workload": DECODE_WORKLOAD, "B": wd.B, "H_q": wd.H_q, "H_kv": wd.H_kv,
                    "d": wd.d, "S_kv": wd.S_max, "num_splits": splits, "chunk_keys": chunk,
                    "prefill_workload": PREFILL_WORKLOAD if "prefill" in parts else None,
-                   "step": "+".join(p for p in ("decode", "prefill") if p in parts),
+                   "ragged_workload": RAGGED_WORKLOAD if "ragged" in parts else None,
+                   "chunked_workload": CHUNKED_WORKLOAD if "chunked" in parts else None,
+                   "step": "+".join(p for p in ("decode", "prefill", "ragged", "chunked")
+                                    if p in parts),
                    "layers_per_step": layers,
                    "l2": (f"each of the {layers} decode calls of a step reads its own 128 MiB "
                           f"K/V copy ({layers * 128} MiB rotating set)"),
@@ -495,6 +554,36 @@ def run_ours(args, rank, world, device):
         if "decode" not in parts:
             result["value"] = world * tflops
             result["unit"] = "TFLOP/s"
+    if "ragged" in parts:
+        rus = ragged_ms / K * 1e3
+        gbs = bytes_ragged / (rus * 1e-6) / 1e9
+        rk_count = gqa.gqa_attn_decode_kernel_count(wr.B, wr.H_q, wr.H_kv, wr.S_max, wr.d,
+                                                    wr.num_splits, device)
+        rsplits, rchunk = gqa.gqa_attn_decode_plan(wr.B, wr.H_kv, wr.S_max, sms, wr.num_splits)
+        result["ragged_decode"] = {
+            "workload": RAGGED_WORKLOAD, "value": world * gbs, "unit": "GB/s",
+            "us_per_call": rus, "bytes_per_call": bytes_ragged, "kernels_per_call": rk_count,
+            "seqlens_sum": int(rsl_cpu.sum()), "num_splits": rsplits, "chunk_keys": rchunk,
+            "l2": f"{2 * rk.numel() * 2 >> 30} GiB padded K/V cache, larger than L2",
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_merge_kernel "
+                         "(whole call)", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "frac_of_8tbs_nominal": gbs / 8000.0, "traffic": None,
+                         "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}}
+    if "chunked" in parts:
+        cus = chunked_ms / K * 1e3
+        ctf = flops_chunked / (cus * 1e-6) / 1e12
+        result["chunked_prefill"] = {
+            "workload": CHUNKED_WORKLOAD, "value": world * ctf, "unit": "TFLOP/s",
+            "us_per_call": cus, "flops_per_call": flops_chunked,
+            "kernels_per_call": gqa.gqa_attn_prefill_causal_kernel_count(
+                wc.B, wc.H_q, wc.H_kv, wc.T_q, wc.S_kv, wc.d, wc.q_offset, cws.numel(), device),
+            "roofline": {"bound": "tensor", "kernel": prefill_kernel_name(wc.G) +
+                         " (+ piece merge)", "achieved": ctf, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": ctf / peaks["bf16_tflops"],
+                         "frac_of_sustained": ctf / peaks["bf16_tflops_sustained"],
+                         "traffic": None,
+                         "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)"}}
     result["clocks"] = clocks
 
     # ---- end to end through the host-buffer entry points ----

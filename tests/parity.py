@@ -5,8 +5,11 @@ error <= 1e-3 against the fp64 oracle, lse max-abs error <= 1e-3.
 
 O is bf16, so correct rounding alone can exceed 1e-2 where |O| >= 4 (half a
 bf16 ulp there is 2^-6 = 0.0156).  For elements above the bound the test also
-accepts |O_gpu - bf16(O_oracle)| <= 1 bf16 ulp and reports how many such
-elements it saw; nothing is hidden and no seed is re-picked.
+accepts |O_gpu - bf16(O_oracle)| <= 1 bf16 ulp.  Such an element is counted
+(``ESCAPES`` below; the test session prints the counts per comparison), and
+the escape is only taken where |O_oracle| >= 2: below 2 half a bf16 ulp is at
+most 2^-8 = 0.0039, so an error above 1e-2 there is not a rounding matter.
+Nothing is hidden and no seed is re-picked.
 """
 from __future__ import annotations
 
@@ -16,6 +19,10 @@ import torch
 O_MAX_ABS = 1e-2
 O_MEAN_ABS = 1e-3
 LSE_MAX_ABS = 1e-3
+ESCAPE_MIN_ABS = 2.0
+
+# one record per compare() call: (what, O elements, escapes, o_max, o_mean, lse_max)
+ESCAPES: list[tuple] = []
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:
@@ -28,18 +35,27 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
-    """Asserts the tolerance rules; returns a dict of the observed errors."""
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what="", max_escape_frac=None):
+    """Asserts the tolerance rules; returns a dict of the observed errors.
+
+    ``max_escape_frac``, when given, also bounds the share of O elements that
+    needed the one-ulp escape.
+    """
     o = to_f64(o_gpu) if isinstance(o_gpu, torch.Tensor) else np.asarray(o_gpu, np.float64)
     lse = to_f64(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else np.asarray(lse_gpu, np.float64)
     o_ref = np.asarray(o_ref, np.float64)
     lse_ref = np.asarray(lse_ref, np.float64)
     assert o.shape == o_ref.shape, (o.shape, o_ref.shape)
+    assert lse.shape == lse_ref.shape, (lse.shape, lse_ref.shape)
     assert np.all(np.isfinite(o)), f"{what}: non-finite O"
     err = np.abs(o - o_ref)
     over = err > O_MAX_ABS
     n_over = int(over.sum())
     if n_over:
+        big = np.abs(o_ref[over]) >= ESCAPE_MIN_ABS
+        assert big.all(), (
+            f"{what}: {int((~big).sum())} O elements exceed {O_MAX_ABS} where |O| < "
+            f"{ESCAPE_MIN_ABS}; worst {err.max():.4e}")
         o_ref_bf16 = torch.from_numpy(o_ref[over]).to(torch.bfloat16).double().numpy()
         within_ulp = np.abs(o[over] - o_ref_bf16) <= bf16_ulp(o_ref[over]) * (1 + 1e-9)
         assert within_ulp.all(), (
@@ -52,5 +68,11 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     lerr = np.abs(np.where(both_inf, 0.0, lse - np.where(both_inf, 0.0, lse_ref)))
     lerr_max = float(lerr.max()) if lerr.size else 0.0
     assert lerr_max <= LSE_MAX_ABS, f"{what}: max |dlse| = {lerr_max:.3e}"
-    return {"o_max": float(err.max()) if err.size else 0.0, "o_mean": mean_err,
-            "lse_max": lerr_max, "o_over_bound_within_1ulp": n_over}
+    o_max = float(err.max()) if err.size else 0.0
+    ESCAPES.append((what, int(err.size), n_over, o_max, mean_err, lerr_max))
+    if max_escape_frac is not None and err.size:
+        assert n_over <= max_escape_frac * err.size, (
+            f"{what}: {n_over} of {err.size} O elements needed the one-ulp escape "
+            f"(bound {max_escape_frac:g} of the elements)")
+    return {"o_max": o_max, "o_mean": mean_err,
+            "lse_max": lerr_max, "o_over_bound_within_1ulp": n_over, "o_elements": int(err.size)}

@@ -75,13 +75,74 @@ def test_decode_plan(lib, B, H_kv, S_max, sms, req, expect):
 
 @pytest.mark.parametrize("B,H_kv,S_max,sms", [(1, 8, 32768, 152), (3, 2, 1000, 20),
                                                (16, 8, 131072, 152), (1, 1, 1, 152),
-                                               (7, 3, 4097, 152)])
+                                               (7, 3, 4097, 152),
+                                               # one-wave plans with uncapped chunks
+                                               (1, 8, 1 << 20, 152), (1, 1, 1 << 22, 152)])
 def test_decode_plan_covers_every_key_once(lib, B, H_kv, S_max, sms):
     for req in (0, 1, 3, 1000):
         splits, chunk = gqa.gqa_attn_decode_plan(B, H_kv, S_max, sms, req)
         assert chunk % 64 == 0 and chunk > 0 and splits >= 1
         assert splits * chunk >= S_max          # the splits cover the cache
         assert (splits - 1) * chunk < S_max     # and no split starts past it
+
+
+def _tc_splits(S_max, chunk):
+    """The tcgen05 kernel's plan: the chunk rounded up to whole 128-key tiles."""
+    c = -(-chunk // 128) * 128
+    return -(-S_max // c), c
+
+
+@pytest.mark.parametrize("B,H_kv,S_max", [(1, 8, (1 << 31) - 1), (1, 1, (1 << 31) - 64),
+                                          (2, 8, (1 << 31) - 1000), (1, 8, 1 << 30)])
+@pytest.mark.parametrize("req", [0, 100000])
+def test_decode_plan_split_cap_near_int_max(lib, B, H_kv, S_max, req):
+    """Splits run along the grid's z dimension (at most 65535): caches near 2^31
+    keys get longer chunks instead, on both decode kernels."""
+    splits, chunk = gqa.gqa_attn_decode_plan(B, H_kv, S_max, 152, req)
+    assert 1 <= splits <= 65535 and chunk % 64 == 0
+    assert splits * chunk >= S_max and (splits - 1) * chunk < S_max
+    # the tensor-core path (G > 8, or G * T_q > 32 rows) rounds chunks to 128 keys
+    tc_splits, tc_chunk = _tc_splits(S_max, chunk)
+    assert 1 <= tc_splits <= splits <= 65535
+    assert tc_splits * tc_chunk >= S_max and (tc_splits - 1) * tc_chunk < S_max
+    H_q = 16 * H_kv                                            # G = 16
+    assert gqa.gqa_attn_decode_workspace_size(B, H_q, H_kv, S_max, 128, 152, req) == \
+        -(-(B * H_q * tc_splits * 129 * 4) // 256) * 256
+    assert gqa.gqa_attn_decode_multi_workspace_size(B, 8 * H_kv, H_kv, 16, S_max, 128, 152,
+                                                    req) == \
+        -(-(B * 8 * H_kv * 16 * tc_splits * 129 * 4) // 256) * 256
+
+
+def _device_chunk(seqlen, B, S_max, chunk, splits, H_kv, num_sms, tile):
+    """The kernels' per-sequence chunk rule, restated with exact integer division:
+    the sequence's tiles spread as if the batch held B like it, at most the
+    host's chunk, at least what fits the sequence into the grid's splits."""
+    if seqlen >= S_max:
+        return chunk
+    t = -(-seqlen // tile)
+    chunk_tiles = chunk // tile
+    work = t * H_kv * B
+    c = chunk_tiles if work >= (1 << 20) else -(-work // num_sms)
+    c = min(c, chunk_tiles)
+    c = max(c, -(-t // splits) if t < (1 << 20) else chunk_tiles)
+    return max(c, 1) * tile
+
+
+@pytest.mark.parametrize("B,H_kv,S_max", [(1, 8, 32768), (16, 8, 131072), (1, 8, 1 << 20),
+                                          (1, 1, 1 << 22), (4, 8, 65536), (3, 2, 1000)])
+@pytest.mark.parametrize("req", [0, 7, 1000])
+def test_device_chunk_fits_the_grid(lib, B, H_kv, S_max, req):
+    """For any length in [0, S_max] the device-side chunk never exceeds the host's
+    and fits the sequence into the grid's splits, so every key is covered."""
+    splits, chunk = gqa.gqa_attn_decode_plan(B, H_kv, S_max, 152, req)
+    rng = np.random.default_rng(S_max + req)
+    lens = {0, 1, 63, 64, 65, S_max - 1, S_max} | set(int(x) for x in
+                                                       rng.integers(0, S_max + 1, 300))
+    for tile, (sp, ch) in ((64, (splits, chunk)), (128, _tc_splits(S_max, chunk))):
+        for n in sorted(x for x in lens if 0 <= x <= S_max):
+            c = _device_chunk(n, B, S_max, ch, sp, H_kv, 152, tile)
+            assert c % tile == 0 and 0 < c <= ch
+            assert -(-n // c) <= sp
 
 
 def test_workspace_size(lib):

@@ -1,10 +1,11 @@
 """GPU parity of the causal GQA prefill against the fp64 oracle, through the C ABI.
 
 Small cases span several 128-row and 128-key tiles with ragged tails and are
-compared in full; the two prefill workloads (8K causal, and the last 2K chunk
-of a 32K prompt with q_offset = 30720) are run at full size and compared on
-sampled rows, which include the first rows (few visible keys), rows around
-tile boundaries and the last rows.
+compared in full; so are the two prefill workloads (8K causal, and the last
+2K chunk of a 32K prompt with q_offset = 30720), at full size.  Longer
+problems outside the workload list (a 32K square prompt, 256 tokens after
+128K keys, G = 16) are compared on sampled rows: the first rows (few visible
+keys), rows around tile boundaries and the last rows.
 """
 import math
 
@@ -65,36 +66,17 @@ def test_small_cases_full_compare(B, H_q, H_kv, T_q, S_kv, q_offset):
     compare(o, lse, o_ref, lse_ref, f"prefill {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
 
 
-def _sampled_rows(w, n_random, seed):
-    rng = np.random.default_rng(seed)
-    rows = {0, 1, 2, 3, 127, 128, 129, 255, 256, w.T_q - 2, w.T_q - 1}
-    rows |= set(int(x) for x in rng.integers(0, w.T_q, n_random))
-    picks = []
-    for i in sorted(r for r in rows if 0 <= r < w.T_q):
-        picks.append((0, int(rng.integers(0, w.H_q)), i))
-    for h in (0, 1, 7, 8, 63):
-        picks.append((0, h, int(rng.integers(0, w.T_q))))
-    return picks
-
-
 @pytest.mark.parametrize("name", ["causal_prefill_8k", "chunked_prefill_32k"])
-def test_prefill_workloads_sampled(name):
+def test_prefill_workloads_full(name):
+    """Both prefill workloads at full size, every (head, row) against the oracle
+    (the oracle runs in parallel processes over (KV head, row range) pieces)."""
+    from oracle_pool import prefill_causal_parallel
     w = gqa_synth.WORKLOADS[name]
     q, k, v = gqa_synth.workload_prefill_inputs(w, DEV)
     o, lse = run(q, k, v, w.q_offset, w.scale)
-    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-    picks = _sampled_rows(w, 48, 7)
-    ref_o = np.zeros((len(picks), w.d))
-    ref_lse = np.zeros(len(picks))
-    G = w.G
-    for r, (b, h, i) in enumerate(picks):
-        n = w.q_offset + i + 1
-        ro, rl = oracle.attend_rows(np64(q[b, h, i])[None], np64(k[b, h // G, :n]),
-                                    np64(v[b, h // G, :n]), w.scale, [n])
-        ref_o[r], ref_lse[r] = ro[0], rl[0]
-    got_o = torch.stack([o[b, h, i] for b, h, i in picks])
-    got_lse = torch.stack([lse[b, h, i] for b, h, i in picks])
-    compare(got_o, got_lse, ref_o, ref_lse, name)
+    qn, kn, vn = (t.float().cpu().numpy() for t in (q, k, v))
+    o_ref, lse_ref = prefill_causal_parallel(qn, kn, vn, w.q_offset, w.scale)
+    compare(o, lse, o_ref, lse_ref, name, max_escape_frac=1e-5)
 
 
 def _seeded_configs(n, seed):
@@ -120,22 +102,15 @@ def test_seeded_random_shapes(B, H_q, H_kv, T_q, S_kv, q_offset):
     compare(o, lse, o_ref, lse_ref, f"random {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
 
 
-def test_group_of_16_sampled():
-    """G = 16 (four head quads per KV head), 4K causal, sampled rows."""
+def test_group_of_16_full():
+    """G = 16 (four head quads per KV head), 4K causal, every row."""
+    from oracle_pool import prefill_causal_parallel
     B, H_q, H_kv, T = 1, 32, 2, 4096
     q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T, T, 128, seed=38, device=DEV)
     o, lse = run(q, k, v, 0, 1 / math.sqrt(128))
-    rng = np.random.default_rng(8)
-    picks = [(0, int(h), int(i)) for h, i in zip(rng.integers(0, H_q, 40), rng.integers(0, T, 40))]
-    picks += [(0, 31, T - 1), (0, 16, 0), (0, 15, 128)]
-    ref_o = np.zeros((len(picks), 128))
-    ref_lse = np.zeros(len(picks))
-    for r, (b, h, i) in enumerate(picks):
-        ro, rl = oracle.attend_rows(np64(q[b, h, i])[None], np64(k[b, h // 16, :i + 1]),
-                                    np64(v[b, h // 16, :i + 1]), 1 / math.sqrt(128), [i + 1])
-        ref_o[r], ref_lse[r] = ro[0], rl[0]
-    compare(torch.stack([o[b, h, i] for b, h, i in picks]),
-            torch.stack([lse[b, h, i] for b, h, i in picks]), ref_o, ref_lse, "G = 16")
+    o_ref, lse_ref = prefill_causal_parallel(*(t.float().cpu().numpy() for t in (q, k, v)), 0,
+                                             1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, "G = 16, 4K causal", max_escape_frac=1e-5)
 
 
 @pytest.mark.parametrize("H_q,H_kv", [(8, 2), (4, 2)])   # G = 4 (CTA pairs), G = 2 (one CTA)
@@ -220,26 +195,18 @@ def test_key_split_scores_jump_between_pieces():
     compare(o, lse, o_ref, lse_ref, "split, scores jump between pieces")
 
 
-def test_short_chunk_after_long_prefix_sampled():
+def test_short_chunk_after_long_prefix_full():
     """A 128-token chunk after 32K keys (Llama3-70B layer): 16 units on 76 pairs,
-    each cut in 4 pieces; sampled rows against the oracle."""
+    each cut in 4 pieces; every row against the oracle."""
+    from oracle_pool import prefill_causal_parallel
     B, H_q, H_kv, T_q, S_kv = 1, 64, 8, 128, 32768
     q_offset = S_kv - T_q
     q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=43, device=DEV)
     o, lse = gqa.gqa_attn_prefill_causal(q, k, v, 1 / math.sqrt(128), q_offset)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(9)
-    picks = [(0, int(h), int(i)) for h, i in zip(rng.integers(0, H_q, 24), rng.integers(0, T_q, 24))]
-    picks += [(0, 0, 0), (0, 63, 127), (0, 7, 64)]
-    ref_o = np.zeros((len(picks), 128))
-    ref_lse = np.zeros(len(picks))
-    for r, (b, h, i) in enumerate(picks):
-        n = q_offset + i + 1
-        ro, rl = oracle.attend_rows(np64(q[b, h, i])[None], np64(k[b, h // 8, :n]),
-                                    np64(v[b, h // 8, :n]), 1 / math.sqrt(128), [n])
-        ref_o[r], ref_lse[r] = ro[0], rl[0]
-    compare(torch.stack([o[b, h, i] for b, h, i in picks]),
-            torch.stack([lse[b, h, i] for b, h, i in picks]), ref_o, ref_lse, "128 after 32K")
+    o_ref, lse_ref = prefill_causal_parallel(*(t.float().cpu().numpy() for t in (q, k, v)),
+                                             q_offset, 1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, "128 after 32K")
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.15, 0.3])
@@ -293,17 +260,30 @@ def test_rejects_bad_q_offset_and_misalignment():
     assert e.value.status == gqa.GQA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("T_q,S_kv", [(256, 131072), (32768, 32768)])
-def test_long_context_sampled(T_q, S_kv):
-    """A 256-token chunk after 128K keys (32 units on the CTA pairs, each split by
-    key range) and a 32K square causal prefill; sampled rows against the oracle."""
+def test_chunk_after_128k_keys_full():
+    """A 256-token chunk after 128K keys: 32 units on the CTA pairs, each split by
+    key range; every row against the oracle."""
+    from oracle_pool import prefill_causal_parallel
+    B, H_q, H_kv, T_q, S_kv = 1, 64, 8, 256, 131072
+    q_offset = S_kv - T_q
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=72, device=DEV)
+    o, lse = run(q, k, v, q_offset, 1 / math.sqrt(128))
+    o_ref, lse_ref = prefill_causal_parallel(*(t.float().cpu().numpy() for t in (q, k, v)),
+                                             q_offset, 1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, "256 after 128K", max_escape_frac=1e-5)
+
+
+def test_long_context_sampled():
+    """A 32K square causal prefill (too long for the oracle in full); sampled rows
+    against the oracle."""
+    T_q = S_kv = 32768
     B, H_q, H_kv = 1, 64, 8
     q_offset = S_kv - T_q
     q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=72, device=DEV)
     o, lse = run(q, k, v, q_offset, 1 / math.sqrt(128))
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
     rng = np.random.default_rng(10)
-    rows = sorted({0, 127, 128, T_q - 1} | set(int(x) for x in rng.integers(0, T_q, 6)))
+    rows = sorted({0, 127, 128, T_q - 1} | set(int(x) for x in rng.integers(0, T_q, 40)))
     picks = [(0, int(rng.integers(0, H_q)), i) for i in rows]
     ref_o = np.zeros((len(picks), 128))
     ref_lse = np.zeros(len(picks))
