@@ -44,4 +44,10 @@ from ._binding import (  # noqa: F401
     gqa_attn_selftest_bounded_wait,
     gqa_attn_bounds_checked,
     gqa_attn_selftest_bounds,
+    gqa_attn_debug_s_tile_count,
+)
+from .sequence_parallel import (  # noqa: F401
+    block_seqlens,
+    decode_sequence_parallel,
+    gather_states,
 )

@@ -75,6 +75,7 @@ _SIGNATURES = {
     "gqa_attn_selftest_bounded_wait": (_c_int, [_c_int, _vp]),
     "gqa_attn_bounds_checked": (_c_int, []),
     "gqa_attn_selftest_bounds": (_c_int, [_vp]),
+    "gqa_attn_debug_s_tile_count": (_c_int, [_vp, ctypes.POINTER(ctypes.c_ulonglong)]),
 }
 
 
@@ -609,6 +610,19 @@ def gqa_attn_selftest_bounds(stream=None, device=None) -> None:
     with torch.cuda.device(dev):
         _check(load_library().gqa_attn_selftest_bounds(_stream_handle(stream, dev)),
                "gqa_attn_selftest_bounds")
+
+
+def gqa_attn_debug_s_tile_count(stream=None, device=None) -> int:
+    """Bounds-checked builds: S = Q K^T tile products (per query head and 128-key
+    tile) the prefill kernels issued since the previous call; the counter resets.
+    Raises GQAError (GQA_ERR_UNSUPPORTED) in release builds."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    out = ctypes.c_ulonglong(0)
+    with torch.cuda.device(dev):
+        _check(load_library().gqa_attn_debug_s_tile_count(_stream_handle(stream, dev),
+                                                          ctypes.byref(out)),
+               "gqa_attn_debug_s_tile_count")
+    return int(out.value)
 
 
 def gqa_attn_selftest_bounded_wait(timeout_us: int, stream=None, device=None) -> None:

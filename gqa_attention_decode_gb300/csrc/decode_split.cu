@@ -142,16 +142,25 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     // One-wave grid: pull the first tiles of this split's key range into L2
-    // while the preceding grid finishes (its length is not known yet, so the
-    // range is the split's whole chunk; keys past the sequence are masked
-    // later).  Only a grid that is resident all at once can overlap the
-    // preceding grid; in a larger one, splits past their sequence's end would
-    // only prefetch padding.  A paged cache's table is read here ahead of the
-    // wait as a hint only (relaxed loads, ids outside the pool skipped): the
-    // loads that matter read it again after the wait.
-    const int tiles = min(p.l2_prefetch_tiles, p.chunk / kTileKeys);
+    // while the preceding grid finishes.  Only a grid that is resident all at
+    // once can overlap the preceding grid; in a larger one, splits past their
+    // sequence's end would only prefetch padding.  The sequence length and a
+    // paged cache's table are read here ahead of the wait as hints only
+    // (relaxed loads; the preceding grid may still write them): the length
+    // gives this split's device-side chunk and where the sequence ends, and a
+    // stale value costs at most a wasted L2 fill.  Everything that matters is
+    // read again after the wait.
+    int tiles = 0, key_first = 0;
+    if (p.l2_prefetch_tiles > 0) {
+      const int len = min(max(ld_relaxed_s32(p.seqlens + b), 0), p.S_max);
+      const int c = device_chunk(len, p.B, p.S_max, p.chunk, p.num_splits, p.H_kv, p.num_sms,
+                                 kTileKeys);
+      key_first = split * c;
+      const int n = min(key_first + c, len) - key_first;
+      tiles = n > 0 ? min(p.l2_prefetch_tiles, (n + kTileKeys - 1) / kTileKeys) : 0;
+    }
     for (int i = 0; i < tiles; ++i) {
-      const int key0 = split * p.chunk + i * kTileKeys;
+      const int key0 = key_first + i * kTileKeys;
       int c2 = key0, c3 = b * p.H_kv + kv;
       if (kPaged) {
         const int page = key0 / p.page_size;

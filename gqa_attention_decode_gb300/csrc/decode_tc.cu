@@ -136,19 +136,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // One-wave grid: the first key tile of this split's chunk is pulled into L2
   // while the preceding grid finishes (L2 is the point of coherence, so this is
-  // safe ahead of the wait; the sequence length is not known yet).  A paged
-  // cache's block-table entry is read here as a hint only: a preceding grid
-  // may still write it, and the loads after the wait read it again, so a stale
-  // entry costs one wasted L2 fill; an id outside the pool is skipped.
+  // safe ahead of the wait).  The sequence length and a paged cache's
+  // block-table entry are read here as hints only (relaxed loads): a preceding
+  // grid may still write them, and the loads after the wait read them again,
+  // so a stale value costs one wasted L2 fill; the length gives this split's
+  // device-side chunk, and a split that starts past the sequence prefetches
+  // nothing; an id outside the pool is skipped.
   if (p.l2_prefetch && warp == kWarpTma && lane == 0 && p.chunk >= kBN) {
-    const int key0 = split * p.chunk;
+    const int len = min(max(ld_relaxed_s32(p.seqlens + b), 0), p.S_max);
+    const int key0 =
+        split * device_chunk(len, p.B, p.S_max, p.chunk, p.num_splits, p.H_kv, p.num_sms, kBN);
     int c2 = key0, c3 = b * p.H_kv + kv;
-    bool go = true;
+    bool go = key0 < len;
     if (p.block_table != nullptr) {
       const int page = key0 / p.page_size;
       const int page_id =
           page < p.max_pages ? ld_relaxed_s32(p.block_table + (size_t)b * p.max_pages + page) : -1;
-      go = page_id >= 0 && page_id < p.num_pages;
+      go = go && page_id >= 0 && page_id < p.num_pages;
       c2 = key0 - page * p.page_size;
       c3 = page_id * p.H_kv + kv;
     }

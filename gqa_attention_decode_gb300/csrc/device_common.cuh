@@ -36,7 +36,23 @@ __device__ __forceinline__ bool store_ok(size_t idx, size_t extent, int *status)
 struct WaitCtl {
   int *status;          // device status word (never null)
   uint64_t timeout_ns;  // per-wait limit
+#ifdef GQA_DEBUG_BOUNDS
+  unsigned long long *s_tiles;  // S = Q K^T tile products issued (one per query head and key tile)
+#endif
 };
+
+// Bounds-checked builds count every S = Q K^T product of one query head's
+// 128-row tile with one 128-key tile that a prefill kernel issues, so a test can
+// hold the total against the causal (lower-triangular) tile count; release
+// builds compile this away.
+__device__ __forceinline__ void count_s_tiles(const WaitCtl &w, unsigned n) {
+#ifdef GQA_DEBUG_BOUNDS
+  atomicAdd(w.s_tiles, (unsigned long long)n);
+#else
+  (void)w;
+  (void)n;
+#endif
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -15,6 +15,11 @@ namespace {
 // Status word written by bounded waits that run out (one per device, in the
 // library's static device memory; read and cleared by gqa_attn_device_status).
 __device__ int g_wait_status;
+#ifdef GQA_DEBUG_BOUNDS
+// S tile products issued by the prefill kernels (bounds-checked builds only; read
+// and cleared by gqa_attn_debug_s_tile_count).
+__device__ unsigned long long g_s_tiles;
+#endif
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxDevices = 64;
@@ -32,6 +37,7 @@ struct DeviceState {
   int fused_clusters[gqa::kDecodeMaxFusedSplits + 1] = {};
   int prefill_pairs = 0;  // clusters of two of the CTA-pair prefill kernel resident at once
   int *status = nullptr;
+  unsigned long long *s_tiles = nullptr;  // bounds-checked builds: the S tile counter
 };
 
 std::mutex g_mutex;
@@ -63,6 +69,11 @@ int device_state(DeviceState **out) {
       return GQA_ERR_CUDA;
     void *status = nullptr;
     if (cudaGetSymbolAddress(&status, g_wait_status) != cudaSuccess) return GQA_ERR_CUDA;
+#ifdef GQA_DEBUG_BOUNDS
+    void *s_tiles = nullptr;
+    if (cudaGetSymbolAddress(&s_tiles, g_s_tiles) != cudaSuccess) return GQA_ERR_CUDA;
+    st.s_tiles = static_cast<unsigned long long *>(s_tiles);
+#endif
     if (gqa::decode_prepare_device(st.fused_clusters) != cudaSuccess) return GQA_ERR_CUDA;
     if (gqa::prefill_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
     if (gqa::decode_tc_prepare_device() != cudaSuccess) return GQA_ERR_CUDA;
@@ -312,6 +323,9 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   a.fused_clusters = st->fused_clusters;
   a.wait.status = st->status;
   a.wait.timeout_ns = kWaitTimeoutNs;
+#ifdef GQA_DEBUG_BOUNDS
+  a.wait.s_tiles = st->s_tiles;
+#endif
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (phase == kPhaseBoth && !tensor_cores && gqa::decode_fused_eligible(a)) {
     return gqa::decode_fused_launch(a, s, g_encode) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
@@ -467,6 +481,9 @@ gqa::PrefillLaunch prefill_launch_args(const gqa_bf16_t *q, const gqa_bf16_t *k,
   a.ws_bytes = workspace ? ws_bytes : 0;
   a.wait.status = st->status;
   a.wait.timeout_ns = kWaitTimeoutNs;
+#ifdef GQA_DEBUG_BOUNDS
+  a.wait.s_tiles = st->s_tiles;
+#endif
   return a;
 }
 }  // namespace
@@ -770,6 +787,9 @@ GQA_API int gqa_attn_selftest_bounded_wait(int timeout_us, gqa_stream_t stream) 
   gqa::WaitCtl w;
   w.status = st->status;
   w.timeout_ns = (uint64_t)timeout_us * 1000ull;
+#ifdef GQA_DEBUG_BOUNDS
+  w.s_tiles = st->s_tiles;
+#endif
   return to_status(gqa::selftest_bounded_wait_launch(w, static_cast<cudaStream_t>(stream)));
 }
 
@@ -778,6 +798,28 @@ GQA_API int gqa_attn_bounds_checked(void) {
   return 1;
 #else
   return 0;
+#endif
+}
+
+GQA_API int gqa_attn_debug_s_tile_count(gqa_stream_t stream, unsigned long long *out_count) {
+#ifndef GQA_DEBUG_BOUNDS
+  (void)stream;
+  (void)out_count;
+  return GQA_ERR_UNSUPPORTED;  // release builds count nothing
+#else
+  if (!out_count) return GQA_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int rc = device_state(&st);
+  if (rc != GQA_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
+  unsigned long long value = 0;
+  if (cudaMemcpy(&value, st->s_tiles, sizeof(value), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  const unsigned long long zero = 0;
+  if (cudaMemcpy(st->s_tiles, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  *out_count = value;
+  return GQA_OK;
 #endif
 }
 

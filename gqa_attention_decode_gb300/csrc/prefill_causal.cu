@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_ss(t_s[i], tc::desc_advance(i == 0 ? dq0 : dq1, kmajor_step(kk)),
                            tc::desc_advance(dk, kmajor_step(kk)), idesc_s, kk > 0 ? 1u : 0u);
               tc::commit(s_full(i));
+              count_s_tiles(p.wait, 1);
               if (i == 1) {
                 tc::commit(kv_empty(ldK % kStages));
                 if (j == n - 1) tc::commit(q_empty);

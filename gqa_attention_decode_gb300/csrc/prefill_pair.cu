@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_ss_pair(t_s[i], tc::desc_advance(i == 0 ? dq0 : dq1, q_step(kk)),
                                 tc::desc_advance(dk, k_step(kk)), idesc_s, kk > 0 ? 1u : 0u);
               tc::commit_pair(s_full(i), kBothCtas);
+              count_s_tiles(p.wait, 2);  // one query head in each CTA of the pair
               if (i == 1) {
                 tc::commit_pair(kv_empty(ldK % kStages), kBothCtas);
                 if (j == n - 1) tc::commit_pair(q_empty, kBothCtas);

@@ -527,6 +527,25 @@ GQA_API int gqa_attn_selftest_bounded_wait(int timeout_us, gqa_stream_t stream);
 GQA_API int gqa_attn_bounds_checked(void);
 GQA_API int gqa_attn_selftest_bounds(gqa_stream_t stream);
 
+/*
+ * Causal tile count (ADR-0060, section 11 "Verification plan": the causal
+ * prefill must issue the lower-triangular number of Q K^T tile products, never
+ * a full square).  Bounds-checked builds count every S = Q K^T product of one
+ * query head's 128-row tile with one 128-key tile that the prefill kernels
+ * issue (key-range pieces of a split unit each count their own tiles).  This
+ * call waits for `stream`, stores the count since the previous call in
+ * *out_count and resets it to 0 (a device-wide counter: concurrent prefill
+ * calls on other streams add to it).  Release builds return GQA_ERR_UNSUPPORTED.
+ * Expected values: query tile t of a head (rows [128t, min(128t + 128, T_q)))
+ * sees key tiles 0 .. (q_offset + min(128t + 128, T_q) - 1) / 128, and the sum of
+ * those counts over every (sequence, query head, query tile) is the causal
+ * count.  One known excess: for odd group sizes the group's last head runs query
+ * tiles t and t - 1 in one unit over tile t's key range (one more key tile for
+ * tile t - 1, wholly in its future and masked), and a lone tile 0 in such a unit
+ * is paired with a discarded copy of itself.
+ */
+GQA_API int gqa_attn_debug_s_tile_count(gqa_stream_t stream, unsigned long long *out_count);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -7,7 +7,9 @@ stand-in for a memory checker.  The calls below reach the warp-MMA and
 tcgen05 decode kernels (dense and paged, one and many tokens, the
 single-kernel cluster merge and split + merge), both causal prefill kernels
 with and without the key-range split, and the merge of shard states; none may
-record a violation, and sampled results must match the oracle.  The library
+record a violation, and the results must match the oracle.  The same build
+counts the S = Q K^T tile products the prefill kernels issue, which must equal
+the causal (lower-triangular) count of the design record's verification plan.  The library
 is loaded in a child process (one library per process).
 """
 import os
@@ -72,14 +74,47 @@ SCRIPT = textwrap.dedent("""
                                            sl.numpy(), 0.088)
         compare(o, lse, o_ref, l_ref, "debug short in long cache")
 
-    # prefill: CTA pairs (G = 8, 4) and one CTA per unit (G = 3, 1), whole and split
-    for (H_q, H_kv, T, S) in [(16, 2, 300, 300), (8, 2, 128, 4096), (6, 2, 200, 200),
-                              (6, 2, 128, 4096), (4, 4, 256, 2304), (16, 2, 200, 3000)]:
+    # The record's causal tile count (section 11): query tile t of a head sees key
+    # tiles 0 .. (q_offset + min(128 t + 128, T_q) - 1) // 128; the kernels must
+    # issue exactly that many S products per head and tile -- plus, for odd group
+    # sizes, the known extra of the group's last head, which runs query tiles t
+    # and t - 1 together over tile t's key range (a lone tile 0 with a discarded
+    # copy of itself).
+    def n_kv(t, T_q, q_offset):
+        return (q_offset + min(128 * t + 128, T_q) - 1) // 128 + 1
+
+    def causal_s_tiles(B, H_q, T_q, q_offset):
+        return B * H_q * sum(n_kv(t, T_q, q_offset) for t in range(-(-T_q // 128)))
+
+    def issued_s_tiles(B, H_q, H_kv, T_q, q_offset):
+        G, n_qt = H_q // H_kv, -(-T_q // 128)
+        extra = 0
+        if G % 2 == 1:
+            for r in range(0, n_qt, 2):
+                t0 = n_qt - 1 - r
+                extra += (n_kv(t0, T_q, q_offset) - n_kv(t0 - 1, T_q, q_offset) if t0 > 0
+                          else n_kv(0, T_q, q_offset))
+        return causal_s_tiles(B, H_q, T_q, q_offset) + B * H_kv * extra
+
+    gqa.gqa_attn_debug_s_tile_count()          # start from zero
+    # prefill: CTA pairs (G = 8, 4) and one CTA per unit (G = 3, 1, 2), whole and split
+    for (B, H_q, H_kv, T, S) in [(1, 16, 2, 300, 300), (1, 8, 2, 128, 4096), (1, 6, 2, 200, 200),
+                                 (1, 6, 2, 128, 4096), (1, 4, 4, 256, 2304),
+                                 (1, 16, 2, 200, 3000), (2, 16, 2, 1024, 1024),
+                                 (1, 8, 4, 1000, 1000), (1, 3, 3, 640, 700),
+                                 (1, 64, 8, 2048, 2048), (1, 64, 8, 512, 8192)]:
         qo = S - T
-        q, k, v = gqa_synth.prefill_inputs(1, H_q, H_kv, T, S, 128, seed=3, device=dev)
+        q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T, S, 128, seed=3, device=dev)
         o, lse = gqa.gqa_attn_prefill_causal(q, k, v, 0.088, qo)
         torch.cuda.synchronize()
-        ok(("prefill", H_q, H_kv, T, S))
+        ok(("prefill", B, H_q, H_kv, T, S))
+        got = gqa.gqa_attn_debug_s_tile_count()
+        want = issued_s_tiles(B, H_q, H_kv, T, qo)
+        assert got == want, ("S tile count", B, H_q, H_kv, T, S, got, want)
+        if (H_q // H_kv) % 2 == 0:   # no odd-group extra: exactly the lower triangle
+            assert got == causal_s_tiles(B, H_q, T, qo)
+        print("S tiles", (B, H_q, H_kv, T, S), got, "causal", causal_s_tiles(B, H_q, T, qo),
+              "square", B * H_q * (-(-T // 128)) * (-(-S // 128)))
         o_ref, l_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), qo, 0.088)
         compare(o, lse, o_ref, l_ref, "debug prefill")
 
