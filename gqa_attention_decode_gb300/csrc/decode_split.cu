@@ -529,17 +529,20 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// One CTA per (query head, new token) row of a sequence, 256 threads: thread
-// (g, lane) owns columns 4*lane .. 4*lane+3 and merges splits g, g+8, g+16, ...
+// One CTA per (query head, new token) row of a sequence, 128 threads: thread
+// (g, lane) owns columns 4*lane .. 4*lane+3 and merges splits g, g+4, g+8, ...
 // with an online log-sum-exp, kMergeRound splits per round whose lse and O
 // loads are all issued before any is used (one L2 round trip for up to 32
-// splits); the eight group states are then combined once in shared memory.
+// splits); the four group states are then combined once in shared memory.
+// Small CTAs keep every row of a large merge (16 new tokens of 64 heads, or a
+// batch of 16 sequences: 1024 rows) resident in one wave (9 CTAs per SM at 56
+// registers); 256-thread CTAs at 44 registers fit 5 per SM and took two waves.
 // lse = m + ln sum_s exp(lse_s - m); O = sum_s exp(lse_s - lse) O_s.
 // Launched as a programmatic dependent of the split kernel; the partials are
 // read through L2 (they were written by the split grid).
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;
 constexpr int kMergeGroups = kMergeThreads / 32;
-constexpr int kMergeRound = 4;
+constexpr int kMergeRound = 8;
 
 __global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,

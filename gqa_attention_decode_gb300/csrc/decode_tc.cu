@@ -46,11 +46,11 @@ constexpr int kOffQ = 0;
 constexpr int kOffStage = kTileBytes;
 constexpr int kOffBar = kOffStage + kStages * kTileBytes;
 // barriers: kv_full[S], kv_empty[S], q_full, s_full[2], p_full[2], o_final[2], tok[2],
-// slot-1 epilogue, drain, V tail cleared
-constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+// drain, V tail cleared
+constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 2 + 2 + 1 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;        // tmem slot, abort flag
-constexpr int kOffRed = kOffMisc + 16;                  // slot-1 (m, l) per row
-constexpr int kSmemBytes = kOffRed + 2 * kRows * 4 + 1024;
+constexpr int kOffRed = kOffMisc + 16;                  // (m, l) of both slots per row
+constexpr int kSmemBytes = kOffRed + 4 * kRows * 4 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kSumTrigger = 256.0f;      // 2^kRescaleThreshold
@@ -86,6 +86,19 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   }
 }
 
+// Barrier over the 256 softmax threads (warps 0-7, named barrier 1) that also
+// returns the AND of their flags.
+__device__ __forceinline__ bool softmax_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
 // Operand descriptors, built once per tile and advanced per k-step by a
 // compile-time byte offset.  K-major 128-row tile stored as two 128B-swizzled
 // 64-column halves (k-step kk = 16 columns); MN-major V tile (keys x d, d
@@ -117,13 +130,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto p_full = [&](int i) { return bar0 + 8u * (2 * kStages + 3 + i); };
   auto o_final = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + i); };
   auto tok = [&](int i) { return bar0 + 8u * (2 * kStages + 7 + i); };
-  const uint32_t slot1_done = bar0 + 8u * (2 * kStages + 9);
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 10);
-  const uint32_t v_tail = bar0 + 8u * (2 * kStages + 11);
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 9);
+  const uint32_t v_tail = bar0 + 8u * (2 * kStages + 10);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
-  float *red_m = reinterpret_cast<float *>(smem + kOffRed);
-  float *red_l = red_m + kRows;
+  float *red_m = reinterpret_cast<float *>(smem + kOffRed);  // [slot][row]
+  float *red_l = red_m + 2 * kRows;
 
   // grid (H_kv, B, splits): the first splits of every (sequence, KV head) come
   // first in launch order (CTAs that hold keys before empty ones)
@@ -175,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_final(i), 1);
       mbar_init(tok(i), 128);
     }
-    mbar_init(slot1_done, 128);
     mbar_init(drain_bar, 1);
     mbar_init(v_tail, 1);
     *abort_flag = 0;
@@ -388,8 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
         return pos_scale ? mx * p.sl2 : mx;
       };
-      uint32_t pk[kBN / 2];
-      // P = exp2(s * scale log2e - ref) as bf16 pairs; ref = 0 while no key was seen
+      // P = exp2(s * scale log2e - ref) as bf16 pairs, packed in place over the
+      // scores (pair e goes to sv[e], whose score was already used); ref = 0 while
+      // no key was seen
       auto exp_pass = [&]() {
         const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
         const uint64_t mul2 = f32x2(mul, mul), negm2 = f32x2(negm, negm);
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       x0, x1);
           const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           rs2[e & 1] = add_f32x2(rs2[e & 1], f32x2(p0, p1));
-          pk[e] = pack_bf16x2(p0, p1);
+          sv[e] = pack_bf16x2(p0, p1);
         }
         float a0, a1, a2, a3;
         f32x2_split(rs2[0], a0, a1);
@@ -440,95 +452,96 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::wait_st();
           m_ref = m_new;
-          tsum = exp_pass();
         }
+        tsum = exp_pass();  // the scores were reloaded over P: P again (for m_ref)
       }
       // the other slot may use the exp unit now (slot 1 of an odd tile count has
       // no tile k = n_slot[0] - 1 to hand the token to: it is simply not awaited)
       mbar_arrive(tok(1 - s));
-      tc::st32(t_s, pk);
-      tc::st32(t_s + 32, pk + 32);
+      tc::st32(t_s, sv);
+      tc::st32(t_s + 32, sv + 32);
       tc::wait_st();
       l += tsum;
       tc::fence_before_sync();
       mbar_arrive(p_full(s));
     }
     // ---- epilogue: combine the two slots per row, write the split partial ----
-    if (s == 1) {
-      if (ok && n_slot[1] > 0) {
-        const bool ready = wait_bar(o_final(1), 0, p.wait, abort_flag);
-        ok = __all_sync(0xffffffffu, ready);
-      }
-      red_m[row] = (ok && n_slot[1] > 0) ? m_ref : -INFINITY;
-      red_l[row] = (ok && n_slot[1] > 0) ? l : 0.f;
-      tc::fence_before_sync();
-      mbar_arrive(slot1_done);
-    } else {
-      if (ok) {
-        const bool ready = wait_bar(o_final(0), 0, p.wait, abort_flag) &&
-                           wait_bar(slot1_done, 0, p.wait, abort_flag);
-        ok = __all_sync(0xffffffffu, ready);
-      }
-      if (ok) {
-        tc::fence_after_sync();
-        const float m1 = red_m[row], l1 = red_l[row];
-        const float m0 = l > 0.f ? m_ref : -INFINITY;
-        const float mx = fmaxf(m0, m1);
-        const float w0 = l > 0.f ? fast_exp2(m0 - mx) : 0.f;
-        const float w1 = l1 > 0.f ? fast_exp2(m1 - mx) : 0.f;
-        const float L = w0 * l + w1 * l1;
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const float c0 = w0 * inv, c1 = w1 * inv;  // 0 for a slot with no visible key
-        const bool use1 = n_slot[1] > 0;            // warp-uniform
-        // rows past G * T_q belong to other heads' queries: computed, never stored
-        const size_t orow = (size_t)(b * p.H_q + kv * p.G) * p.T_q + row;
-        const size_t n_part_rows = (size_t)p.B * p.H_q * p.T_q * p.num_splits;
-        if (row < R && store_ok(orow * p.num_splits + split, n_part_rows, p.wait.status))
-          p.lse_part[orow * p.num_splits + split] =
-              L > 0.f ? mx * 0.69314718055994531f + logf(L) : -INFINITY;
-        // The combined rows go through shared memory so that the global stores
-        // are whole 512-byte rows: a thread holds one row, and storing it
-        // directly would make every warp store touch 32 rows.  The ring is idle
-        // here (both slots' last P V completed, so every copy has landed and
-        // every MMA that read a stage is done).  Each warp stages its 32 rows,
-        // 16-byte chunk ch of row i at chunk slot ch ^ i (conflict-free both ways).
-        uint8_t *stage = smem + kOffStage + wq * (32 * kD * 4);
+    // Both slots' warps share it: after their (m, l) are exchanged through shared
+    // memory, the warps of slot s combine and store columns [64 s, 64 s + 64) of
+    // their 32 rows (eight warps storing instead of four).
+    const bool has1 = n_slot[1] > 0;  // CTA-uniform: slot 1 holds a tile
+    const bool live = ok && (s == 0 || has1);
+    red_m[s * kRows + row] = live ? m_ref : -INFINITY;
+    red_l[s * kRows + row] = live ? l : 0.f;
+    ok = softmax_bar_and(ok);  // all 256 softmax threads; true only if every one is ok
+    if (ok) {
+      const bool ready = wait_bar(o_final(0), 0, p.wait, abort_flag) &&
+                         (!has1 || wait_bar(o_final(1), 0, p.wait, abort_flag));
+      ok = __all_sync(0xffffffffu, ready);
+    }
+    if (ok) {
+      tc::fence_after_sync();
+      const float m0 = red_m[row], l0 = red_l[row];
+      const float m1 = red_m[kRows + row], l1 = red_l[kRows + row];
+      const float mx = fmaxf(l0 > 0.f ? m0 : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
+      const float w0 = l0 > 0.f ? fast_exp2(m0 - mx) : 0.f;
+      const float w1 = l1 > 0.f ? fast_exp2(m1 - mx) : 0.f;
+      const float L = w0 * l0 + w1 * l1;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float c0 = w0 * inv, c1 = w1 * inv;  // 0 for a slot with no visible key
+      // rows past G * T_q belong to other heads' queries: computed, never stored
+      const size_t row0 = (size_t)(b * p.H_q + kv * p.G) * p.T_q;  // the group's first row
+      const size_t n_part_rows = (size_t)p.B * p.H_q * p.T_q * p.num_splits;
+      if (s == 0 && row < R && store_ok((row0 + row) * p.num_splits + split, n_part_rows,
+                                        p.wait.status))
+        p.lse_part[(row0 + row) * p.num_splits + split] =
+            L > 0.f ? mx * 0.69314718055994531f + logf(L) : -INFINITY;
+      // The combined rows go through shared memory so that the global stores are
+      // contiguous 256-byte row halves: a thread holds one row, and storing it
+      // directly would make every warp store touch 32 rows.  The ring is idle
+      // here (both slots' last P V completed, so every copy has landed and every
+      // MMA that read a stage is done).  Each warp stages its 32 rows x 64
+      // columns (8 KiB), 16-byte chunk ch of row i at chunk slot ch ^ (i & 7)
+      // (conflict-free both ways).
+      uint8_t *stage = smem + kOffStage + (4 * s + wq) * (32 * 64 * 4);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r0[32], r1[32];
-          tc::ld32(t_o + 32 * c, r0);
-          if (use1) tc::ld32(t_o + 128u + 32 * c, r1);
-          tc::wait_ld32(r0);         // waits for both loads; ties r0's registers to it
-          if (use1) tc::wait_ld32(r1);  // (already complete) ties r1's
-          // both slots' O are finite (every slot with a tile wrote its O, and V
-          // rows past the sequence were cleared); a slot with no tile is skipped
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * s + cc;  // 32-column chunk of O
+        uint32_t r0[32], r1[32];
+        tc::ld32(t_o - 128u * s + 32 * c, r0);          // slot 0's O
+        if (has1) tc::ld32(t_o - 128u * s + 128u + 32 * c, r1);  // slot 1's O
+        tc::wait_ld32(r0);            // waits for both loads; ties r0's registers to it
+        if (has1) tc::wait_ld32(r1);  // (already complete) ties r1's
+        // both slots' O are finite (every slot with a tile wrote its O, and V
+        // rows past the sequence were cleared); a slot with no tile is skipped
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float4 v;
-            v.x = c0 * __uint_as_float(r0[4 * e + 0]);
-            v.y = c0 * __uint_as_float(r0[4 * e + 1]);
-            v.z = c0 * __uint_as_float(r0[4 * e + 2]);
-            v.w = c0 * __uint_as_float(r0[4 * e + 3]);
-            if (use1) {
-              v.x = fmaf(c1, __uint_as_float(r1[4 * e + 0]), v.x);
-              v.y = fmaf(c1, __uint_as_float(r1[4 * e + 1]), v.y);
-              v.z = fmaf(c1, __uint_as_float(r1[4 * e + 2]), v.z);
-              v.w = fmaf(c1, __uint_as_float(r1[4 * e + 3]), v.w);
-            }
-            *reinterpret_cast<float4 *>(stage + lane * (kD * 4) + (((8 * c + e) ^ lane) & 31) * 16) =
-                v;
+        for (int e = 0; e < 8; ++e) {
+          float4 v;
+          v.x = c0 * __uint_as_float(r0[4 * e + 0]);
+          v.y = c0 * __uint_as_float(r0[4 * e + 1]);
+          v.z = c0 * __uint_as_float(r0[4 * e + 2]);
+          v.w = c0 * __uint_as_float(r0[4 * e + 3]);
+          if (has1) {
+            v.x = fmaf(c1, __uint_as_float(r1[4 * e + 0]), v.x);
+            v.y = fmaf(c1, __uint_as_float(r1[4 * e + 1]), v.y);
+            v.z = fmaf(c1, __uint_as_float(r1[4 * e + 2]), v.z);
+            v.w = fmaf(c1, __uint_as_float(r1[4 * e + 3]), v.w);
           }
+          const int ch = 8 * cc + e;  // 16-byte chunk of the warp's 64 columns
+          *reinterpret_cast<float4 *>(stage + lane * 256 + ((ch ^ (lane & 7)) * 16)) = v;
         }
-        __syncwarp();
-        // row i of the warp: lane l stores its 16-byte chunk l
+      }
+      __syncwarp();
+      // two rows per step: lanes 0-15 store row 2 it, lanes 16-31 row 2 it + 1,
+      // lane l its 16-byte chunk l % 16 of the row's 256-byte half
 #pragma unroll 4
-        for (int i = 0; i < 32; ++i) {
-          const int r = 32 * wq + i;
-          const size_t prow = ((size_t)(b * p.H_q + kv * p.G) * p.T_q + r) * p.num_splits + split;
-          if (r < R && store_ok(prow, n_part_rows, p.wait.status))
-            reinterpret_cast<float4 *>(p.o_part + prow * kD)[lane] =
-                *reinterpret_cast<const float4 *>(stage + i * (kD * 4) + ((lane ^ i) & 31) * 16);
-        }
+      for (int it = 0; it < 16; ++it) {
+        const int i = 2 * it + (lane >> 4), k = lane & 15;
+        const int r = 32 * wq + i;
+        const size_t prow = (row0 + r) * p.num_splits + split;
+        if (r < R && store_ok(prow, n_part_rows, p.wait.status))
+          reinterpret_cast<float4 *>(p.o_part + prow * kD + 64 * s)[k] =
+              *reinterpret_cast<const float4 *>(stage + i * 256 + ((k ^ (i & 7)) * 16));
       }
     }
   }
