@@ -554,10 +554,13 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ float red_m[kMergeGroups];
   // the next kernel (typically the next layer's split) may start its prologue
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int h = blockIdx.x, b = blockIdx.y;  // h: (query head, new token) row of sequence b
   const int t = threadIdx.x, grp = t >> 5, lane = t & 31;
+  // The lengths are read ahead of the dependency wait: the merge takes the
+  // lengths its split phase took, which the grids before that phase wrote (the
+  // split kernel itself never writes them), so they are already visible here.
   const int seqlen = min(max(__ldcg(seqlens + b), 0), S_max);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the splits that hold keys of this row: the chunk the split kernel derived
   // from the same lengths
   const int dchunk = device_chunk(seqlen, gridDim.y, S_max, chunk, num_splits, H_kv, num_sms, tile);

@@ -202,6 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // inputs written by earlier grids are visible after this wait (coherent loads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the row block of Q does not depend on the sequence length: its copy starts
+  // before the length is read
+  const uint64_t pol = l2_policy_evict_first();
+  if (warp == kWarpTma && lane == 0) {
+    const int q_row0 = (b * p.H_q + kv * p.G) * p.T_q;  // first (head, token) row of the group
+    mbar_arrive_expect_tx(q_full, kTileBytes);
+    for (int half = 0; half < 2; ++half)
+      tma_load_4d(sbase + kOffQ + half * kHalfBytes, &tm_q, q_full, 0, half, q_row0, 0, pol);
+  }
   const int seqlen_in = __ldca(p.seqlens + b);
   const int seqlen = min(max(seqlen_in, 0), p.S_max);
   // the chunk for the batch's actual lengths (the host's chunk when they are S_max)
@@ -213,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int key_begin = split * chunk;
   const int key_end = min(key_begin + chunk, seqlen);
   if (key_begin >= key_end) {  // empty split: the merge never reads it (CTA-uniform)
+    // no copy may still be in flight when the CTA exits
+    if (warp == kWarpTma && lane == 0) wait_bar(q_full, 0, p.wait, abort_flag);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == kWarpMma) {
@@ -235,13 +246,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128-key tile never straddles pages: page sizes are multiples of 128).
     int ld = 0;
     bool ok = true;
-    const uint64_t pol = l2_policy_evict_first();
-    if (lane == 0) {
-      const int q_row0 = (b * p.H_q + kv * p.G) * p.T_q;  // first (head, token) row of the group
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      for (int half = 0; half < 2; ++half)
-        tma_load_4d(sbase + kOffQ + half * kHalfBytes, &tm_q, q_full, 0, half, q_row0, 0, pol);
-    }
     int page_base = -(1 << 30), page_reg = 0;
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int key0 = key_begin + j * kBN;

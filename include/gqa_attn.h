@@ -263,7 +263,9 @@ GQA_API int gqa_attn_decode_kernel_count(int B, int H_q, int H_kv, int S_max, in
  * leaves the per-split partials in `workspace`; gqa_attn_decode_merge reads
  * them and writes o and lse.  Calling split then merge on one stream is
  * the result of gqa_attn_decode (bit for bit when gqa_attn_decode also runs
- * split + merge); between the two the workspace must not be touched.
+ * split + merge); between the two the workspace must not be touched, and
+ * seqlens must hold the lengths the split call read (the merge kernel may read
+ * them before a kernel launched between the two calls has finished).
  * split needs q, k_cache, v_cache, seqlens; merge needs seqlens, o, lse (the
  * other pointers may be NULL for the phase that does not use them).
  */
