@@ -26,7 +26,9 @@ Conventions taken from the record:
   * Causal prefill: query row i sits at absolute position q_offset + i and
     sees keys 0..q_offset+i inclusive; keys after it are masked (section 5.4
     "PREFILL, no SP": all-past tiles unmasked, all-future tiles skipped,
-    boundary tiles masked).
+    boundary tiles masked).  A row at or past the last key sees every key:
+    the steps of section 5.5's ring where a KV block lies wholly before the
+    query block attend to the whole block.
   * An empty visible set gives O = 0 and lse = -inf (the record is silent;
     this is the reading the merge needs so that an empty split is the
     identity of the log-sum-exp merge).
@@ -158,25 +160,26 @@ def prefill_causal(q, k, v, q_offset, scale, row_block: int = 512):
     """Causal prefill for every (b, h_q, i).
 
     q [B, H_q, T_q, d]; k, v [B, H_kv, S_kv, d].  Row i is at absolute
-    position q_offset + i and sees keys 0..q_offset+i.  Rows are processed
-    in blocks of `row_block` only to bound memory; each row is independent.
+    position q_offset + i and sees keys 0..min(q_offset+i, S_kv-1) (rows at or
+    past the last key see every key).  Rows are processed in blocks of
+    `row_block` only to bound memory; each row is independent.
     Returns O [B, H_q, T_q, d] and lse [B, H_q, T_q] in float64.
     """
     B, H_q, T_q, d = q.shape
     H_kv, S_kv = k.shape[1], k.shape[2]
     G = _group_size(H_q, H_kv)
-    if q_offset < 0 or q_offset + T_q > S_kv:
-        raise ValueError("need 0 <= q_offset and q_offset + T_q <= S_kv")
+    if q_offset < 0 or (T_q > 0 and S_kv == 0):
+        raise ValueError("need 0 <= q_offset and, with queries, at least one key")
     o = np.zeros((B, H_q, T_q, d))
     lse = np.zeros((B, H_q, T_q))
     for b in range(B):
         for kv in range(H_kv):
             for r0 in range(0, T_q, row_block):
                 r1 = min(T_q, r0 + row_block)
-                n_keys = q_offset + r1            # keys the last row of the block sees
+                n_keys = min(q_offset + r1, S_kv)  # keys the last row of the block sees
                 kb = _f64(k[b, kv, :n_keys])
                 vb = _f64(v[b, kv, :n_keys])
-                n_visible = q_offset + np.arange(r0, r1) + 1
+                n_visible = np.minimum(q_offset + np.arange(r0, r1) + 1, S_kv)
                 for h in range(kv * G, (kv + 1) * G):
                     o[b, h, r0:r1], lse[b, h, r0:r1] = attend_rows(
                         _f64(q[b, h, r0:r1]), kb, vb, scale, n_visible)
@@ -190,7 +193,7 @@ def prefill_causal_rows(q, k, v, q_offset, scale, picks):
     o = np.zeros((len(picks), d))
     lse = np.zeros(len(picks))
     for r, (b, h, i) in enumerate(picks):
-        n = q_offset + int(i) + 1
+        n = min(q_offset + int(i) + 1, k.shape[2])
         kb = _f64(k[b, h // G, :n])
         vb = _f64(v[b, h // G, :n])
         o[r:r + 1], lse[r:r + 1] = attend_rows(_f64(q[b, h, i])[None, :], kb, vb, scale, [n])

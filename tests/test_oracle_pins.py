@@ -158,6 +158,59 @@ def test_prefill_matches_torch_sdpa_gqa(q_offset, T_q, S_kv):
     np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("q_offset,T_q,S_kv", [(3, 4, 5), (5, 3, 5), (9, 2, 4)])
+def test_prefill_rows_past_the_keys_match_brute_force(q_offset, T_q, S_kv):
+    """Rows at or past the last key see every key (the ring's whole-past blocks)."""
+    B, H_q, H_kv, d = 2, 4, 2, 4
+    q, k, v = rng_inputs(30 + q_offset, (B, H_q, T_q, d), (B, H_kv, S_kv, d), (B, H_kv, S_kv, d))
+    o, lse = oracle.prefill_causal(q, k, v, q_offset, 0.53)
+    bo, blse = brute_prefill(q, k, v, q_offset, 0.53)
+    np.testing.assert_allclose(o, bo, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, blse, rtol=0, atol=1e-12)
+
+
+def test_rows_wholly_past_the_keys_equal_unmasked_attention():
+    """q_offset >= S_kv - 1: every row sees the whole block, i.e. plain (unmasked)
+    attention -- torch SDPA without a mask, KV heads repeated."""
+    B, H_q, H_kv, T_q, S_kv, d = 2, 8, 2, 6, 9, 16
+    q, k, v = rng_inputs(41, (B, H_q, T_q, d), (B, H_kv, S_kv, d), (B, H_kv, S_kv, d))
+    o, _ = oracle.prefill_causal(q, k, v, S_kv + 3, 0.2, row_block=4)
+    qt, kt, vt = (torch.from_numpy(x) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt.repeat_interleave(4, dim=1), vt.repeat_interleave(4, dim=1), scale=0.2).numpy()
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+    o2, _ = oracle.prefill_causal(q, k, v, S_kv - 1, 0.2)     # the last key is row 0's own
+    np.testing.assert_allclose(o2, ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("n_ranks", [2, 3, 4])
+def test_ring_steps_merge_to_the_causal_prefill(n_ranks):
+    """The record's section 5.5 ring: a causal prefill whose sequence is cut into
+    n chunks equals, for query chunk r, the log-sum-exp merge over the KV chunks
+    src <= r of attention over chunk src -- causal on the diagonal (src = r),
+    unmasked for whole-past chunks (src < r) -- with whole-future chunks skipped."""
+    B, H_q, H_kv, C, d = 1, 4, 2, 5, 8
+    S = n_ranks * C
+    q, k, v = rng_inputs(50 + n_ranks, (B, H_q, S, d), (B, H_kv, S, d), (B, H_kv, S, d))
+    o_ref, lse_ref = oracle.prefill_causal(q, k, v, 0, 0.3)
+    for r in range(n_ranks):
+        qc = q[:, :, r * C:(r + 1) * C]
+        parts_o, parts_l = [], []
+        for src in range(n_ranks):
+            if src > r:
+                continue                                      # whole-future block: skipped
+            kc, vc = k[:, :, src * C:(src + 1) * C], v[:, :, src * C:(src + 1) * C]
+            po, pl = oracle.prefill_causal(qc, kc, vc, (r - src) * C, 0.3)
+            parts_o.append(po)
+            parts_l.append(pl)
+        o, lse = oracle.merge_states(np.stack(parts_o).reshape(len(parts_o), -1, d),
+                                     np.stack(parts_l).reshape(len(parts_l), -1))
+        np.testing.assert_allclose(o.reshape(B, H_q, C, d), o_ref[:, :, r * C:(r + 1) * C],
+                                   rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse.reshape(B, H_q, C), lse_ref[:, :, r * C:(r + 1) * C],
+                                   rtol=0, atol=1e-12)
+
+
 def test_decode_matches_torch_sdpa_gqa():
     B, H_q, H_kv, S, d = 2, 8, 2, 40, 16
     q, k, v = rng_inputs(30, (B, H_q, d), (B, H_kv, S, d), (B, H_kv, S, d))
