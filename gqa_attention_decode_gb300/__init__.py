@@ -50,4 +50,7 @@ from .sequence_parallel import (  # noqa: F401
     block_seqlens,
     decode_sequence_parallel,
     gather_states,
+    ring_pass,
+    ring_prefill_causal,
+    ring_schedule,
 )

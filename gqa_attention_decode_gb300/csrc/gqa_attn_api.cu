@@ -200,7 +200,8 @@ int check_prefill_args(const void *q, const void *k, const void *v, int B, int H
   if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0)
     return GQA_ERR_INVALID_ARG;
   if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
-  if ((long long)q_offset + T_q > S_kv) return GQA_ERR_INVALID_ARG;
+  // rows past the last key see every key; a prefill with queries needs keys
+  if (T_q > 0 && S_kv == 0) return GQA_ERR_INVALID_ARG;
   if (!finite_scale(scale)) return GQA_ERR_INVALID_ARG;
   if (B == 0 || T_q == 0) return GQA_OK;
   if (!q || !k || !v || !o || !lse) return GQA_ERR_INVALID_ARG;
@@ -492,7 +493,7 @@ GQA_API size_t gqa_attn_prefill_causal_workspace_size(int B, int H_q, int H_kv, 
                                                       int S_kv, int d, int q_offset,
                                                       int num_sms) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0 ||
-      num_sms <= 0 || H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
+      num_sms <= 0 || H_q % H_kv != 0 || (T_q > 0 && S_kv == 0))
     return 0;
   const int G = H_q / H_kv;
   // the CTA-pair kernel's units (G % 4 == 0), else the single-CTA kernel's
@@ -510,7 +511,7 @@ GQA_API int gqa_attn_prefill_causal_plan(int B, int H_q, int H_kv, int T_q, int 
                                          int *out_pieces_per_unit) {
   if (!out_units || !out_split_units || !out_pieces_per_unit) return GQA_ERR_INVALID_ARG;
   if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0 ||
-      num_sms < 2 || H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
+      num_sms < 2 || H_q % H_kv != 0 || (T_q > 0 && S_kv == 0))
     return GQA_ERR_INVALID_ARG;
   *out_units = *out_split_units = 0;
   *out_pieces_per_unit = 1;
@@ -600,7 +601,7 @@ GQA_API int gqa_attn_prefill_causal_kernel_count(int B, int H_q, int H_kv, int T
                                                  int *out_kernels) {
   if (!out_kernels) return GQA_ERR_INVALID_ARG;
   if (B < 0 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 0 || d <= 0 || q_offset < 0 ||
-      H_q % H_kv != 0 || (long long)q_offset + T_q > S_kv)
+      H_q % H_kv != 0 || (T_q > 0 && S_kv == 0))
     return GQA_ERR_INVALID_ARG;
   if (B == 0 || T_q == 0) {
     *out_kernels = 0;

@@ -139,7 +139,9 @@ __device__ __forceinline__ Unit unit_at(const Params &p, int item) {
     w.qt1 = w.second_valid ? w.qt0 - 1 : w.qt0;
   }
   const int qe = min((w.qt0 + 1) * kBM, p.T_q);
-  w.n_kv = (p.q_offset + qe - 1) / kBN + 1;
+  // key tiles up to the one of the tile's last query row (rows past the last key
+  // see every key: no tile past the keys)
+  w.n_kv = min((p.q_offset + qe - 1) / kBN + 1, (p.S_kv + kBN - 1) / kBN);
   w.kv_lo = 0;
   w.kv_hi = w.n_kv;
   if (w.piece >= 0) {
@@ -637,7 +639,9 @@ long long prefill_units(int B, int H_q, int H_kv, int T_q) {
 PrefillPlan prefill_plan(const PrefillLaunch &a) {
   using namespace prefill;
   const long long units = prefill_units(a.B, a.H_q, a.H_kv, a.T_q);
-  const int n_kv_min = (a.q_offset + (a.T_q < kBM ? a.T_q : kBM) - 1) / kBN + 1;
+  const int n_kv_first = (a.q_offset + (a.T_q < kBM ? a.T_q : kBM) - 1) / kBN + 1;
+  const int n_kv_all = (a.S_kv + kBN - 1) / kBN;
+  const int n_kv_min = n_kv_first < n_kv_all ? n_kv_first : n_kv_all;
   return prefill_split::make_plan(units, a.num_sms, n_kv_min, 2, a.ws, a.ws_bytes);
 }
 

@@ -113,7 +113,9 @@ __device__ __forceinline__ Unit unit_at(const Params &p, int item) {
   w.kv = r % p.H_kv;
   w.b = r / p.H_kv;
   const int qe = min((w.qt + 1) * kBM, p.T_q);
-  w.n_kv = (p.q_offset + qe - 1) / kBN + 1;
+  // key tiles up to the one of the tile's last query row (rows past the last key
+  // see every key: no tile past the keys)
+  w.n_kv = min((p.q_offset + qe - 1) / kBN + 1, (p.S_kv + kBN - 1) / kBN);
   w.kv_lo = 0;
   w.kv_hi = w.n_kv;
   if (w.piece >= 0) {
@@ -664,7 +666,9 @@ PrefillPlan prefill_pair_plan(const PrefillLaunch &a) {
   const int G = a.H_q / a.H_kv;
   const int n_qtiles = (a.T_q + kBM - 1) / kBM;
   const long long units = (long long)n_qtiles * a.B * a.H_kv * (G / 4);
-  const int n_kv_min = (a.q_offset + (a.T_q < kBM ? a.T_q : kBM) - 1) / kBN + 1;
+  const int n_kv_first = (a.q_offset + (a.T_q < kBM ? a.T_q : kBM) - 1) / kBN + 1;
+  const int n_kv_all = (a.S_kv + kBN - 1) / kBN;
+  const int n_kv_min = n_kv_first < n_kv_all ? n_kv_first : n_kv_all;
   return prefill_split::make_plan(units, a.max_pairs, n_kv_min, 4, a.ws, a.ws_bytes);
 }
 

@@ -321,10 +321,12 @@ GQA_API int gqa_attn_decode_noalloc(const gqa_bf16_t *q, const gqa_bf16_t *k_cac
  *   q        device [B, H_q, T_q, d] bf16; row i is the query at absolute
  *            position q_offset + i.
  *   k, v     device [B, H_kv, S_kv, d] bf16; read only.
- *   q_offset 0 <= q_offset and q_offset + T_q <= S_kv.  Row i sees keys
- *            0..q_offset+i (the diagonal included); q_offset = 0 with
- *            T_q = S_kv is the square causal mask, q_offset = S_kv - T_q is the
- *            last chunk of a chunked prefill.
+ *   q_offset 0 <= q_offset.  Row i sees keys 0..min(q_offset+i, S_kv-1) (the
+ *            diagonal included); q_offset = 0 with T_q = S_kv is the square
+ *            causal mask, q_offset = S_kv - T_q is the last chunk of a chunked
+ *            prefill, and rows at or past the last key (q_offset + i >= S_kv - 1)
+ *            see every key -- a KV block wholly before the query block, as in
+ *            the ring steps of section 5.5.  S_kv >= 1 when T_q > 0.
  *   scale    softmax scale.
  *   o        device [B, H_q, T_q, d] bf16 output.
  *   lse      device [B, H_q, T_q] fp32 output.
@@ -539,9 +541,9 @@ GQA_API int gqa_attn_selftest_bounds(gqa_stream_t stream);
  * *out_count and resets it to 0 (a device-wide counter: concurrent prefill
  * calls on other streams add to it).  Release builds return GQA_ERR_UNSUPPORTED.
  * Expected values: query tile t of a head (rows [128t, min(128t + 128, T_q)))
- * sees key tiles 0 .. (q_offset + min(128t + 128, T_q) - 1) / 128, and the sum of
- * those counts over every (sequence, query head, query tile) is the causal
- * count.  One known excess: for odd group sizes the group's last head runs query
+ * sees key tiles 0 .. min((q_offset + min(128t + 128, T_q) - 1) / 128,
+ * (S_kv - 1) / 128), and the sum of those counts over every (sequence, query
+ * head, query tile) is the causal count.  One known excess: for odd group sizes the group's last head runs query
  * tiles t and t - 1 in one unit over tile t's key range (one more key tile for
  * tile t - 1, wholly in its future and masked), and a lone tile 0 in such a unit
  * is paired with a discarded copy of itself.

@@ -229,7 +229,9 @@ def test_prefill_workspace_size(lib):
                                                       152) == 128 * PIECE_BYTES_1
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 6, 2, 2048, 32768, 128, 30720,
                                                       152) == 152 * PIECE_BYTES_1
-    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 100, 128, 0, 152) == 0
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 0, 128, 0, 152) == 0
+    # rows past the last key are valid: 8 units on 76 pairs, each cut by key range
+    assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 100, 128, 0, 152) > 0
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 256, 128, 0, 0) == 0
 
 
@@ -283,8 +285,9 @@ def _raw_prefill(lib, **kw):
 @pytest.mark.parametrize("kw,expect", [
     (dict(v=0), gqa.GQA_ERR_INVALID_ARG),
     (dict(o=(1 << 20) + 8), gqa.GQA_ERR_INVALID_ARG),
-    (dict(q_offset=200), gqa.GQA_ERR_INVALID_ARG),             # q_offset + T_q > S_kv
     (dict(q_offset=-1), gqa.GQA_ERR_INVALID_ARG),
+    (dict(S_kv=0), gqa.GQA_ERR_INVALID_ARG),                   # queries but no key
+    (dict(S_kv=0, T_q=0), gqa.GQA_OK),
     (dict(H_kv=7), gqa.GQA_ERR_INVALID_ARG),
     (dict(d=96), gqa.GQA_ERR_UNSUPPORTED),
     (dict(T_q=0), gqa.GQA_OK),

@@ -251,13 +251,31 @@ def test_host_buffer_variant_matches_device_call():
 def test_rejects_bad_q_offset_and_misalignment():
     q, k, v = gqa_synth.prefill_inputs(1, 8, 1, 64, 64, 128, seed=36, device=DEV)
     with pytest.raises(gqa.GQAError) as e:
-        gqa.gqa_attn_prefill_causal(q, k, v, 0.1, q_offset=1)   # q_offset + T_q > S_kv
+        gqa.gqa_attn_prefill_causal(q, k, v, 0.1, q_offset=-1)
     assert e.value.status == gqa.GQA_ERR_INVALID_ARG
     flat = torch.empty(k.numel() + 8, dtype=torch.bfloat16, device=DEV)
     k_off = flat[4:4 + k.numel()].view(k.shape)                # 8-byte offset
     with pytest.raises(gqa.GQAError) as e:
         gqa.gqa_attn_prefill_causal(q, k_off, v, 0.1)
     assert e.value.status == gqa.GQA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,T_q,S_kv,q_offset", [
+    (1, 16, 2, 300, 256, 256),     # every row past the keys: unmasked (G = 8, CTA pairs)
+    (1, 16, 2, 300, 256, 100),     # rows 0..155 causal, the rest see every key
+    (2, 6, 2, 200, 130, 1000),     # G = 3 (one CTA per unit), a ragged key tile
+    (1, 4, 4, 129, 385, 300),      # MHA, the boundary inside a query tile
+    (1, 64, 8, 512, 1024, 4096),   # a ring step's whole-past block (Llama3-70B heads)
+    (1, 32, 8, 256, 4096, 3968),   # G = 4, one query tile straddling the last key
+])
+def test_rows_past_the_last_key(B, H_q, H_kv, T_q, S_kv, q_offset):
+    """Rows at or past the last key see every key (q_offset + T_q > S_kv): the
+    whole-past blocks of a ring prefill, through the causal prefill call."""
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=44, device=DEV)
+    o, lse = run(q, k, v, q_offset, 1 / math.sqrt(128))
+    o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), q_offset,
+                                           1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, f"past the keys {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
 
 
 def test_chunk_after_128k_keys_full():

@@ -80,40 +80,42 @@ SCRIPT = textwrap.dedent("""
     # sizes, the known extra of the group's last head, which runs query tiles t
     # and t - 1 together over tile t's key range (a lone tile 0 with a discarded
     # copy of itself).
-    def n_kv(t, T_q, q_offset):
-        return (q_offset + min(128 * t + 128, T_q) - 1) // 128 + 1
+    def n_kv(t, T_q, q_offset, S):
+        return min((q_offset + min(128 * t + 128, T_q) - 1) // 128 + 1, -(-S // 128))
 
-    def causal_s_tiles(B, H_q, T_q, q_offset):
-        return B * H_q * sum(n_kv(t, T_q, q_offset) for t in range(-(-T_q // 128)))
+    def causal_s_tiles(B, H_q, T_q, q_offset, S):
+        return B * H_q * sum(n_kv(t, T_q, q_offset, S) for t in range(-(-T_q // 128)))
 
-    def issued_s_tiles(B, H_q, H_kv, T_q, q_offset):
+    def issued_s_tiles(B, H_q, H_kv, T_q, q_offset, S):
         G, n_qt = H_q // H_kv, -(-T_q // 128)
         extra = 0
         if G % 2 == 1:
             for r in range(0, n_qt, 2):
                 t0 = n_qt - 1 - r
-                extra += (n_kv(t0, T_q, q_offset) - n_kv(t0 - 1, T_q, q_offset) if t0 > 0
-                          else n_kv(0, T_q, q_offset))
-        return causal_s_tiles(B, H_q, T_q, q_offset) + B * H_kv * extra
+                extra += (n_kv(t0, T_q, q_offset, S) - n_kv(t0 - 1, T_q, q_offset, S) if t0 > 0
+                          else n_kv(0, T_q, q_offset, S))
+        return causal_s_tiles(B, H_q, T_q, q_offset, S) + B * H_kv * extra
 
     gqa.gqa_attn_debug_s_tile_count()          # start from zero
     # prefill: CTA pairs (G = 8, 4) and one CTA per unit (G = 3, 1, 2), whole and split
-    for (B, H_q, H_kv, T, S) in [(1, 16, 2, 300, 300), (1, 8, 2, 128, 4096), (1, 6, 2, 200, 200),
-                                 (1, 6, 2, 128, 4096), (1, 4, 4, 256, 2304),
-                                 (1, 16, 2, 200, 3000), (2, 16, 2, 1024, 1024),
-                                 (1, 8, 4, 1000, 1000), (1, 3, 3, 640, 700),
-                                 (1, 64, 8, 2048, 2048), (1, 64, 8, 512, 8192)]:
-        qo = S - T
+    # (the last cases put rows past the last key: every key tile, none beyond)
+    for (B, H_q, H_kv, T, S, qo) in [(1, 16, 2, 300, 300, 0), (1, 8, 2, 128, 4096, 3968),
+                                     (1, 6, 2, 200, 200, 0), (1, 6, 2, 128, 4096, 3968),
+                                     (1, 4, 4, 256, 2304, 2048), (1, 16, 2, 200, 3000, 2800),
+                                     (2, 16, 2, 1024, 1024, 0), (1, 8, 4, 1000, 1000, 0),
+                                     (1, 3, 3, 640, 700, 60), (1, 64, 8, 2048, 2048, 0),
+                                     (1, 64, 8, 512, 8192, 7680), (1, 16, 2, 300, 256, 100),
+                                     (1, 6, 2, 400, 300, 1000), (1, 64, 8, 256, 1024, 4096)]:
         q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T, S, 128, seed=3, device=dev)
         o, lse = gqa.gqa_attn_prefill_causal(q, k, v, 0.088, qo)
         torch.cuda.synchronize()
         ok(("prefill", B, H_q, H_kv, T, S))
         got = gqa.gqa_attn_debug_s_tile_count()
-        want = issued_s_tiles(B, H_q, H_kv, T, qo)
+        want = issued_s_tiles(B, H_q, H_kv, T, qo, S)
         assert got == want, ("S tile count", B, H_q, H_kv, T, S, got, want)
         if (H_q // H_kv) % 2 == 0:   # no odd-group extra: exactly the lower triangle
-            assert got == causal_s_tiles(B, H_q, T, qo)
-        print("S tiles", (B, H_q, H_kv, T, S), got, "causal", causal_s_tiles(B, H_q, T, qo),
+            assert got == causal_s_tiles(B, H_q, T, qo, S)
+        print("S tiles", (B, H_q, H_kv, T, S), got, "causal", causal_s_tiles(B, H_q, T, qo, S),
               "square", B * H_q * (-(-T // 128)) * (-(-S // 128)))
         o_ref, l_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), qo, 0.088)
         compare(o, lse, o_ref, l_ref, "debug prefill")
