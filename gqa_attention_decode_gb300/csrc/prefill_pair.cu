@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           return sum;
         };
-        // common path: the whole row in registers (one load wait), before the exp turn
+        // common path: the whole row in registers (one load wait)
         uint32_t sv[kBN];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tc::ld32(t_s + 32 * c, sv + 32 * c);
