@@ -57,12 +57,20 @@ template <>
 struct PageArgs<false> {};
 
 using Plan = PrefillPlan;
+constexpr int kMaxPieceRounds = 4;     // pieces never exceed this many rounds of workers
+constexpr int kPieceOverheadTiles = 2;  // a piece's start and partial store, in key tiles
+
 // `units` units on `workers` resident workers; `n_kv_min` key tiles of the
 // shortest unit; a workspace of `ws_bytes` (none if `ws` is null).  The
 // r = units mod workers units of the last round (all of them when there are
-// fewer units than workers) are each cut into min(workers / r, kMaxPieces,
-// n_kv_min / kMinPieceTiles) pieces, if that is at least 2 and the pieces' partials
-// fit the workspace.
+// fewer units than workers) may each be cut into s pieces of contiguous key
+// tiles, dealt after the whole units like any other item, so the pieces of the
+// last round can take several rounds of their own.  The s chosen minimises the
+// modelled span of those rounds, ceil(r s / workers) * (n_kv_min / s +
+// kPieceOverheadTiles + 1), against n_kv_min for the units run whole; at most
+// kMaxPieces pieces per unit, at least kMinPieceTiles tiles each, at most
+// kMaxPieceRounds rounds of pieces, and only pieces whose partials fit the
+// workspace.
 inline Plan make_plan(long long units, int workers, int n_kv_min, int heads, const void *ws,
                       size_t ws_bytes) {
   Plan pl;
@@ -72,12 +80,24 @@ inline Plan make_plan(long long units, int workers, int n_kv_min, int heads, con
   pl.n_full = U;
   const int r = U % workers;
   if (ws != nullptr && r > 0) {
-    int sp = workers / r;
-    if (sp > kMaxPieces) sp = kMaxPieces;
-    if (sp > n_kv_min / kMinPieceTiles) sp = n_kv_min / kMinPieceTiles;
-    if (sp >= 2 && (size_t)r * sp * piece_bytes(heads) <= ws_bytes) {
+    int s_max = n_kv_min / kMinPieceTiles;
+    if (s_max > kMaxPieces) s_max = kMaxPieces;
+    double best = (double)n_kv_min;  // the last round's units run whole
+    int best_s = 1;
+    for (int sp = 2; sp <= s_max; ++sp) {
+      const long long pieces = (long long)r * sp;
+      const long long rounds = (pieces + workers - 1) / workers;
+      if (rounds > kMaxPieceRounds || (size_t)pieces * piece_bytes(heads) > ws_bytes) break;
+      const double span =
+          (double)rounds * ((double)n_kv_min / sp + kPieceOverheadTiles + 1);
+      if (span < best) {
+        best = span;
+        best_s = sp;
+      }
+    }
+    if (best_s >= 2) {
       pl.n_full = U - r;
-      pl.split_s = sp;
+      pl.split_s = best_s;
     }
   }
   pl.pieces = (U - pl.n_full) * pl.split_s;
@@ -86,11 +106,13 @@ inline Plan make_plan(long long units, int workers, int n_kv_min, int heads, con
   return pl;
 }
 
-// Workspace that lets any partial round split: never more pieces than workers,
-// nor than kMaxPieces per unit.
+// Workspace that lets any partial round split as far as make_plan may cut it:
+// at most kMaxPieceRounds rounds of workers, nor more than kMaxPieces pieces
+// per unit.
 inline size_t workspace_bound(long long units, int workers, int heads) {
   const long long most = units * kMaxPieces;
-  const long long pieces = most < workers ? most : workers;
+  const long long cap = (long long)workers * kMaxPieceRounds;
+  const long long pieces = most < cap ? most : cap;
   return pieces > 0 ? (size_t)pieces * piece_bytes(heads) : 0;
 }
 

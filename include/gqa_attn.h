@@ -344,14 +344,16 @@ GQA_API int gqa_attn_prefill_causal(const gqa_bf16_t *q, const gqa_bf16_t *k,
  * query rows of four heads of a KV group on a CTA pair when G is a multiple of
  * 4, else of two 128-row slots on one CTA) over the device's resident workers;
  * when the last round is partial -- or there are fewer units than workers, as
- * for a short chunk after a long prefix -- its units are cut into pieces of
- * contiguous key tiles (at least 8 tiles each, at most 32 per unit and one per
- * worker), each piece's partial softmax state (O before division, m, l) goes to
- * the workspace and a log-sum-exp merge kernel combines them: the record's
- * split-and-reduce (sections 2.2 and 4) applied to prefill.  The bound is one
- * piece per worker: min(32 * units, num_sms / 2) * 266240 bytes (CTA pairs)
- * or min(32 * units, num_sms) * 133120 bytes (single CTAs), rounded up to 256.
- * Returns 0 for invalid arguments.
+ * for a short chunk after a long prefix -- its units may be cut into pieces of
+ * contiguous key tiles (at least 8 tiles each, at most 32 per unit, at most
+ * four rounds of pieces over the workers; the count chosen to shorten those
+ * rounds most), each piece's partial softmax state (O before division, m, l)
+ * goes to the workspace and a log-sum-exp merge kernel combines them: the
+ * record's split-and-reduce (sections 2.2 and 4) applied to prefill.  The
+ * bound is four pieces per worker: min(32 * units, 4 * (num_sms / 2)) *
+ * 266240 bytes (CTA pairs) or min(32 * units, 4 * num_sms) * 133120 bytes
+ * (single CTAs), rounded up to 256; with less workspace the plan takes fewer
+ * pieces (or none).  Returns 0 for invalid arguments.
  */
 GQA_API size_t gqa_attn_prefill_causal_workspace_size(int B, int H_q, int H_kv, int T_q,
                                                       int S_kv, int d, int q_offset,

@@ -156,13 +156,33 @@ PIECE_BYTES = 4 * 128 * 130 * 4   # per piece, CTA pairs: 4 heads x 128 rows x (
 PIECE_BYTES_1 = 2 * 128 * 130 * 4  # per piece, one CTA: 2 slots x 128 rows
 
 
+def _split_rule(units, workers, n_kv_min, piece_bytes, ws_bytes):
+    """The planner's choice restated: the r = units % workers units of the last
+    round are cut into the s pieces (2..min(32, n_kv_min // 8)) that minimise
+    ceil(r s / workers) * (n_kv_min / s + 3), at most 4 rounds of pieces and
+    within the workspace, if that beats n_kv_min (the units run whole)."""
+    r = units % workers
+    best, best_s = float(n_kv_min), 1
+    if r:
+        for s in range(2, min(32, n_kv_min // 8) + 1):
+            pieces = r * s
+            rounds = -(-pieces // workers)
+            if rounds > 4 or pieces * piece_bytes > ws_bytes:
+                break
+            span = rounds * (n_kv_min / s + 3)
+            if span < best:
+                best, best_s = span, s
+    return (units, r if best_s > 1 else 0, best_s)
+
+
 @pytest.mark.parametrize("shape,sms,expect", [
-    # chunked 32K (last 2K): 256 units on 76 pairs, the 28 of the fourth round cut in 2
-    ((1, 64, 8, 2048, 32768, 30720), 152, (256, 28, 2)),
+    # chunked 32K (last 2K): 256 units on 76 pairs, the 28 of the fourth round cut
+    # in 8 (224 pieces: three rounds of pieces of ~30 tiles instead of one of ~120)
+    ((1, 64, 8, 2048, 32768, 30720), 152, (256, 28, 8)),
     # 8K causal: the last round's units are 1-3 key tiles long, nothing to split
     ((1, 64, 8, 8192, 8192, 0), 152, (1024, 0, 1)),
-    # a 128-token chunk after 32K keys: 16 units, each cut in 4 (76 // 16)
-    ((1, 64, 8, 128, 32768, 32640), 152, (16, 16, 4)),
+    # a 128-token chunk after 32K keys: 16 units, each cut in 9 (two rounds)
+    ((1, 64, 8, 128, 32768, 32640), 152, (16, 16, 9)),
     # two units of 32 tiles: at most 32 // 8 = 4 pieces each
     ((1, 8, 2, 128, 4096, 3968), 152, (2, 2, 4)),
     # units fill whole rounds: no split
@@ -174,8 +194,11 @@ PIECE_BYTES_1 = 2 * 128 * 130 * 4  # per piece, one CTA: 2 slots x 128 rows
     ((1, 6, 2, 2048, 32768, 30720), 152, (48, 48, 3)),
     # G = 2, 8K causal: 2048 units, nothing to split
     ((1, 64, 32, 8192, 8192, 0), 152, (2048, 0, 1)),
-    # MHA, a 256-token chunk after 128K keys: 64 heads x 1 two-tile unit on 152 CTAs
-    ((1, 64, 64, 256, 131072, 130816), 152, (64, 64, 2)),
+    # MHA, a 256-token chunk after 128K keys: 64 heads x 1 two-tile unit on 152
+    # CTAs, cut in 7 (three rounds of pieces of ~146 tiles)
+    ((1, 64, 64, 256, 131072, 130816), 152, (64, 64, 7)),
+    # G = 3 over 16 KV heads: 384 units on 152 CTAs, the 80 of the last round cut in 7
+    ((1, 48, 16, 2048, 32768, 30720), 152, (384, 80, 7)),
 ])
 def test_prefill_split_plan(lib, shape, sms, expect):
     B, H_q, H_kv, T_q, S_kv, q_off = shape
@@ -183,14 +206,20 @@ def test_prefill_split_plan(lib, shape, sms, expect):
     assert got == expect
     units, split_units, s = got
     piece = PIECE_BYTES if (H_q // H_kv) % 4 == 0 else PIECE_BYTES_1
+    workers = sms // 2 if (H_q // H_kv) % 4 == 0 else sms
+    n_kv_min = min((q_off + min(T_q, 128) - 1) // 128 + 1, -(-S_kv // 128))
+    assert got == _split_rule(units, workers, n_kv_min, piece, 1 << 30)
     if split_units:
         # the workspace the plan needs is within the size query's bound
         bound = gqa.gqa_attn_prefill_causal_workspace_size(B, H_q, H_kv, T_q, S_kv, 128, q_off,
                                                            sms)
         assert split_units * s * piece <= bound
-        # too small a workspace: no split, never an error
-        assert gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, sms,
-                                                split_units * s * piece - 1)[1] == 0
+        # a workspace one byte short: fewer pieces that fit (or none), never an error
+        small = split_units * s * piece - 1
+        _, su2, s2 = gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, sms,
+                                                      small)
+        assert s2 < s and su2 * s2 * piece <= small
+        assert (units, su2, s2) == _split_rule(units, workers, n_kv_min, piece, small)
         # no workspace: no split
         assert gqa.gqa_attn_prefill_causal_plan(B, H_q, H_kv, T_q, S_kv, 128, q_off, sms,
                                                 0)[1] == 0
@@ -216,10 +245,10 @@ def test_prefill_pieces_cover_the_key_range(q_off, T_q, s):
 
 
 def test_prefill_workspace_size(lib):
-    # one piece per pair at most: 76 pairs on 152 SMs
+    # four rounds of pieces at most: 4 x 76 pairs on 152 SMs
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 2048, 32768, 128, 30720,
-                                                      152) == 76 * PIECE_BYTES
-    # fewer units than pairs: up to 32 pieces per unit, never more than the pairs
+                                                      152) == 304 * PIECE_BYTES
+    # few units: up to 32 pieces per unit
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 8, 2, 128, 4096, 128, 3968,
                                                       152) == 64 * PIECE_BYTES
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 4, 1, 100, 4096, 128, 3996,
@@ -228,7 +257,7 @@ def test_prefill_workspace_size(lib):
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 6, 2, 128, 4096, 128, 3968,
                                                       152) == 128 * PIECE_BYTES_1
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 6, 2, 2048, 32768, 128, 30720,
-                                                      152) == 152 * PIECE_BYTES_1
+                                                      152) == 608 * PIECE_BYTES_1
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 0, 128, 0, 152) == 0
     # rows past the last key are valid: 8 units on 76 pairs, each cut by key range
     assert gqa.gqa_attn_prefill_causal_workspace_size(1, 64, 8, 128, 100, 128, 0, 152) > 0
