@@ -104,7 +104,7 @@ cudaError_t prefill_launch(const PrefillLaunch &a, cudaStream_t stream,
 cudaError_t prefill_pair_prepare_device(int *max_pairs);
 bool prefill_pair_eligible(const PrefillLaunch &a);
 PrefillPlan prefill_pair_plan(const PrefillLaunch &a);
-// Workspace that lets every partial round split (at most one piece per pair).
+// Workspace that lets every partial round split as far as the plan may cut it.
 size_t prefill_pair_workspace_bound(long long units, int num_sms);
 cudaError_t prefill_pair_launch(const PrefillLaunch &a, cudaStream_t stream,
                                 PFN_cuTensorMapEncodeTiled_v12000 encode);
