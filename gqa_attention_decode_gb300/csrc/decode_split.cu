@@ -56,12 +56,17 @@ constexpr int kOneWaveStages = GQA_DECODE_ONE_WAVE_STAGES;
 #ifndef GQA_DECODE_L2_PREFETCH_TILES
 #define GQA_DECODE_L2_PREFETCH_TILES 3
 #endif
-template <int kStages>
-constexpr int smem_bytes() {
-  return kStages * kStageBytes + 2 * kStages * 8 + 1024;  // ring + barriers + alignment slack
-}
 constexpr int kRedStride = kD + 4;  // padded row of the per-warp O reduction buffer
 constexpr int kMaxFusedSplits = kDecodeMaxFusedSplits;  // largest cluster of the fused variant
+// Cluster-merged variant: what a CTA receives from the cluster, one slot per
+// (sender, column it finalises): at most 16 slots for at most 8 columns (a
+// cluster of cs CTAs gives each ceil(8 / cs) columns, cs * ceil(8 / cs) <= 16).
+constexpr int kRecvSlots = 16;
+constexpr int kRecvBytes = 16 + kRecvSlots * (kD + 1) * 4;  // barrier (padded), O rows, lse
+template <int kStages, bool kFused = false>
+constexpr int smem_bytes() {  // ring + barriers (+ receive area) + alignment slack
+  return kStages * kStageBytes + 2 * kStages * 8 + (kFused ? kRecvBytes : 0) + 1024;
+}
 
 struct Params {
   const uint16_t *q;
@@ -94,9 +99,10 @@ __device__ __forceinline__ uint32_t tile_offset(int r, int chunk) {
 
 // kFused = false: each CTA writes its split partial to the workspace and the
 // merge kernel combines them.  kFused = true: the num_splits CTAs of one
-// (sequence, KV head) form a thread-block cluster; each keeps its partial in
-// shared memory and the cluster merges them through distributed shared memory,
-// so one launch produces o and lse and no workspace is touched.
+// (sequence, KV head) form a thread-block cluster; each sends the partial of
+// column n to the shared memory of CTA n % num_splits (st.async, the bytes
+// counted on that CTA's barrier), which merges the columns it received, so one
+// launch produces o and lse and no workspace is touched.
 // kPaged = true: K and V live in pages [num_pages, H_kv, page_size, d] and
 // block_table[b][i] names the page that holds keys [i*page_size, (i+1)*page_size)
 // of sequence b (page_size a multiple of the 64-key tile, so no tile straddles
@@ -117,6 +123,11 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
   uint64_t *empty_bar = full_bar + kStages;
+  // cluster-merged variant: barrier counting the bytes the cluster sends this CTA,
+  // then the received partials (slot = sender * per_rank + column / cluster size)
+  uint64_t *recv_bar = empty_bar + kStages;
+  float *recv_o = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(recv_bar) + 16);
+  float *recv_lse = recv_o + kRecvSlots * kD;
 
   // grid (H_kv, B, splits): the first splits of every (sequence, KV head) come
   // first in launch order, so a multi-wave grid puts the CTAs that hold keys on
@@ -128,16 +139,34 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_consumers = kConsumerWarps * p.cgroups;  // warps before the producer
   __shared__ int failed;
+  // A cluster-merged grid that leaves at least half of the SMs idle lets the next
+  // grid start its prologue there right away (tiny decode 5.13 -> 4.75 us per
+  // call).  A larger one triggers at its end: dependents placed early double up
+  // on the SMs that are free first (batch of 4 at 4K keys: 15.08 -> 15.42 us).
+  if (kFused && 2u * gridDim.x * gridDim.y * gridDim.z <= (unsigned)p.num_sms)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // prologue that reads no input: overlaps the previous kernel when this grid
   // was launched as its programmatic dependent
+  // Cluster-merged variant with cs > 1 CTAs: CTA r finalises columns r, r + cs, ...
+  // (per_rank of them at most), each sent by every CTA of the cluster.
+  const int cs = p.num_splits;
+  const int per_rank = (p.n_cols + cs - 1) / cs;
+  const int n_mine = split < p.n_cols ? (p.n_cols - split + cs - 1) / cs : 0;
+  const bool cluster_merge = kFused && cs > 1 && cs * per_rank <= kRecvSlots;
   if (threadIdx.x == 0) {
     failed = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), n_consumers);
     }
+    if (cluster_merge) {
+      mbar_init(smem_u32(recv_bar), 1);
+      mbar_arrive_expect_tx(smem_u32(recv_bar), (uint32_t)(n_mine * cs * (kD + 1) * 4));
+    }
     fence_mbar_init();
   }
+  // every CTA's receive barrier exists before any CTA of the cluster sends to it
+  if (cluster_merge) cluster_sync();
   if (warp == n_consumers && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -433,15 +462,15 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     }
   }
   __syncthreads();
-  // pass 1, one thread per column: reference max, and the weight of each key
-  // slice with the 1/l normalisation folded in (0 for slices without keys)
-  float *wts = red_o + kConsumerWarps * kMaxCols * kRedStride;  // [4][kMaxCols]
-  float *col_lse = wts + kConsumerWarps * kMaxCols;            // [kMaxCols]
-  int *col_row = reinterpret_cast<int *>(col_lse + kMaxCols);  // [kMaxCols], -1: padding
-  float *cta_o = reinterpret_cast<float *>(col_row + kMaxCols);  // fused: [8][kD] O_s
-  float *cta_lse = cta_o + 8 * kD;                                // fused: [8] lse_s
-  if (threadIdx.x < n_cols_pad) {
-    const int n = threadIdx.x;
+  // One item = (column n, four d values); each item weighs the key slices of
+  // its column itself: reference max, weight 2^(m_w - max) / l of each slice
+  // (0 for slices without keys), O_s = sum of weight * O_slice,
+  // lse_s = max ln 2 + ln l.  The split's partial goes to the workspace, or
+  // (cluster-merged) to the output when the cluster is one CTA, else to the
+  // CTA that finalises the column.
+  for (int item = threadIdx.x; item < n_cols_pad * (kD / 4); item += blockDim.x) {
+    const int n = item / (kD / 4), d4 = item % (kD / 4);
+    if (n >= p.n_cols) continue;  // padding columns (warp-uniform: 32 items per column)
     float mmax = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) mmax = fmaxf(mmax, red_m[w * kMaxCols + n]);
@@ -452,33 +481,12 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
       lsum += red_l[w * kMaxCols + n] * f[w];
     }
     // a column that saw no key in this split (or a failed CTA) contributes nothing
-    const bool empty = failed || !(lsum > 0.f) || n >= p.n_cols;
+    const bool empty = failed || !(lsum > 0.f);
     const float inv = empty ? 0.f : 1.f / lsum;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) wts[w * kMaxCols + n] = f[w] * inv;
-    const float lse_s = empty ? -INFINITY : mmax * 0.69314718055994531f + logf(lsum);
-    int row = -1;
-    if (n < p.n_cols)
-      row = (int)(((size_t)b * p.H_q + (size_t)kv * p.G + n / p.T_q) * p.T_q + n % p.T_q);
-    col_row[n] = row;
-    if (kFused) {
-      cta_lse[n] = lse_s;
-    } else if (row >= 0 &&
-               store_ok((size_t)row * p.num_splits + split,
-                        (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) {
-      p.lse_part[(size_t)row * p.num_splits + split] = lse_s;
-    }
-  }
-  __syncthreads();
-  // pass 2: O_s = sum over key slices of weight * O_slice, four columns per item
-  for (int item = threadIdx.x; item < n_cols_pad * (kD / 4); item += blockDim.x) {
-    const int n = item / (kD / 4), d4 = item % (kD / 4);
-    const int row = col_row[n];
-    if (row < 0) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float wt = wts[w * kMaxCols + n];
+      const float wt = f[w] * inv;
       const float4 x =
           reinterpret_cast<const float4 *>(red_o + ((size_t)w * kMaxCols + n) * kRedStride)[d4];
       acc.x = fmaf(wt, x.x, acc.x);
@@ -486,46 +494,76 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
       acc.z = fmaf(wt, x.z, acc.z);
       acc.w = fmaf(wt, x.w, acc.w);
     }
-    if (kFused) {
-      reinterpret_cast<float4 *>(cta_o + n * kD)[d4] = acc;
-    } else if (store_ok((size_t)row * p.num_splits + split,
-                        (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) {
-      reinterpret_cast<float4 *>(p.o_part + ((size_t)row * p.num_splits + split) * kD)[d4] = acc;
+    const float lse_s = empty ? -INFINITY : mmax * 0.69314718055994531f + logf(lsum);
+    const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + n / p.T_q) * p.T_q + n % p.T_q;
+    if (!kFused) {
+      const size_t prow = row * p.num_splits + split;
+      if (!store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) continue;
+      if (d4 == 0) p.lse_part[prow] = lse_s;
+      reinterpret_cast<float4 *>(p.o_part + prow * kD)[d4] = acc;
+    } else if (cs == 1) {  // a cluster of one: this split is the whole sequence
+      if (!store_ok(row, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) continue;
+      if (d4 == 0) p.lse[row] = lse_s;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x, acc.y);
+      pk.y = pack_bf16x2(acc.z, acc.w);
+      reinterpret_cast<uint2 *>(p.o + row * kD)[d4] = pk;
+    } else if (cluster_merge) {
+      // to CTA n % cs, slot (this split, n / cs): bytes counted on its barrier
+      const uint32_t dst = (uint32_t)(n % cs);
+      const int slot = split * per_rank + n / cs;
+      const uint32_t bar = dsmem_addr(smem_u32(recv_bar), dst);
+      st_async_f32x4(dsmem_addr(smem_u32(recv_o + slot * kD + 4 * d4), dst), acc, bar);
+      if (d4 == 0) st_async_f32(dsmem_addr(smem_u32(recv_lse + slot), dst), lse_s, bar);
     }
   }
-  if (kFused) {
-    // log-sum-exp merge across the cluster: CTA r finalises columns r, r + splits, ...
-    cluster_sync();
-    const int cs = p.num_splits;
-    const uint32_t rank = cluster_ctarank();
-    if (threadIdx.x < kD) {
-      const int dd = threadIdx.x;
-      constexpr float kLog2e = 1.4426950408889634f;
-      for (int n = (int)rank; n < p.n_cols; n += cs) {
-        const uint32_t lse_at = smem_u32(cta_lse + n), o_at = smem_u32(cta_o + n * kD + dd);
-        float mx = -INFINITY;
-        for (int c = 0; c < cs; ++c) mx = fmaxf(mx, ld_dsmem_f32(dsmem_addr(lse_at, c)));
-        float wsum = 0.f, acc = 0.f;
-        if (mx != -INFINITY) {
-          for (int c = 0; c < cs; ++c) {
-            const float w = fast_exp2((ld_dsmem_f32(dsmem_addr(lse_at, c)) - mx) * kLog2e);
-            wsum += w;
-            acc = fmaf(w, ld_dsmem_f32(dsmem_addr(o_at, c)), acc);
-          }
-        }
-        const int gh = n / p.T_q, tq = n % p.T_q;
-        const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + gh) * p.T_q + tq;
-        const __nv_bfloat16 r = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
-        if (!store_ok(row, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) continue;
-        p.o[row * kD + dd] = *reinterpret_cast<const uint16_t *>(&r);
-        if (dd == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+  if (kFused && cs > 1 && !cluster_merge && threadIdx.x == 0)
+    atomicExch(p.wait.status, kStatusInvalidArg);  // more columns than the receive area holds
+  if (cluster_merge && n_mine > 0) {
+    // log-sum-exp merge of the cluster's partials of this CTA's columns, once every
+    // CTA's bytes have landed here: lse = m + ln sum_c e^(lse_c - m),
+    // O = sum_c e^(lse_c - lse) O_c.  No CTA reads another's shared memory, so
+    // none waits for the others before it exits.
+    const bool landed = mbar_wait(smem_u32(recv_bar), 0, p.wait);
+    constexpr float kLog2e = 1.4426950408889634f;
+    for (int item = threadIdx.x; landed && item < n_mine * (kD / 4); item += blockDim.x) {
+      const int nl = item / (kD / 4), d4 = item % (kD / 4);
+      const int n = split + cs * nl;
+      float ls[kMaxFusedSplits];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMaxFusedSplits; ++c) {
+        ls[c] = c < cs ? recv_lse[c * per_rank + nl] : -INFINITY;
+        mx = fmaxf(mx, ls[c]);
       }
+      float wsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int c = 0; c < kMaxFusedSplits; ++c) {
+          if (c >= cs) break;
+          const float w = fast_exp2((ls[c] - mx) * kLog2e);  // 0 for a split without keys
+          const float4 x = reinterpret_cast<const float4 *>(recv_o + (c * per_rank + nl) * kD)[d4];
+          wsum += w;
+          acc.x = fmaf(w, x.x, acc.x);
+          acc.y = fmaf(w, x.y, acc.y);
+          acc.z = fmaf(w, x.z, acc.z);
+          acc.w = fmaf(w, x.w, acc.w);
+        }
+      }
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+      const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + n / p.T_q) * p.T_q + n % p.T_q;
+      if (!store_ok(row, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) continue;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      reinterpret_cast<uint2 *>(p.o + row * kD)[d4] = pk;
+      if (d4 == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
     }
-    cluster_sync();  // no CTA leaves while others still read its shared memory
   }
   // this CTA's partial is written: the merge grid may be scheduled (triggering
   // at the start instead measured 1 us slower per call: the waiting merge CTAs
-  // slow the streaming ones)
+  // slow the streaming ones; the cluster-merged grid has triggered at its start)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -651,10 +689,11 @@ static cudaError_t set_smem_attr() {
   using namespace decode;
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused, false, kNT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes<kStages>());
+                                       smem_bytes<kStages, kFused>());
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(decode_split_kernel<kStages, kMinBlocks, kFused, true, kNT>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<kStages>());
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes<kStages, kFused>());
 }
 
 cudaError_t decode_prepare_device(int *fused_clusters) {
@@ -680,7 +719,7 @@ cudaError_t decode_prepare_device(int *fused_clusters) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, 1, 1);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<3>();
+    cfg.dynamicSmemBytes = smem_bytes<3, true>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
@@ -712,7 +751,7 @@ template <int kStages, int kMinBlocks, bool kFused, int kNT>
 static cudaError_t launch_variant(cudaLaunchConfig_t *cfg, const CUtensorMap &tm_k,
                                   const CUtensorMap &tm_v, const decode::Params &p, bool paged) {
   using namespace decode;
-  cfg->dynamicSmemBytes = smem_bytes<kStages>();
+  cfg->dynamicSmemBytes = smem_bytes<kStages, kFused>();
   cfg->blockDim = dim3(32 * (kConsumerWarps * p.cgroups + 1));
   if (paged)
     return cudaLaunchKernelEx(cfg, decode_split_kernel<kStages, kMinBlocks, kFused, true, kNT>,

@@ -281,10 +281,19 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+// Asynchronous stores into another CTA's shared memory (shared::cluster addresses,
+// from dsmem_addr): the bytes land in that CTA, whose mbarrier `bar` (also a
+// shared::cluster address) counts them as completed transaction bytes.
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr),
+               "f"(v), "r"(bar)
+               : "memory");
 }
 
 // Every thread of every CTA in the cluster; shared-memory writes before it are
