@@ -462,59 +462,115 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     }
   }
   __syncthreads();
-  // One item = (column n, four d values); each item weighs the key slices of
-  // its column itself: reference max, weight 2^(m_w - max) / l of each slice
-  // (0 for slices without keys), O_s = sum of weight * O_slice,
-  // lse_s = max ln 2 + ln l.  The split's partial goes to the workspace, or
-  // (cluster-merged) to the output when the cluster is one CTA, else to the
-  // CTA that finalises the column.
-  for (int item = threadIdx.x; item < n_cols_pad * (kD / 4); item += blockDim.x) {
-    const int n = item / (kD / 4), d4 = item % (kD / 4);
-    if (n >= p.n_cols) continue;  // padding columns (warp-uniform: 32 items per column)
-    float mmax = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) mmax = fmaxf(mmax, red_m[w * kMaxCols + n]);
-    float f[kConsumerWarps], lsum = 0.f;
+  // Weights of the four key slices of column n: reference max, weight
+  // 2^(m_w - max) / l (0 for slices without keys, and for every slice of a
+  // column that saw no key or of a failed CTA), lse_s = max ln 2 + ln l.
+  const bool failed_cta = failed;
+  auto slice_weights = [&](int n, float (&wt)[kConsumerWarps]) {
+    float mw[kConsumerWarps], lw[kConsumerWarps];
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      f[w] = mmax == -INFINITY ? 0.f : fast_exp2(red_m[w * kMaxCols + n] - mmax);
-      lsum += red_l[w * kMaxCols + n] * f[w];
+      mw[w] = red_m[w * kMaxCols + n];
+      lw[w] = red_l[w * kMaxCols + n];
     }
-    // a column that saw no key in this split (or a failed CTA) contributes nothing
-    const bool empty = failed || !(lsum > 0.f);
-    const float inv = empty ? 0.f : 1.f / lsum;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float mmax = fmaxf(fmaxf(mw[0], mw[1]), fmaxf(mw[2], mw[3]));
+    float lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float wt = f[w] * inv;
-      const float4 x =
-          reinterpret_cast<const float4 *>(red_o + ((size_t)w * kMaxCols + n) * kRedStride)[d4];
-      acc.x = fmaf(wt, x.x, acc.x);
-      acc.y = fmaf(wt, x.y, acc.y);
-      acc.z = fmaf(wt, x.z, acc.z);
-      acc.w = fmaf(wt, x.w, acc.w);
+      wt[w] = mmax == -INFINITY ? 0.f : fast_exp2(mw[w] - mmax);
+      lsum = fmaf(lw[w], wt[w], lsum);
     }
-    const float lse_s = empty ? -INFINITY : mmax * 0.69314718055994531f + logf(lsum);
-    const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + n / p.T_q) * p.T_q + n % p.T_q;
-    if (!kFused) {
-      const size_t prow = row * p.num_splits + split;
-      if (!store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) continue;
-      if (d4 == 0) p.lse_part[prow] = lse_s;
-      reinterpret_cast<float4 *>(p.o_part + prow * kD)[d4] = acc;
-    } else if (cs == 1) {  // a cluster of one: this split is the whole sequence
-      if (!store_ok(row, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) continue;
-      if (d4 == 0) p.lse[row] = lse_s;
-      uint2 pk;
-      pk.x = pack_bf16x2(acc.x, acc.y);
-      pk.y = pack_bf16x2(acc.z, acc.w);
-      reinterpret_cast<uint2 *>(p.o + row * kD)[d4] = pk;
-    } else if (cluster_merge) {
-      // to CTA n % cs, slot (this split, n / cs): bytes counted on its barrier
-      const uint32_t dst = (uint32_t)(n % cs);
-      const int slot = split * per_rank + n / cs;
-      const uint32_t bar = dsmem_addr(smem_u32(recv_bar), dst);
-      st_async_f32x4(dsmem_addr(smem_u32(recv_o + slot * kD + 4 * d4), dst), acc, bar);
-      if (d4 == 0) st_async_f32(dsmem_addr(smem_u32(recv_lse + slot), dst), lse_s, bar);
+    const bool empty = failed_cta || !(lsum > 0.f);
+    const float inv = empty ? 0.f : fast_rcp(lsum);  // lsum >= 1 when not empty
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) wt[w] *= inv;
+    return empty ? -INFINITY : (mmax + fast_log2(lsum)) * 0.69314718055994531f;
+  };
+  auto out_row = [&](int n) {  // (sequence, query head, new token) row of column n
+    const int gh = p.T_q == 1 ? n : n / p.T_q, tq = p.T_q == 1 ? 0 : n % p.T_q;
+    return ((size_t)b * p.H_q + (size_t)kv * p.G + gh) * p.T_q + tq;
+  };
+  if constexpr (kNT == 2 && !kFused) {
+    // many columns: one thread per column weighs its slices, then O_s = sum of
+    // weight * O_slice per (column, four d values)
+    float *wts = red_o + kConsumerWarps * kMaxCols * kRedStride;  // [4][kMaxCols]
+    size_t *col_prow = reinterpret_cast<size_t *>(wts + kConsumerWarps * kMaxCols);  // [kMaxCols]
+    if (threadIdx.x < p.n_cols) {
+      const int n = threadIdx.x;
+      float wt[kConsumerWarps];
+      const float lse_s = slice_weights(n, wt);
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) wts[w * kMaxCols + n] = wt[w];
+      const size_t prow = out_row(n) * p.num_splits + split;
+      col_prow[n] = prow;
+      if (store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status))
+        p.lse_part[prow] = lse_s;
+    }
+    __syncthreads();
+    for (int item = threadIdx.x; item < n_cols_pad * (kD / 4); item += blockDim.x) {
+      const int n = item / (kD / 4), d4 = item % (kD / 4);
+      if (n >= p.n_cols) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float wt = wts[w * kMaxCols + n];
+        const float4 x =
+            reinterpret_cast<const float4 *>(red_o + ((size_t)w * kMaxCols + n) * kRedStride)[d4];
+        acc.x = fmaf(wt, x.x, acc.x);
+        acc.y = fmaf(wt, x.y, acc.y);
+        acc.z = fmaf(wt, x.z, acc.z);
+        acc.w = fmaf(wt, x.w, acc.w);
+      }
+      const size_t prow = col_prow[n];
+      if (store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status))
+        reinterpret_cast<float4 *>(p.o_part + prow * kD)[d4] = acc;
+    }
+  } else {
+    // at most 8 columns: each item = (column n, four d values) weighs its
+    // column's slices itself (no second barrier).  The split's partial goes to
+    // the workspace, or (cluster-merged) to the output when the cluster is one
+    // CTA, else to the CTA that finalises the column.
+    for (int item = threadIdx.x; item < n_cols_pad * (kD / 4); item += blockDim.x) {
+      const int n = item / (kD / 4), d4 = item % (kD / 4);
+      if (n >= p.n_cols) continue;  // padding columns (warp-uniform: 32 items per column)
+      float4 xw[kConsumerWarps];
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w)
+        xw[w] =
+            reinterpret_cast<const float4 *>(red_o + ((size_t)w * kMaxCols + n) * kRedStride)[d4];
+      float wt[kConsumerWarps];
+      const float lse_s = slice_weights(n, wt);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        acc.x = fmaf(wt[w], xw[w].x, acc.x);
+        acc.y = fmaf(wt[w], xw[w].y, acc.y);
+        acc.z = fmaf(wt[w], xw[w].z, acc.z);
+        acc.w = fmaf(wt[w], xw[w].w, acc.w);
+      }
+      const size_t row = out_row(n);
+      if (!kFused) {
+        const size_t prow = row * p.num_splits + split;
+        if (!store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) continue;
+        if (d4 == 0) p.lse_part[prow] = lse_s;
+        reinterpret_cast<float4 *>(p.o_part + prow * kD)[d4] = acc;
+      } else if (cs == 1) {  // a cluster of one: this split is the whole sequence
+        if (!store_ok(row, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) continue;
+        if (d4 == 0) p.lse[row] = lse_s;
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x, acc.y);
+        pk.y = pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2 *>(p.o + row * kD)[d4] = pk;
+      } else if (cluster_merge) {
+        // to CTA n % cs, slot (this split, n / cs): bytes counted on its barrier
+        // (n < 8 and cs >= 2: the quotient is at most 3)
+        const int quo = (n >= cs) + (n >= 2 * cs) + (n >= 3 * cs);
+        const uint32_t dst = (uint32_t)(n - quo * cs);
+        const int slot = split * per_rank + quo;
+        const uint32_t bar = dsmem_addr(smem_u32(recv_bar), dst);
+        st_async_f32x4(dsmem_addr(smem_u32(recv_o + slot * kD + 4 * d4), dst), acc, bar);
+        if (d4 == 0) st_async_f32(dsmem_addr(smem_u32(recv_lse + slot), dst), lse_s, bar);
+      }
     }
   }
   if (kFused && cs > 1 && !cluster_merge && threadIdx.x == 0)
@@ -530,10 +586,16 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
       const int nl = item / (kD / 4), d4 = item % (kD / 4);
       const int n = split + cs * nl;
       float ls[kMaxFusedSplits];
+      float4 x[kMaxFusedSplits];
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kMaxFusedSplits; ++c) {
-        ls[c] = c < cs ? recv_lse[c * per_rank + nl] : -INFINITY;
+        ls[c] = -INFINITY;
+        x[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < cs) {
+          ls[c] = recv_lse[c * per_rank + nl];
+          x[c] = reinterpret_cast<const float4 *>(recv_o + (c * per_rank + nl) * kD)[d4];
+        }
         mx = fmaxf(mx, ls[c]);
       }
       float wsum = 0.f;
@@ -541,24 +603,22 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
       if (mx != -INFINITY) {
 #pragma unroll
         for (int c = 0; c < kMaxFusedSplits; ++c) {
-          if (c >= cs) break;
           const float w = fast_exp2((ls[c] - mx) * kLog2e);  // 0 for a split without keys
-          const float4 x = reinterpret_cast<const float4 *>(recv_o + (c * per_rank + nl) * kD)[d4];
           wsum += w;
-          acc.x = fmaf(w, x.x, acc.x);
-          acc.y = fmaf(w, x.y, acc.y);
-          acc.z = fmaf(w, x.z, acc.z);
-          acc.w = fmaf(w, x.w, acc.w);
+          acc.x = fmaf(w, x[c].x, acc.x);
+          acc.y = fmaf(w, x[c].y, acc.y);
+          acc.z = fmaf(w, x[c].z, acc.z);
+          acc.w = fmaf(w, x[c].w, acc.w);
         }
       }
-      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-      const size_t row = ((size_t)b * p.H_q + (size_t)kv * p.G + n / p.T_q) * p.T_q + n % p.T_q;
+      const float inv = wsum > 0.f ? fast_rcp(wsum) : 0.f;
+      const size_t row = out_row(n);
       if (!store_ok(row, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) continue;
       uint2 pk;
       pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
       pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
       reinterpret_cast<uint2 *>(p.o + row * kD)[d4] = pk;
-      if (d4 == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+      if (d4 == 0) p.lse[row] = wsum > 0.f ? mx + fast_log2(wsum) * 0.69314718055994531f : -INFINITY;
     }
   }
   // this CTA's partial is written: the merge grid may be scheduled (triggering
@@ -657,10 +717,10 @@ __global__ void __launch_bounds__(kMergeThreads)
         sum.w = fmaf(f, x.w, sum.w);
         W = fmaf(f, red_w[g], W);
       }
-      const float inv = 1.f / W;
+      const float inv = fast_rcp(W);  // W >= 1: the largest split weighs 1
       packed.x = pack_bf16x2(sum.x * inv, sum.y * inv);
       packed.y = pack_bf16x2(sum.z * inv, sum.w * inv);
-      lse_out = mx + logf(W);
+      lse_out = mx + fast_log2(W) * 0.69314718055994531f;
     }
     reinterpret_cast<uint2 *>(o + row * kD)[lane] = packed;
     if (lane == 0) lse[row] = lse_out;

@@ -352,4 +352,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Approximate reciprocal and base-2 logarithm (one special-function instruction
+// each; relative errors near 2^-23 and 2^-22), for normalising a softmax row.
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 }  // namespace gqa
