@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float w0 = l0 > 0.f ? fast_exp2(m0 - mx) : 0.f;
       const float w1 = l1 > 0.f ? fast_exp2(m1 - mx) : 0.f;
       const float L = w0 * l0 + w1 * l1;
-      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float inv = L > 0.f ? fast_rcp(L) : 0.f;  // L >= 1: the larger slot weighs 1
       const float c0 = w0 * inv, c1 = w1 * inv;  // 0 for a slot with no visible key
       // rows past G * T_q belong to other heads' queries: computed, never stored
       const size_t row0 = (size_t)(b * p.H_q + kv * p.G) * p.T_q;  // the group's first row
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s == 0 && row < R && store_ok((row0 + row) * p.num_splits + split, n_part_rows,
                                         p.wait.status))
         p.lse_part[(row0 + row) * p.num_splits + split] =
-            L > 0.f ? mx * 0.69314718055994531f + logf(L) : -INFINITY;
+            L > 0.f ? (mx + fast_log2(L)) * 0.69314718055994531f : -INFINITY;
       // The combined rows go through shared memory so that the global stores are
       // contiguous 256-byte row halves: a thread holds one row, and storing it
       // directly would make every warp store touch 32 rows.  The ring is idle
