@@ -133,3 +133,23 @@ def test_nan_padding_tensor_cores():
     o, l = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 0.1)
     torch.cuda.synchronize()
     assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
+@pytest.mark.parametrize("num_splits", [2, 3, 5, 7, 9, 16])
+@pytest.mark.parametrize("G,T_q", [(1, 1), (3, 1), (5, 1), (8, 1), (2, 3), (4, 2)])
+def test_cluster_merge_sizes(num_splits, G, T_q):
+    """The single-kernel path: each CTA of a cluster of num_splits sends every
+    column's partial to the CTA that finalises it (column n to CTA n mod
+    num_splits); clusters of 2-16 CTAs against 1-8 (head, token) columns, with a
+    sequence that leaves splits empty and one with no keys."""
+    H_kv = 2
+    S_max = 128 * num_splits
+    seqlens = [S_max, S_max // 3 + 1, 0]
+    q, k, v, sl = inputs(3, G * H_kv, H_kv, T_q, S_max, seqlens, 60 + num_splits)
+    count = gqa.gqa_attn_decode_kernel_count(3, G * H_kv, H_kv, S_max, 128, num_splits)
+    if num_splits <= 8:  # portable cluster sizes: always the single kernel
+        assert count == 1
+    o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 1 / math.sqrt(128), num_splits)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, f"cluster of {num_splits}, G={G}, T_q={T_q} ({count} kernel)")
