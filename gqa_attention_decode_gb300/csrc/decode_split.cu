@@ -237,22 +237,34 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     const int row = b * p.H_kv + kv;
     int issued = 0;
     int page_base = -1 << 30, page_reg = 0;
+    int page = 0, page_off = 0, page_c3 = 0;  // the tile's page, its first key there, its block
     for (int i = 0; i < n_tiles; ++i) {
       const int key0 = key_begin + i * kTileKeys;
       int c2 = key0, c3 = row;  // tensor-map coordinates of the tile's first key
       if (kPaged) {
-        const int page = key0 / p.page_size;
-        if (page - page_base >= 32 || page < page_base) {
-          page_base = page;
-          const int idx = page_base + lane;
-          page_reg = idx < p.max_pages ? __ldca(p.block_table + (size_t)b * p.max_pages + idx) : 0;
+        // pages advance by whole tiles: the page and the offset in it are
+        // stepped, and the page's block is looked up only when a page begins
+        if (i == 0) {
+          page = key0 / p.page_size;
+          page_off = key0 - page * p.page_size;
+        } else if ((page_off += kTileKeys) == p.page_size) {
+          ++page;
+          page_off = 0;
         }
-        const int page_id = __shfl_sync(0xffffffffu, page_reg, page - page_base);
-        // a page id outside the pool reads zeros (TMA out-of-bounds fill); report it
-        const bool bad = page_id < 0 || page_id >= p.num_pages;
-        if (bad && lane == 0) atomicExch(p.wait.status, kStatusInvalidArg);
-        c2 = key0 - page * p.page_size;
-        c3 = bad ? p.num_pages * p.H_kv : page_id * p.H_kv + kv;  // bad: one block past the map
+        if (i == 0 || page_off == 0) {  // warp-uniform
+          if (page - page_base >= 32 || page < page_base) {
+            page_base = page;
+            const int idx = page_base + lane;
+            page_reg = idx < p.max_pages ? __ldca(p.block_table + (size_t)b * p.max_pages + idx) : 0;
+          }
+          const int page_id = __shfl_sync(0xffffffffu, page_reg, page - page_base);
+          // a page id outside the pool reads zeros (TMA out-of-bounds fill); report it
+          const bool bad = page_id < 0 || page_id >= p.num_pages;
+          if (bad && lane == 0) atomicExch(p.wait.status, kStatusInvalidArg);
+          page_c3 = bad ? p.num_pages * p.H_kv : page_id * p.H_kv + kv;  // bad: past the map
+        }
+        c2 = page_off;
+        c3 = page_c3;
       }
       bool ok = true;
       if (lane == 0) {
