@@ -145,14 +145,14 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   // on the SMs that are free first (batch of 4 at 4K keys: 15.08 -> 15.42 us).
   if (kFused && 2u * gridDim.x * gridDim.y * gridDim.z <= (unsigned)p.num_sms)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // prologue that reads no input: overlaps the previous kernel when this grid
-  // was launched as its programmatic dependent
   // Cluster-merged variant with cs > 1 CTAs: CTA r finalises columns r, r + cs, ...
   // (per_rank of them at most), each sent by every CTA of the cluster.
   const int cs = p.num_splits;
   const int per_rank = (p.n_cols + cs - 1) / cs;
   const int n_mine = split < p.n_cols ? (p.n_cols - split + cs - 1) / cs : 0;
   const bool cluster_merge = kFused && cs > 1 && cs * per_rank <= kRecvSlots;
+  // prologue that reads no input: overlaps the previous kernel when this grid
+  // was launched as its programmatic dependent
   if (threadIdx.x == 0) {
     failed = 0;
     for (int s = 0; s < kStages; ++s) {
