@@ -102,6 +102,30 @@ def test_seeded_random_shapes(B, H_q, H_kv, T_q, S_kv, q_offset):
     compare(o, lse, o_ref, lse_ref, f"random {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
 
 
+def _seeded_wide_configs(n, seed):
+    """Larger random shapes: several rounds of work units, key-range pieces,
+    and query rows past the last key (S_kv < q_offset + T_q)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        G = int(rng.choice([1, 2, 4, 5, 8, 16]))
+        H_kv = int(rng.choice([1, 2, 4]))
+        B = int(rng.integers(1, 3))
+        T_q = int(rng.integers(100, 1500))
+        q_offset = int(rng.integers(0, 3000))
+        short = int(rng.integers(0, min(T_q, 200))) if rng.random() < 0.4 else 0
+        out.append((B, G * H_kv, H_kv, T_q, max(1, q_offset + T_q - short), q_offset))
+    return out
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,T_q,S_kv,q_offset", _seeded_wide_configs(8, 2026))
+def test_seeded_random_shapes_wide(B, H_q, H_kv, T_q, S_kv, q_offset):
+    q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=41, device=DEV)
+    o, lse = run(q, k, v, q_offset, 0.09)
+    o_ref, lse_ref = oracle.prefill_causal(np64(q), np64(k), np64(v), q_offset, 0.09)
+    compare(o, lse, o_ref, lse_ref, f"random wide {B},{H_q},{H_kv},{T_q},{S_kv},{q_offset}")
+
+
 def test_group_of_16_full():
     """G = 16 (four head quads per KV head), 4K causal, every row."""
     from oracle_pool import prefill_causal_parallel
