@@ -223,11 +223,13 @@ __global__ void selftest_wait_kernel(gqa::WaitCtl wait) {
   __syncthreads();
 }
 
+#ifdef GQA_DEBUG_BOUNDS
 // One store of index `extent` into an `extent`-element range: past its end by
 // one, so a bounds-checked build records GQA_ERR_OUT_OF_BOUNDS and skips it.
 __global__ void selftest_bounds_kernel(float *sink, int *status) {
   if (threadIdx.x == 0 && gqa::store_ok(1, 1, status)) sink[0] = 1.f;
 }
+#endif
 
 }  // namespace
 
