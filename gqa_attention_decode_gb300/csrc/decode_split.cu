@@ -592,6 +592,8 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     // CTA's bytes have landed here: lse = m + ln sum_c e^(lse_c - m),
     // O = sum_c e^(lse_c - lse) O_c.  No CTA reads another's shared memory, so
     // none waits for the others before it exits.
+    // (a wait that runs out means a CTA of the cluster is stuck: the timeout is
+    // recorded in the status word and this CTA's columns are not written)
     const bool landed = mbar_wait(smem_u32(recv_bar), 0, p.wait);
     constexpr float kLog2e = 1.4426950408889634f;
     for (int item = threadIdx.x; landed && item < n_mine * (kD / 4); item += blockDim.x) {
