@@ -255,7 +255,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                              w.b * p.H_q + h, pol_q);
         }
         const int kv_row = w.b * p.H_kv + w.kv;
+        // the next unit's Q is pulled into L2 a few key tiles before this unit
+        // ends, so its copy at the unit change reads L2 rather than HBM
+        const int u_next = snake_unit(k + 1, pair_id, p.n_pairs);
+        const int j_pf = max(w.kv_lo, w.kv_hi - 4);
         for (int j = w.kv_lo; ok && j < w.kv_hi; ++j) {
+          if (j == j_pf && u_next < p.n_items) {
+            const Unit wn = unit_at(p, u_next);
+            for (int i = 0; i < 2; ++i)
+              for (int half = 0; half < 2; ++half)
+                tma_prefetch_l2_4d(&tm_q, 0, half, wn.qt * kBM, wn.b * p.H_q + head_of(p, wn, rank, i));
+          }
           for (int which = 0; which < 2; ++which, ++ld) {
             const int s = ld % kStages;
             if (!wait_bar(kv_empty(s), ((ld / kStages) & 1) ^ 1, p.wait, abort_flag)) {
