@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
 
     for (int i = 0; i < n_tiles; ++i) {
       const int s = i % kStages;
-      // every lane waits (acquiring the TMA data); the verdict is made warp-uniform
+      // every lane waits (acquiring the TMA data); the outcome is made warp-uniform
       const bool ready = mbar_wait(smem_u32(&full_bar[s]), (i / kStages) & 1, p.wait);
       if (!__all_sync(0xffffffffu, ready)) {
         if (lane == 0) atomicExch(&failed, 1);
