@@ -82,6 +82,7 @@ struct Params {
   int T_q, n_cols, cgroups;  // new tokens per sequence, G * T_q, column groups of 4 warps
   float scale_log2;  // scale * log2(e)
   int l2_prefetch_tiles;  // tiles of its chunk a CTA pulls into L2 before the dependency wait
+  int direct_out;  // one split per (sequence, KV head): the partial is the output (o, lse)
   WaitCtl wait;
 };
 
@@ -219,8 +220,9 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     atomicExch(p.wait.status, kStatusInvalidArg);
   const int key_begin = split * chunk;
   const int key_end = min(key_begin + chunk, seqlen);
-  if (!kFused && key_begin >= key_end) return;  // empty split: the merge never reads it
-  // (a fused CTA with no keys still takes part in the cluster merge)
+  // an empty split: the merge never reads it (a fused CTA with no keys still takes
+  // part in the cluster merge, and a direct-output CTA writes O = 0, lse = -inf)
+  if (!kFused && !p.direct_out && key_begin >= key_end) return;
   const int n_tiles = max(0, (key_end - key_begin + kTileKeys - 1) / kTileKeys);
   // keys every column may see in this split (token 0 is the most restricted)
   const int key_all = min(key_end, seqlen - p.T_q + 1);
@@ -516,7 +518,7 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
       const size_t prow = out_row(n) * p.num_splits + split;
       col_prow[n] = prow;
       if (store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status))
-        p.lse_part[prow] = lse_s;
+        (p.direct_out ? p.lse : p.lse_part)[prow] = lse_s;  // one split: prow is the row
     }
     __syncthreads();
     for (int item = threadIdx.x; item < n_cols_pad * (kD / 4); item += blockDim.x) {
@@ -534,8 +536,15 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
         acc.w = fmaf(wt, x.w, acc.w);
       }
       const size_t prow = col_prow[n];
-      if (store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status))
+      if (!store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) continue;
+      if (p.direct_out) {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x, acc.y);
+        pk.y = pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2 *>(p.o + prow * kD)[d4] = pk;
+      } else {
         reinterpret_cast<float4 *>(p.o_part + prow * kD)[d4] = acc;
+      }
     }
   } else {
     // at most 8 columns: each item = (column n, four d values) weighs its
@@ -561,12 +570,12 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
         acc.w = fmaf(wt[w], xw[w].w, acc.w);
       }
       const size_t row = out_row(n);
-      if (!kFused) {
+      if (!kFused && !p.direct_out) {
         const size_t prow = row * p.num_splits + split;
         if (!store_ok(prow, (size_t)p.B * p.H_q * p.T_q * p.num_splits, p.wait.status)) continue;
         if (d4 == 0) p.lse_part[prow] = lse_s;
         reinterpret_cast<float4 *>(p.o_part + prow * kD)[d4] = acc;
-      } else if (cs == 1) {  // a cluster of one: this split is the whole sequence
+      } else if (!kFused || cs == 1) {  // one split (or a cluster of one): the whole sequence
         if (!store_ok(row, (size_t)p.B * p.H_q * p.T_q, p.wait.status)) continue;
         if (d4 == 0) p.lse[row] = lse_s;
         uint2 pk;
@@ -932,6 +941,7 @@ static decode::Params make_params(const DecodeLaunch &a) {
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
   p.l2_prefetch_tiles = 0;
+  p.direct_out = a.direct_out && a.num_splits == 1;
   p.wait = a.wait;
   return p;
 }

@@ -333,6 +333,11 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   if (phase == kPhaseBoth && !tensor_cores && gqa::decode_fused_eligible(a)) {
     return gqa::decode_fused_launch(a, s, g_encode) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
   }
+  if (phase == kPhaseBoth && !tensor_cores && splits == 1 && S_max > 0) {
+    // one split per (sequence, KV head): the split kernel writes o and lse itself
+    a.direct_out = 1;
+    return gqa::decode_split_launch(a, s, g_encode) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  }
   if (phase & kPhaseSplit) {
     const cudaError_t e = tensor_cores ? gqa::decode_tc_split_launch(a, s, g_encode)
                                        : gqa::decode_split_launch(a, s, g_encode);
@@ -438,7 +443,8 @@ GQA_API int gqa_attn_decode_kernel_count(int B, int H_q, int H_kv, int S_max, in
   a.S_max = S_max;
   a.num_splits = splits;
   a.fused_clusters = st->fused_clusters;
-  const bool single = !decode_on_tensor_cores(H_q, H_kv, 1) && gqa::decode_fused_eligible(a);
+  const bool single = !decode_on_tensor_cores(H_q, H_kv, 1) &&
+                      (gqa::decode_fused_eligible(a) || splits == 1);
   *out_kernels = single ? 1 : (S_max > 0 ? 2 : 1);
   return GQA_OK;
 }

@@ -28,6 +28,7 @@ struct DecodeLaunch {
   float *lse_part;  // [B, H_q, T_q, num_splits]
   int num_sms;
   const int *fused_clusters;  // [kDecodeMaxFusedSplits + 1]: co-resident clusters per size
+  int direct_out;  // split kernel with num_splits == 1: write o and lse, no merge follows
   WaitCtl wait;
 };
 

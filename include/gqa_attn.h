@@ -160,6 +160,8 @@ GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_ma
  *     the splits of a (sequence, KV head) form a thread-block cluster and
  *     merge their partials through distributed shared memory; `workspace` is
  *     not touched;
+ *   - other plans of one split per (sequence, KV head): ONE kernel, the split
+ *     kernel writing o and lse itself; `workspace` is not touched;
  *   - other plans: the split kernel, which writes one partial per split to
  *     `workspace`, then the log-sum-exp merge kernel (launched as a
  *     programmatic dependent, so its launch overlaps the split kernel).
@@ -250,7 +252,8 @@ GQA_API int gqa_attn_decode_multi(const gqa_bf16_t *q, const gqa_bf16_t *k_cache
 
 /*
  * Number of kernels gqa_attn_decode launches for these arguments on the current
- * device: 1 (single-kernel cluster path), 2 (split + merge), 0 when B == 0.
+ * device: 1 (single-kernel cluster path, or one split per sequence and KV
+ * head), 2 (split + merge), 0 when B == 0.
  * Host only except for the first call on a device, which performs the
  * per-device set-up.  Returns the status of the argument checks.
  */

@@ -121,6 +121,20 @@ def test_single_kernel_path_matches_two_phase_path(num_splits):
     compare(o1, l1, o_ref, lse_ref, "single kernel vs oracle")
 
 
+@pytest.mark.parametrize("B,S,num_splits", [(64, 1024, 0), (40, 700, 1)])
+def test_one_split_writes_output_directly(B, S, num_splits):
+    """A plan with one split per (sequence, KV head) and too many of them for one
+    wave of clusters: the split kernel writes o and lse itself (one launch, no
+    merge); empty sequences get O = 0, lse = -inf."""
+    rng = np.random.default_rng(B)
+    seqlens = [0, 1, S] + [int(x) for x in rng.integers(0, S + 1, B - 3)]
+    q, k, v, sl = gqa_synth.decode_inputs(B, 64, 8, S, 128, seed=19, device=DEV, seqlens=seqlens)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert gqa.gqa_attn_decode_plan(B, 8, S, sms, num_splits)[0] == 1
+    assert gqa.gqa_attn_decode_kernel_count(B, 64, 8, S, 128, num_splits) == 1
+    check_full(q, k, v, sl, 1 / math.sqrt(128), num_splits, f"one split, B={B}")
+
+
 def test_two_kernel_path_for_many_splits():
     assert gqa.gqa_attn_decode_kernel_count(1, 64, 8, 32768, 128, 37) == 2
     assert gqa.gqa_attn_decode_kernel_count(1, 8, 1, 256, 128, 4) == 1     # tiny: one cluster

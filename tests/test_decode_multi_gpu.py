@@ -153,3 +153,18 @@ def test_cluster_merge_sizes(num_splits, G, T_q):
     torch.cuda.synchronize()
     o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 1 / math.sqrt(128))
     compare(o, lse, o_ref, lse_ref, f"cluster of {num_splits}, G={G}, T_q={T_q} ({count} kernel)")
+
+
+def test_one_split_multi_token_writes_output_directly():
+    """T_q = 3 new tokens (24 columns per KV head: two column groups) with one
+    split per (sequence, KV head): written by the split kernel itself."""
+    B, S = 64, 512
+    rng = np.random.default_rng(5)
+    seqlens = [0, 2, S] + [int(x) for x in rng.integers(0, S + 1, B - 3)]
+    q, k, v, sl = inputs(B, 64, 8, 3, S, seqlens, 70)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert gqa.gqa_attn_decode_plan(B, 8, S, sms, 0)[0] == 1
+    o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 1 / math.sqrt(128), 0)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, "one split, T_q=3, B=64")
