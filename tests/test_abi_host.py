@@ -461,3 +461,30 @@ def test_device_chunk_ceil_division_is_exact():
             assert np.array_equal(ceil_div(n, d, hi), exact), (d, hi)
             lo = np.nextafter(lo, np.float32(0))
             hi = np.nextafter(hi, np.float32(np.inf))
+
+
+def test_cluster_merge_slots_fit_the_receive_area():
+    """Host restatement of the single-kernel decode's cluster merge: in a cluster
+    of cs CTAs, column n (n < n_cols <= 8) is finalised by CTA n mod cs, which
+    receives it from every CTA c of the cluster into slot c * per_rank + n / cs
+    (per_rank = ceil(n_cols / cs)), with n / cs taken as (n >= cs) + (n >= 2 cs)
+    + (n >= 3 cs).  Every finaliser's slots are distinct and below 16, and its
+    expected byte count (columns it owns x cs senders x (128 + 1) floats)
+    matches what the senders send it."""
+    kRecvSlots, kD = 16, 128
+    for cs in range(2, 17):
+        for n_cols in range(1, 9):
+            per_rank = (n_cols + cs - 1) // cs
+            assert cs * per_rank <= kRecvSlots
+            received = {r: [] for r in range(cs)}
+            for c in range(cs):                       # sender
+                for n in range(n_cols):
+                    quo = (n >= cs) + (n >= 2 * cs) + (n >= 3 * cs)
+                    assert quo == n // cs
+                    dst = n - quo * cs
+                    received[dst].append(c * per_rank + quo)
+            for r in range(cs):
+                n_mine = (n_cols - r + cs - 1) // cs if r < n_cols else 0
+                slots = received[r]
+                assert len(slots) == len(set(slots)) and all(0 <= x < kRecvSlots for x in slots)
+                assert len(slots) * (kD + 1) * 4 == n_mine * cs * (kD + 1) * 4
