@@ -98,10 +98,11 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 //    once, a deep ring per CTA; the kernels shorten the chunks on the device
 //    for sequences shorter than S_max);
 //  * otherwise chunks of at most kMaxChunkTiles tiles so that two waves' worth
-//    of CTAs per SM keep ragged batches balanced; when that asks for at most
-//    two splits and one split fits the chunk cap (units >= SMs), one split,
-//    whose CTA writes the output itself and needs no merge (32 sequences of
-//    2K keys: 45.4 -> 41.5 us; 24 of 2K: 37.0 -> 32.2).
+//    of CTAs per SM keep ragged batches balanced; when the units fill at least
+//    half the SMs, only as many splits as the chunk cap needs (every SM still
+//    gets a CTA; one split writes the output itself, two form one-wave
+//    clusters): 32 sequences of 2K keys 45.4 -> 40.1 us, 16 of 4K 46.0 ->
+//    41.6, 10 of 4K 33.8 -> 27.4, 12 of 3000 28.9 -> 24.5.
 // Splits per (sequence, KV head) of a single-wave plan: one CTA per SM.
 int one_wave_splits(long long units, int num_sms) { return (int)(num_sms / units); }
 
@@ -126,7 +127,8 @@ int plan(int B, int H_kv, int S_max, int num_sms, int num_splits, int *out_split
   } else {
     const long long want = (long long)num_sms * kDecodeCtasPerSm;
     int fill = static_cast<int>((want + units - 1) / units);  // splits per unit
-    if (fill <= 2 && tiles <= kMaxChunkTiles) fill = 1;
+    const int min_fill = ceil_div(tiles, kMaxChunkTiles);  // fewest splits within the cap
+    if (units * 2 >= num_sms && min_fill < fill) fill = min_fill;
     chunk_tiles = ceil_div(tiles, fill < 1 ? 1 : fill);
     if (chunk_tiles > kMaxChunkTiles) chunk_tiles = kMaxChunkTiles;
     if (chunk_tiles < 1) chunk_tiles = 1;
