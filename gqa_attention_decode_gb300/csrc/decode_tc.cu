@@ -61,6 +61,8 @@ struct Params {
   const int32_t *block_table;  // paged cache: [B, max_pages]; nullptr: dense cache
   float *o_part;
   float *lse_part;
+  uint16_t *o;     // the direct-output instantiation: [B, H_q, T_q, d] bf16
+  float *lse;      // the direct-output instantiation: [B, H_q, T_q]
   int B, H_q, H_kv, G, T_q, S_max, num_splits, chunk;
   int page_size, max_pages, num_pages;
   int num_sms;  // SMs the host plan counted on (the device-side chunk rule)
@@ -114,6 +116,10 @@ __device__ __forceinline__ uint64_t desc_mnmajor_base(uint32_t tile) {
 }
 __device__ __forceinline__ constexpr uint32_t mnmajor_step(int kk) { return kk * 2048; }
 
+// kDirect: one split per (sequence, KV head); the CTA writes o (bf16) and lse
+// instead of a partial for the merge (a separate instantiation, so the
+// partial-writing kernel's register allocation is untouched).
+template <bool kDirect>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -222,6 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int key_begin = split * chunk;
   const int key_end = min(key_begin + chunk, seqlen);
   if (key_begin >= key_end) {  // empty split: the merge never reads it (CTA-uniform)
+    if constexpr (kDirect) {  // the whole sequence is empty: O = 0, lse = -inf for its rows
+      const size_t row0 = (size_t)(b * p.H_q + kv * p.G) * p.T_q;
+      const int R = p.G * p.T_q;
+      for (int i = threadIdx.x; i < R * (kD / 8); i += blockDim.x)
+        if (store_ok(row0 + i / (kD / 8), (size_t)p.B * p.H_q * p.T_q, p.wait.status))
+          reinterpret_cast<uint4 *>(p.o + (row0 + i / (kD / 8)) * kD)[i % (kD / 8)] =
+              make_uint4(0u, 0u, 0u, 0u);
+      for (int i = threadIdx.x; i < R; i += blockDim.x)
+        if (store_ok(row0 + i, (size_t)p.B * p.H_q * p.T_q, p.wait.status))
+          p.lse[row0 + i] = -INFINITY;
+    }
     // no copy may still be in flight when the CTA exits
     if (warp == kWarpTma && lane == 0) wait_bar(q_full, 0, p.wait, abort_flag);
     tc::fence_before_sync();
@@ -496,9 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // rows past G * T_q belong to other heads' queries: computed, never stored
       const size_t row0 = (size_t)(b * p.H_q + kv * p.G) * p.T_q;  // the group's first row
       const size_t n_part_rows = (size_t)p.B * p.H_q * p.T_q * p.num_splits;
+      // (one split written directly: the partial row is the output row, o and lse)
       if (s == 0 && row < R && store_ok((row0 + row) * p.num_splits + split, n_part_rows,
                                         p.wait.status))
-        p.lse_part[(row0 + row) * p.num_splits + split] =
+        (kDirect ? p.lse : p.lse_part)[(row0 + row) * p.num_splits + split] =
             L > 0.f ? (mx + fast_log2(L)) * 0.69314718055994531f : -INFINITY;
       // The combined rows go through shared memory so that the global stores are
       // contiguous 256-byte row halves: a thread holds one row, and storing it
@@ -543,9 +561,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = 2 * it + (lane >> 4), k = lane & 15;
         const int r = 32 * wq + i;
         const size_t prow = (row0 + r) * p.num_splits + split;
-        if (r < R && store_ok(prow, n_part_rows, p.wait.status))
-          reinterpret_cast<float4 *>(p.o_part + prow * kD + 64 * s)[k] =
-              *reinterpret_cast<const float4 *>(stage + i * 256 + ((k ^ (i & 7)) * 16));
+        if (r < R && store_ok(prow, n_part_rows, p.wait.status)) {
+          const float4 x = *reinterpret_cast<const float4 *>(stage + i * 256 + ((k ^ (i & 7)) * 16));
+          if constexpr (kDirect) {
+            uint2 pk;
+            pk.x = pack_bf16x2(x.x, x.y);
+            pk.y = pack_bf16x2(x.z, x.w);
+            reinterpret_cast<uint2 *>(p.o + prow * kD + 64 * s)[k] = pk;
+          } else {
+            reinterpret_cast<float4 *>(p.o_part + prow * kD + 64 * s)[k] = x;
+          }
+        }
       }
     }
   }
@@ -575,7 +601,11 @@ CUresult make_map(CUtensorMap *map, const uint16_t *base, long long rows, long l
 }  // namespace decode_tc
 
 cudaError_t decode_tc_prepare_device() {
-  return cudaFuncSetAttribute(decode_tc::decode_tc_kernel,
+  const cudaError_t e = cudaFuncSetAttribute(decode_tc::decode_tc_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             decode_tc::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_tc::decode_tc_kernel<true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, decode_tc::kSmemBytes);
 }
 
@@ -605,6 +635,8 @@ cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   p.l2_prefetch = (long long)a.num_splits * a.H_kv * a.B <= a.num_sms;
   p.o_part = a.o_part;
   p.lse_part = a.lse_part;
+  p.o = a.o;
+  p.lse = a.lse;
   p.B = a.B;
   p.H_q = a.H_q;
   p.H_kv = a.H_kv;
@@ -626,7 +658,9 @@ cudaError_t decode_tc_split_launch(const DecodeLaunch &a, cudaStream_t stream,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, tm_q, tm_k, tm_v, p);
+  if (a.direct_out && a.num_splits == 1)
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<true>, tm_q, tm_k, tm_v, p);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<false>, tm_q, tm_k, tm_v, p);
 }
 
 }  // namespace gqa

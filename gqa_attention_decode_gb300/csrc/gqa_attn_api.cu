@@ -339,10 +339,12 @@ int decode_phase(int phase, const gqa_bf16_t *q, const gqa_bf16_t *k_cache,
   if (phase == kPhaseBoth && !tensor_cores && gqa::decode_fused_eligible(a)) {
     return gqa::decode_fused_launch(a, s, g_encode) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
   }
-  if (phase == kPhaseBoth && !tensor_cores && splits == 1 && S_max > 0) {
+  if (phase == kPhaseBoth && splits == 1 && S_max > 0) {
     // one split per (sequence, KV head): the split kernel writes o and lse itself
     a.direct_out = 1;
-    return gqa::decode_split_launch(a, s, g_encode) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    const cudaError_t e = tensor_cores ? gqa::decode_tc_split_launch(a, s, g_encode)
+                                       : gqa::decode_split_launch(a, s, g_encode);
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
   }
   if (phase & kPhaseSplit) {
     const cudaError_t e = tensor_cores ? gqa::decode_tc_split_launch(a, s, g_encode)

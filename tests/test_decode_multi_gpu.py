@@ -168,3 +168,19 @@ def test_one_split_multi_token_writes_output_directly():
     torch.cuda.synchronize()
     o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 1 / math.sqrt(128))
     compare(o, lse, o_ref, lse_ref, "one split, T_q=3, B=64")
+
+
+def test_one_split_tensor_core_decode_writes_output_directly():
+    """16 new tokens (128 rows per KV head: the tcgen05 kernel) for a batch of
+    32 sequences with one split each: the kernel writes o and lse itself; an
+    empty sequence and ones shorter than T_q included."""
+    B, S, T_q = 32, 1024, 16
+    rng = np.random.default_rng(9)
+    seqlens = [0, 3, S, 16] + [int(x) for x in rng.integers(0, S + 1, B - 4)]
+    q, k, v, sl = inputs(B, 64, 8, T_q, S, seqlens, 80)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert gqa.gqa_attn_decode_plan(B, 8, S, sms, 0)[0] == 1
+    o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 1 / math.sqrt(128), 0)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, "one split, tcgen05, T_q=16, B=32")
