@@ -147,12 +147,28 @@ bool decode_on_tensor_cores(int H_q, int H_kv, int T_q) {
   return G > gqa::kDecodeMaxG || G * T_q > gqa::kDecodeMaxCols;
 }
 
-// plan() plus the tcgen05 kernel's rule that a chunk holds whole 128-key tiles.
+// plan() plus the tcgen05 kernel's rules: a chunk holds whole 128-key tiles, and
+// an automatic multi-wave plan whose (sequence, KV head) units fill at least
+// half the SMs, and at most all of them, takes one split — one wave, the kernel
+// writing o and lse itself: its partials (up to 128 rows per unit) make the
+// merge costly (16 sequences x 4K keys x 16 new tokens: 2 splits 68.2 us, 1
+// split 46.4; 10 x 8K: 4 splits 87.9, 1 split 78.3).
 int plan_decode(int B, int H_q, int H_kv, int T_q, int S_max, int num_sms, int num_splits,
                 int *out_splits, int *out_chunk) {
   int rc = plan(B, H_kv, S_max, num_sms, num_splits, out_splits, out_chunk);
   if (rc != GQA_OK || H_q <= 0 || H_kv <= 0 || !decode_on_tensor_cores(H_q, H_kv, T_q)) return rc;
   const int t = gqa::kDecodeTcTileKeys;
+  const long long units = (long long)B * H_kv;
+  if (num_splits == 0 && S_max > 0 && units <= num_sms && units * 2 >= num_sms) {
+    const int tiles = ceil_div(S_max, gqa::kDecodeTileKeys);
+    const int ows = one_wave_splits(units, num_sms);  // >= 1 here
+    const bool one_wave = ceil_div(tiles, ows) <= kMaxChunkTilesOneWave || ows >= kMinOneWaveSplits;
+    if (!one_wave) {
+      *out_chunk = (S_max + t - 1) / t * t;
+      *out_splits = 1;
+      return GQA_OK;
+    }
+  }
   *out_chunk = (*out_chunk + t - 1) / t * t;
   *out_splits = S_max > 0 ? ceil_div(S_max, *out_chunk) : 1;
   return GQA_OK;
