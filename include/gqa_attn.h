@@ -101,7 +101,10 @@ GQA_API int gqa_attn_abi_version(void);
  * out_num_splits chunks; a sequence that fills its cache uses out_chunk.
  * Short sequences in a long cache are thereby spread over the SMs rather than
  * over the first few splits.  A split whose range is empty does no work and
- * is skipped by the merge.
+ * is skipped by the merge.  This is the plan of the warp-MMA split kernel
+ * (G * T_q <= 32 rows per KV head); the tcgen05 kernel rounds chunks up to 128
+ * keys and, for an automatic plan of several waves whose B*H_kv units fill
+ * half to all of the SMs, takes one split.
  *
  *   B, H_kv, S_max  batch, KV heads, capacity of the KV cache in keys (>= 0)
  *   num_sms         streaming multiprocessors of the target device (> 0)
@@ -142,8 +145,8 @@ GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int H_kv, int S_ma
  *   B, H_q, H_kv, S_max, d   sizes; d must be 128; H_q % H_kv == 0 and
  *             G = H_q / H_kv <= 128.  G <= 8: the G heads fill the 8-wide
  *             dimension of the warp-level MMA; 8 < G <= 128: the tcgen05 split
- *             kernel (one 128-row tensor-core tile per KV head), always split +
- *             merge.
+ *             kernel (one 128-row tensor-core tile per KV head): split +
+ *             merge, or one kernel when the plan has one split.
  *   scale     softmax scale (the record uses 1/sqrt(d)); any finite value.
  *   num_splits 0 = automatic plan, else the requested split count (see
  *             gqa_attn_decode_plan; the plan uses this device's SM count).
