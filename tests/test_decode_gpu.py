@@ -276,3 +276,16 @@ def test_l2_prefetch_sees_the_preceding_grids_writes():
     o_ref, lse_ref = oracle.decode(np64(q), np64(parts[0].view(1, H_kv, S, d)), np64(v),
                                    sl.numpy(), 1 / math.sqrt(d))
     compare(o, lse, o_ref, lse_ref, "decode after a grid writing its K cache")
+
+
+@pytest.mark.parametrize("B,S", [(10, 4096), (12, 3000)])
+def test_plan_of_few_splits(B, S):
+    """Batches whose units fill at least half the SMs take only as many splits as
+    the 2048-key chunk cap needs (two here: one-wave clusters)."""
+    rng = np.random.default_rng(B + 100)
+    seqlens = [0, S] + [int(x) for x in rng.integers(1, S + 1, B - 2)]
+    q, k, v, sl = gqa_synth.decode_inputs(B, 64, 8, S, 128, seed=23, device=DEV, seqlens=seqlens)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    if sms >= 152:
+        assert gqa.gqa_attn_decode_plan(B, 8, S, sms, 0)[0] == 2
+    check_full(q, k, v, sl, 1 / math.sqrt(128), 0, f"few splits B={B} S={S}")

@@ -184,3 +184,17 @@ def test_one_split_tensor_core_decode_writes_output_directly():
     torch.cuda.synchronize()
     o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 1 / math.sqrt(128))
     compare(o, lse, o_ref, lse_ref, "one split, tcgen05, T_q=16, B=32")
+
+
+@pytest.mark.parametrize("B,S,T_q", [(12, 4096, 16), (10, 2500, 9)])
+def test_tensor_core_plan_of_one_split(B, S, T_q):
+    """Batches whose (sequence, KV head) units fill half to all of the SMs, with
+    caches past one wave's chunk limit: the tcgen05 path plans one split and
+    writes o and lse itself (ragged lengths, an empty sequence)."""
+    rng = np.random.default_rng(B)
+    seqlens = [0, S] + [int(x) for x in rng.integers(1, S + 1, B - 2)]
+    q, k, v, sl = inputs(B, 64, 8, T_q, S, seqlens, 90)
+    o, lse = gqa.gqa_attn_decode_multi(q, k, v, sl.to(DEV), 1 / math.sqrt(128), 0)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(np64(q), np64(k), np64(v), sl.numpy(), 1 / math.sqrt(128))
+    compare(o, lse, o_ref, lse_ref, f"tcgen05 one-split plan B={B} S={S} T_q={T_q}")
