@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   }
   // every CTA's receive barrier exists before any CTA of the cluster sends to it
   if (cluster_merge) cluster_sync();
+  int hint_page = 0;  // paged: the page of this split's first key, as the hints give it
   if (warp == n_consumers && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -188,14 +189,21 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
       key_first = split * c;
       const int n = min(key_first + c, len) - key_first;
       tiles = n > 0 ? min(p.l2_prefetch_tiles, (n + kTileKeys - 1) / kTileKeys) : 0;
+    } else {
+      key_first = split * p.chunk;  // the host's chunk: exact for full-length sequences
     }
+    if constexpr (kPaged) hint_page = key_first / p.page_size;
+    int last_page = -1, page_id = -1;  // paged: one table read per page, not per tile
     for (int i = 0; i < tiles; ++i) {
       const int key0 = key_first + i * kTileKeys;
       int c2 = key0, c3 = b * p.H_kv + kv;
       if (kPaged) {
         const int page = key0 / p.page_size;
         if (page >= p.max_pages) break;
-        const int page_id = ld_relaxed_s32(p.block_table + (size_t)b * p.max_pages + page);
+        if (page != last_page) {
+          page_id = ld_relaxed_s32(p.block_table + (size_t)b * p.max_pages + page);
+          last_page = page;
+        }
         if (page_id < 0 || page_id >= p.num_pages) continue;
         c2 = key0 - page * p.page_size;
         c3 = page_id * p.H_kv + kv;
@@ -210,6 +218,17 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
   // with coherent loads (ld.global.ca), never the non-coherent read-only path.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  // Paged: the producer warp loads the 32 block-table entries from the hinted
+  // page on, alongside the length, so the first copy does not wait for two
+  // dependent loads in a row; the entries are read after the wait (only which
+  // window to load came from the hints), and a window that misses the split's
+  // pages is simply loaded again.
+  int page_base = -1 << 30, page_reg = 0;
+  if (kPaged && warp == n_consumers) {
+    page_base = __shfl_sync(0xffffffffu, hint_page, 0);
+    const int idx = page_base + lane;
+    page_reg = idx < p.max_pages ? __ldca(p.block_table + (size_t)b * p.max_pages + idx) : 0;
+  }
   const int seqlen_in = __ldca(p.seqlens + b);
   const int seqlen = min(max(seqlen_in, 0), p.S_max);
   // the chunk for the batch's actual lengths (the host's chunk when they are S_max)
@@ -238,7 +257,6 @@ __global__ void __launch_bounds__(kNT == 1 ? kThreads : kThreadsWide, kMinBlocks
     const uint64_t pol = l2_policy_evict_first();
     const int row = b * p.H_kv + kv;
     int issued = 0;
-    int page_base = -1 << 30, page_reg = 0;
     int page = 0, page_off = 0, page_c3 = 0;  // the tile's page, its first key there, its block
     for (int i = 0; i < n_tiles; ++i) {
       const int key0 = key_begin + i * kTileKeys;

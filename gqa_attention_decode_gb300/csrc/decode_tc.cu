@@ -160,6 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // so a stale value costs one wasted L2 fill; the length gives this split's
   // device-side chunk, and a split that starts past the sequence prefetches
   // nothing; an id outside the pool is skipped.
+  int hint_page = 0;  // paged: the page of this split's first key, as the hints give it
+  if (p.block_table != nullptr && warp == kWarpTma && lane == 0)
+    hint_page = split * p.chunk / p.page_size;  // the host's chunk: exact for full lengths
   if (p.l2_prefetch && warp == kWarpTma && lane == 0 && p.chunk >= kBN) {
     const int len = min(max(ld_relaxed_s32(p.seqlens + b), 0), p.S_max);
     const int key0 =
@@ -168,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool go = key0 < len;
     if (p.block_table != nullptr) {
       const int page = key0 / p.page_size;
+      hint_page = page;
       const int page_id =
           page < p.max_pages ? ld_relaxed_s32(p.block_table + (size_t)b * p.max_pages + page) : -1;
       go = go && page_id >= 0 && page_id < p.num_pages;
@@ -217,6 +221,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int half = 0; half < 2; ++half)
       tma_load_4d(sbase + kOffQ + half * kHalfBytes, &tm_q, q_full, 0, half, q_row0, 0, pol);
   }
+  // Paged: the producer warp loads the 32 block-table entries from the hinted
+  // page on, alongside the length, so the first K/V copy does not wait for two
+  // dependent loads in a row; the entries are read after the wait (only which
+  // window to load came from the hints), and a window that misses the split's
+  // pages is simply loaded again.
+  int page_base = -(1 << 30), page_reg = 0;
+  if (p.block_table != nullptr && warp == kWarpTma) {
+    page_base = __shfl_sync(0xffffffffu, hint_page, 0);
+    const int idx = page_base + lane;
+    page_reg = idx < p.max_pages ? __ldca(p.block_table + (size_t)b * p.max_pages + idx) : 0;
+  }
   const int seqlen_in = __ldca(p.seqlens + b);
   const int seqlen = min(max(seqlen_in, 0), p.S_max);
   // the chunk for the batch's actual lengths (the host's chunk when they are S_max)
@@ -263,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128-key tile never straddles pages: page sizes are multiples of 128).
     int ld = 0;
     bool ok = true;
-    int page_base = -(1 << 30), page_reg = 0;
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int key0 = key_begin + j * kBN;
       int c2 = key0, c3 = b * p.H_kv + kv;  // tensor-map coordinates of the tile's first key
