@@ -1,0 +1,78 @@
+"""Randomized sweep: many more seeded shapes from the parity tests' own generators.
+
+The decode, prefill and paged-prefill parity tests each draw a few dozen shapes
+from seeded generators.  This test keeps drawing from the same generators with
+fresh seeds (GQA_SWEEP_SEED, default 5000, then 5001, ...) and compares every
+case against the oracle, for GQA_SWEEP_SECONDS seconds (10 by default, so the
+GPU suite stays short; a long sweep only needs the variable set).  Per seed:
+16 decode shapes (every decode path, dense and paged, ragged lengths, forced
+split counts), 4 prefill shapes with ragged query tiles, every third seed one
+wide prefill (several rounds of units, key-range pieces, rows past the last
+key), and one paged prefill over a shuffled page pool.  The device status word
+is checked after every seed, so a bounds violation reported by the
+bounds-checked build (GQA_ATTN_LIB set to libgqa_attn_debug.so) fails the
+sweep too.
+"""
+import os
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_attention_decode_gb300 as gqa
+import test_decode_random_gpu as decode_tests
+import test_paged_prefill_gpu as paged_prefill_tests
+import test_prefill_gpu as prefill_tests
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_attention_decode_gb300 import build
+    build.build()
+    gqa.load_library()
+    torch.cuda.set_device(0)
+    yield
+
+
+def _paged_prefill_case(seed):
+    """One paged prefill shape: group sizes for one CTA per unit and for CTA
+    pairs, page sizes of 128 to 512 keys, key counts on and off whole tiles."""
+    rng = np.random.default_rng(seed)
+    G = int(rng.choice([1, 2, 3, 4, 8]))
+    H_kv = int(rng.choice([1, 2]))
+    B = int(rng.integers(1, 3))
+    page = int(rng.choice([128, 256, 512]))
+    T_q = int(rng.integers(1, 600))
+    q_offset = int(rng.integers(0, 2500))
+    S_kv = q_offset + T_q
+    if rng.random() < 0.5:
+        S_kv = -(-S_kv // 128) * 128  # whole key tiles: the CTA-pair kernel reads pages
+    return (B, G * H_kv, H_kv, T_q, S_kv, q_offset, page)
+
+
+def test_random_sweep():
+    budget = float(os.environ.get("GQA_SWEEP_SECONDS", "10"))
+    t0 = time.time()
+    seed = first = int(os.environ.get("GQA_SWEEP_SEED", "5000"))
+    counts = dict(decode=0, prefill=0, wide=0, paged=0)
+    while True:
+        for c in decode_tests._cases(16, seed):
+            decode_tests.test_random_decode_shapes(*c)
+            counts["decode"] += 1
+        for c in prefill_tests._seeded_configs(4, seed):
+            prefill_tests.test_seeded_random_shapes(*c)
+            counts["prefill"] += 1
+        if seed % 3 == 0:
+            for c in prefill_tests._seeded_wide_configs(1, seed):
+                prefill_tests.test_seeded_random_shapes_wide(*c)
+                counts["wide"] += 1
+        paged_prefill_tests.test_paged_prefill_against_oracle(*_paged_prefill_case(seed))
+        counts["paged"] += 1
+        assert gqa.gqa_attn_device_status() == gqa.GQA_OK, f"device status after seed {seed}"
+        seed += 1
+        if time.time() - t0 >= budget:
+            break
+    print(f"random sweep: seeds {first}..{seed - 1}, cases {counts}")
