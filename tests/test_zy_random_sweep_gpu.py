@@ -11,7 +11,9 @@ wide prefill (several rounds of units, key-range pieces, rows past the last
 key), and one paged prefill over a shuffled page pool.  The device status word
 is checked after every seed, so a bounds violation reported by the
 bounds-checked build (GQA_ATTN_LIB set to libgqa_attn_debug.so) fails the
-sweep too.
+sweep too.  A second sweep (GQA_SWEEP_LARGE_SECONDS) draws larger decode
+problems — batches up to 24, caches up to 64K keys, up to 2M cached rows —
+which reach the planner's multi-wave, few-split, one-split and cluster plans.
 """
 import os
 import time
@@ -76,3 +78,44 @@ def test_random_sweep():
         if time.time() - t0 >= budget:
             break
     print(f"random sweep: seeds {first}..{seed - 1}, cases {counts}")
+
+
+def _large_decode_case(seed):
+    """A decode problem large enough for multi-wave plans: (G, H_kv, T_q, B,
+    S_max, seqlens, splits, page) as the decode parity test takes them, with at
+    most 2M cached rows and 2^27 (row, key) pairs for the oracle."""
+    rng = np.random.default_rng(seed)
+    G = int(rng.choice([1, 2, 4, 5, 8, 16]))
+    H_kv = int(rng.choice([1, 2, 4, 8])) if G <= 8 else int(rng.choice([1, 2, 4]))
+    T_q = int(rng.integers(1, max(1, min(16, 128 // G)) + 1))
+    B = int(rng.integers(1, 25))
+    tensor_cores = G > 8 or G * T_q > 32
+    paged = bool(rng.random() < 0.4)
+    page = (int(rng.choice([128, 256])) if tensor_cores else int(rng.choice([64, 128, 256]))) if paged else 0
+    unit = page or 64
+    cap = min((1 << 21) // (B * H_kv), (1 << 27) // (B * H_kv * G * T_q))
+    S_max = int(rng.integers(1, 65536 // unit + 1)) * unit
+    S_max = max(unit, min(S_max, cap // unit * unit))
+    kind = rng.random()
+    if kind < 0.4:
+        seqlens = [S_max] * B                                    # every sequence full
+    elif kind < 0.8:
+        seqlens = [int(x) for x in rng.integers(0, S_max + 1, B)]  # ragged
+    else:
+        seqlens = [int(x) for x in rng.integers(0, min(S_max, 600) + 1, B)]  # short in a long cache
+    splits = int(rng.choice([0, 0, 0, 1, 2, 7, 33]))
+    return (G, H_kv, T_q, B, S_max, tuple(seqlens), splits, page)
+
+
+def test_random_sweep_large_decode():
+    budget = float(os.environ.get("GQA_SWEEP_LARGE_SECONDS", "10"))
+    t0 = time.time()
+    seed = first = int(os.environ.get("GQA_SWEEP_SEED", "5000"))
+    while True:
+        decode_tests.test_random_decode_shapes(*_large_decode_case(seed))
+        assert gqa.gqa_attn_device_status() == gqa.GQA_OK, f"device status after seed {seed}"
+        seed += 1
+        torch.cuda.empty_cache()
+        if time.time() - t0 >= budget:
+            break
+    print(f"large decode sweep: seeds {first}..{seed - 1}")
