@@ -14,6 +14,9 @@ bounds-checked build (GQA_ATTN_LIB set to libgqa_attn_debug.so) fails the
 sweep too.  A second sweep (GQA_SWEEP_LARGE_SECONDS) draws larger decode
 problems — batches up to 24, caches up to 64K keys, up to 2M cached rows —
 which reach the planner's multi-wave, few-split, one-split and cluster plans.
+A third (GQA_SWEEP_PREFILL_SECONDS) runs causal prefills up to 8K query rows
+after up to 32K keys, dense or paged, and checks sampled rows (tile edges and
+random ones) against the oracle and every output for finiteness.
 """
 import os
 import time
@@ -22,10 +25,13 @@ import numpy as np
 import pytest
 import torch
 
+import gqa_synth
 import gqa_attention_decode_gb300 as gqa
+import oracle
 import test_decode_random_gpu as decode_tests
 import test_paged_prefill_gpu as paged_prefill_tests
 import test_prefill_gpu as prefill_tests
+from parity import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -119,3 +125,71 @@ def test_random_sweep_large_decode():
         if time.time() - t0 >= budget:
             break
     print(f"large decode sweep: seeds {first}..{seed - 1}")
+
+
+def _large_prefill_case(seed):
+    """(B, H_q, H_kv, T_q, S_kv, q_offset, page): up to 8K query rows after up to
+    32K keys, at most 2^22 query rows and 2^21 cached rows in all; sometimes
+    rows past the last key; page 0 for a dense cache."""
+    rng = np.random.default_rng(seed)
+    G = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+    H_kv = int(rng.choice([1, 2, 4, 8]))
+    B = int(rng.integers(1, 5))
+    T_q = int(rng.integers(1, 8193))
+    T_q = max(1, min(T_q, (1 << 22) // (B * G * H_kv)))
+    q_offset = int(rng.integers(0, 32769 - T_q)) if rng.random() < 0.7 else 0
+    S_kv = q_offset + T_q
+    if rng.random() < 0.2:
+        S_kv = max(1, S_kv - int(rng.integers(0, min(T_q, 300) + 1)))  # rows past the last key
+    if B * H_kv * S_kv > (1 << 21):
+        return _large_prefill_case(seed + 100000)
+    page = 0
+    if rng.random() < 0.3 and q_offset + T_q <= S_kv:
+        page = int(rng.choice([128, 256, 512]))
+        if rng.random() < 0.5:
+            S_kv = -(-S_kv // 128) * 128  # whole key tiles: the CTA-pair kernel reads pages
+    return (B, G * H_kv, H_kv, T_q, S_kv, q_offset, page)
+
+
+def test_random_sweep_large_prefill():
+    budget = float(os.environ.get("GQA_SWEEP_PREFILL_SECONDS", "10"))
+    t0 = time.time()
+    seed = first = int(os.environ.get("GQA_SWEEP_SEED", "5000"))
+    dev = torch.device("cuda", 0)
+    scale = 0.088
+    while True:
+        B, H_q, H_kv, T_q, S_kv, q_offset, page = _large_prefill_case(seed)
+        G = H_q // H_kv
+        q, k, v = gqa_synth.prefill_inputs(B, H_q, H_kv, T_q, S_kv, 128, seed=seed, device=dev)
+        if page:
+            kp, vp, table = paged_prefill_tests.to_pages(k, v, page, extra_pages=1, seed=seed)
+            o, lse = gqa.gqa_attn_prefill_causal_paged(q, kp, vp, table, S_kv, scale, q_offset)
+            del kp, vp
+        else:
+            o, lse = gqa.gqa_attn_prefill_causal(q, k, v, scale, q_offset)
+        torch.cuda.synchronize()
+        what = f"seed {seed}: B={B} H_q={H_q} H_kv={H_kv} T_q={T_q} S_kv={S_kv} q_offset={q_offset} page={page}"
+        assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all(), what
+        rng = np.random.default_rng(seed)
+        edges = {0, T_q - 1} | {min(T_q - 1, t) for t in (127, 128, 255, 256)}
+        rows = sorted(edges | set(int(x) for x in rng.integers(0, T_q, 40)))
+        picks = [(int(rng.integers(0, B)), int(rng.integers(0, H_q)), i) for i in rows]
+        qs = q[[b for b, _, _ in picks], [h for _, h, _ in picks], rows]
+        ref_o = np.zeros((len(picks), 128))
+        ref_lse = np.zeros(len(picks))
+        for r, (b, h, i) in enumerate(picks):
+            n = min(q_offset + i + 1, S_kv)
+            ro, rl = oracle.attend_rows(qs[r:r + 1].float().cpu().numpy().astype(np.float64),
+                                        k[b, h // G, :n].float().cpu().numpy().astype(np.float64),
+                                        v[b, h // G, :n].float().cpu().numpy().astype(np.float64),
+                                        scale, [n])
+            ref_o[r], ref_lse[r] = ro[0], rl[0]
+        compare(torch.stack([o[b, h, i] for b, h, i in picks]),
+                torch.stack([lse[b, h, i] for b, h, i in picks]), ref_o, ref_lse, what)
+        del q, k, v, o, lse
+        assert gqa.gqa_attn_device_status() == gqa.GQA_OK, f"device status after seed {seed}"
+        seed += 1
+        torch.cuda.empty_cache()
+        if time.time() - t0 >= budget:
+            break
+    print(f"large prefill sweep: seeds {first}..{seed - 1}")
