@@ -8,7 +8,8 @@ GPU suite stays short; a long sweep only needs the variable set).  Per seed:
 16 decode shapes (every decode path, dense and paged, ragged lengths, forced
 split counts), 4 prefill shapes with ragged query tiles, every third seed one
 wide prefill (several rounds of units, key-range pieces, rows past the last
-key), and one paged prefill over a shuffled page pool.  The device status word
+key), one paged prefill over a shuffled page pool, and one merge of random
+attention states (1 to 70 shards, some empty).  The device status word
 is checked after every seed, so a bounds violation reported by the
 bounds-checked build (GQA_ATTN_LIB set to libgqa_attn_debug.so) fails the
 sweep too.  A second sweep (GQA_SWEEP_LARGE_SECONDS) draws larger decode
@@ -61,11 +62,40 @@ def _paged_prefill_case(seed):
     return (B, G * H_kv, H_kv, T_q, S_kv, q_offset, page)
 
 
+def _merge_states_case(seed):
+    """Random shard states: n_parts 1..70, rows 0..3000, lse spread over +-18,
+    whole shards, single entries and whole rows with no visible key (-inf);
+    against the oracle's merge within the bf16 rounding of O."""
+    rng = np.random.default_rng(seed)
+    P = int(rng.integers(1, 71))
+    rows = int(rng.integers(0, 3001))
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    o_parts = torch.randn((P, rows, 128), generator=g).to(torch.bfloat16)
+    lse_parts = (torch.randn((P, rows), generator=g) * 6.0).float()
+    if rows:
+        lse_parts[torch.rand((P, rows), generator=g) < 0.2] = float("-inf")
+        lse_parts[int(rng.integers(0, P))] = float("-inf")       # an empty shard
+        lse_parts[:, int(rng.integers(0, rows))] = float("-inf")  # a row empty everywhere
+    dev = torch.device("cuda", 0)
+    o, lse = gqa.gqa_attn_merge_states(o_parts.to(dev), lse_parts.to(dev))
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.merge_states(o_parts.double().numpy(), lse_parts.double().numpy())
+    if rows == 0:
+        return
+    err = np.abs(o.double().cpu().numpy() - o_ref)
+    assert err.max() <= 2.0 ** -7 * max(1.0, np.abs(o_ref).max()), f"merge seed {seed}"
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse.cpu().numpy()), fin), f"merge seed {seed}"
+    if fin.any():
+        assert np.abs(lse.cpu().numpy()[fin] - lse_ref[fin]).max() <= 1e-5, f"merge seed {seed}"
+    assert torch.all(o[torch.from_numpy(~fin).to(o.device)] == 0), f"merge seed {seed}"
+
+
 def test_random_sweep():
     budget = float(os.environ.get("GQA_SWEEP_SECONDS", "10"))
     t0 = time.time()
     seed = first = int(os.environ.get("GQA_SWEEP_SEED", "5000"))
-    counts = dict(decode=0, prefill=0, wide=0, paged=0)
+    counts = dict(decode=0, prefill=0, wide=0, paged=0, merge=0)
     while True:
         for c in decode_tests._cases(16, seed):
             decode_tests.test_random_decode_shapes(*c)
@@ -79,6 +109,8 @@ def test_random_sweep():
                 counts["wide"] += 1
         paged_prefill_tests.test_paged_prefill_against_oracle(*_paged_prefill_case(seed))
         counts["paged"] += 1
+        _merge_states_case(seed)
+        counts["merge"] += 1
         assert gqa.gqa_attn_device_status() == gqa.GQA_OK, f"device status after seed {seed}"
         seed += 1
         if time.time() - t0 >= budget:
