@@ -3,21 +3,24 @@
 The decode, prefill and paged-prefill parity tests each draw a few dozen shapes
 from seeded generators.  This test keeps drawing from the same generators with
 fresh seeds (GQA_SWEEP_SEED, default 5000, then 5001, ...) and compares every
-case against the oracle, for GQA_SWEEP_SECONDS seconds (10 by default, so the
-GPU suite stays short; a long sweep only needs the variable set).  Per seed:
-16 decode shapes (every decode path, dense and paged, ragged lengths, forced
-split counts), 4 prefill shapes with ragged query tiles, every third seed one
-wide prefill (several rounds of units, key-range pieces, rows past the last
-key), one paged prefill over a shuffled page pool, and one merge of random
-attention states (1 to 70 shards, some empty).  The device status word
-is checked after every seed, so a bounds violation reported by the
-bounds-checked build (GQA_ATTN_LIB set to libgqa_attn_debug.so) fails the
-sweep too.  A second sweep (GQA_SWEEP_LARGE_SECONDS) draws larger decode
+case against the oracle: a fixed number of seeds by default (so the GPU suite
+is short and always runs the same cases), or for GQA_SWEEP_SECONDS seconds
+when that is set (a long sweep only needs the variable).  Per seed: 16 decode
+shapes (every decode path, dense and paged, ragged lengths, forced split
+counts), 4 prefill shapes with ragged query tiles, every third seed one wide
+prefill (several rounds of units, key-range pieces, rows past the last key),
+one paged prefill over a shuffled page pool, and one merge of random attention
+states (1 to 70 shards, some empty).  The device status word is checked after
+every seed, so a bounds violation reported by the bounds-checked build
+(GQA_ATTN_LIB set to libgqa_attn_debug.so) fails the sweep too.
+
+A second sweep (20 seeds, or GQA_SWEEP_LARGE_SECONDS) draws larger decode
 problems — batches up to 24, caches up to 64K keys, up to 2M cached rows —
 which reach the planner's multi-wave, few-split, one-split and cluster plans.
-A third (GQA_SWEEP_PREFILL_SECONDS) runs causal prefills up to 8K query rows
-after up to 32K keys, dense or paged, and checks sampled rows (tile edges and
-random ones) against the oracle and every output for finiteness.
+A third (100 seeds, or GQA_SWEEP_PREFILL_SECONDS) runs causal prefills of up to
+8K query rows after up to 32K keys, dense or paged, and checks sampled rows
+(tile edges and random ones) against the oracle and every output for
+finiteness.
 """
 import os
 import time
@@ -91,8 +94,21 @@ def _merge_states_case(seed):
     assert torch.all(o[torch.from_numpy(~fin).to(o.device)] == 0), f"merge seed {seed}"
 
 
+def _sweep_limits(var, default_seeds):
+    """(seconds, seeds): a time budget when the variable is set, else a seed count."""
+    if os.environ.get(var):
+        return float(os.environ[var]), None
+    return None, default_seeds
+
+
+def _done(t0, budget, seed, first, n_seeds):
+    if n_seeds is not None:
+        return seed - first >= n_seeds
+    return time.time() - t0 >= budget
+
+
 def test_random_sweep():
-    budget = float(os.environ.get("GQA_SWEEP_SECONDS", "10"))
+    budget, n_seeds = _sweep_limits("GQA_SWEEP_SECONDS", 12)
     t0 = time.time()
     seed = first = int(os.environ.get("GQA_SWEEP_SEED", "5000"))
     counts = dict(decode=0, prefill=0, wide=0, paged=0, merge=0)
@@ -113,7 +129,7 @@ def test_random_sweep():
         counts["merge"] += 1
         assert gqa.gqa_attn_device_status() == gqa.GQA_OK, f"device status after seed {seed}"
         seed += 1
-        if time.time() - t0 >= budget:
+        if _done(t0, budget, seed, first, n_seeds):
             break
     print(f"random sweep: seeds {first}..{seed - 1}, cases {counts}")
 
@@ -146,7 +162,7 @@ def _large_decode_case(seed):
 
 
 def test_random_sweep_large_decode():
-    budget = float(os.environ.get("GQA_SWEEP_LARGE_SECONDS", "10"))
+    budget, n_seeds = _sweep_limits("GQA_SWEEP_LARGE_SECONDS", 20)
     t0 = time.time()
     seed = first = int(os.environ.get("GQA_SWEEP_SEED", "5000"))
     while True:
@@ -154,7 +170,7 @@ def test_random_sweep_large_decode():
         assert gqa.gqa_attn_device_status() == gqa.GQA_OK, f"device status after seed {seed}"
         seed += 1
         torch.cuda.empty_cache()
-        if time.time() - t0 >= budget:
+        if _done(t0, budget, seed, first, n_seeds):
             break
     print(f"large decode sweep: seeds {first}..{seed - 1}")
 
@@ -184,7 +200,7 @@ def _large_prefill_case(seed):
 
 
 def test_random_sweep_large_prefill():
-    budget = float(os.environ.get("GQA_SWEEP_PREFILL_SECONDS", "10"))
+    budget, n_seeds = _sweep_limits("GQA_SWEEP_PREFILL_SECONDS", 100)
     t0 = time.time()
     seed = first = int(os.environ.get("GQA_SWEEP_SEED", "5000"))
     dev = torch.device("cuda", 0)
@@ -222,6 +238,6 @@ def test_random_sweep_large_prefill():
         assert gqa.gqa_attn_device_status() == gqa.GQA_OK, f"device status after seed {seed}"
         seed += 1
         torch.cuda.empty_cache()
-        if time.time() - t0 >= budget:
+        if _done(t0, budget, seed, first, n_seeds):
             break
     print(f"large prefill sweep: seeds {first}..{seed - 1}")
